@@ -1,0 +1,419 @@
+"""Benchmark of the SCAPE sharded optimizer step on GB300.
+
+One step = the whole hot path over one batch of synthetic per-worker gradients:
+scape_step (error-feedback compaction, ordered sparse reduce, sparse AdamS)
+plus scape_refresh_mask (the partitioned top-k that the next step uses).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload llama500m]
+    python bench.py --impl reference ...     # the CPU oracle, same metric
+
+Rank 0 prints one JSON line.  With N > 1 (torchrun) every rank runs its own
+independent problem of the same shape (optimizer shards are independent), no
+data-path collective runs, and the value is the sum over ranks of the
+parameters stepped divided by the slowest rank's time (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "SCAPE optimizer-step params/s and achieved HBM GB/s (% of GB300 peak)"
+UNIT = "params/s"
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+# --------------------------------------------------------------------- helpers
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _grad_bytes(wl):
+    return 2 if wl.grad_dtype == "bf16" else 4
+
+
+def algorithmic_bytes(wl, k):
+    """Bytes the method must move per step, by kernel (see the design notes)."""
+    P, W, G = wl.P, wl.W, _grad_bytes(wl)
+    ntiles = (P + 2047) // 2048
+    ef = W * P * (G + 8) + P / 8 + 4 * ntiles + 4 * k * W
+    red = 4 * k * W + 4 * k
+    upd = 24 * k
+    refresh = 4 * P + P / 8 + P / 8 + 4 * k
+    return {"ef_compact": ef, "reduce": red, "adams_sparse": upd, "refresh": refresh,
+            "total": ef + red + upd + refresh}
+
+
+def _kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("step_kernels.cu", "scape_internal.cuh"):
+        with open(os.path.join(ROOT, "sparse_communication_sharded_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _ncu_traffic(workload):
+    """DRAM bytes per ef_compact launch from the committed ncu summary, if it
+    was taken on the current kernel source; else None."""
+    p = os.path.join(PROFILES, f"ef_compact_{workload}.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("kernel_source_sha256_16") != _kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        if self.path and os.path.exists(self.path):
+            with open(self.path) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) >= 9 and parts[0] == str(self.gpu_index):
+                        rows.append(parts)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+def _mem_available():
+    """Host MemAvailable in bytes (0 if unknown)."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# --------------------------------------------------------------------- oracle sample
+def run_oracle_sample(wl, steps, seed=0, device=None):
+    """Time the CPU oracle (single thread) on one optimizer shard of the
+    workload: a dense first step (untimed), then `steps` lagged sparse steps
+    with their mask refreshes (timed).  Gradients are drawn on `device` (GPU if
+    given) and copied to host memory.  Returns (params/s, seconds, n_shard)."""
+    import numpy as np
+    import torch
+
+    from oracle import oracle as O
+    from sparse_communication_sharded_gb300 import synth
+
+    start, ks = O.layout(wl.P, wl.W, wl.sparsity)
+    sh = wl.W // 2
+    lo, hi = int(start[sh]), int(start[sh + 1])
+    n = hi - lo
+    gdev = device if device is not None else "cpu"
+    gen = synth.GradientStream(wl, seed=seed, device=gdev, P=n, offset=lo)
+    w0 = synth.init_params(n, seed=seed, device=gdev).cpu().numpy()
+    st = O.new_state(w0, wl.W, wl.sparsity, O.Hyper(),
+                     shard_start=np.array([0, n], np.int64), shard_k=np.array([ks[sh]], np.int64))
+    bufs = gen.alloc()
+
+    def host_grads():
+        gen.next_into(bufs)
+        return [synth.to_numpy_grad(b) for b in bufs]
+
+    O.advance(st, host_grads(), keep=())          # dense first step, untimed
+    total = 0.0
+    for _ in range(steps):
+        g = host_grads()
+        t0 = time.perf_counter()
+        O.advance(st, g, keep=())
+        total += time.perf_counter() - t0
+    del bufs
+    if device is not None:
+        torch.cuda.empty_cache()
+    return n * steps / total, total, n
+
+
+# --------------------------------------------------------------------- reference arm
+def bench_reference(args, wl):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    import torch
+    dev = torch.device("cuda:0") if torch.cuda.is_available() else None
+    steps = max(1, args.steps)
+    rate, secs, n = run_oracle_sample(wl, steps, device=dev)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": ws,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": 1000.0 * secs / steps * wl.P / n,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "P": wl.P, "W": wl.W, "sparsity": wl.sparsity,
+                   "grad_dtype": wl.grad_dtype},
+        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"one optimizer shard ({n} params x {wl.W} workers), "
+                                   f"{steps} lagged sparse steps + refreshes after an untimed "
+                                   f"dense step; ms_per_step scaled to the full P"},
+        "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------- GPU arm
+def bench_gpu(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    import sparse_communication_sharded_gb300 as pkg
+    from sparse_communication_sharded_gb300 import synth
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    torch.cuda.set_device(local)
+    dev = torch.device(f"cuda:{local}")
+    pkg.load()
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+
+    P, W = wl.P, wl.W
+    gdt = torch.bfloat16 if wl.grad_dtype == "bf16" else torch.float32
+    seed = 1000 * rank
+    params = synth.init_params(P, seed=seed, device=dev)
+    opt = pkg.Scape(params, W, wl.sparsity, layer_numel=[n for _, n in wl.layers],
+                    grad_dtype=gdt)
+    gen = synth.GradientStream(wl, seed=seed, device=dev)
+    grads = gen.alloc()
+
+    # warm-up: the dense first step and W - 1 lagged steps
+    for _ in range(args.warmup):
+        gen.next_into(grads)
+        opt.step(grads)
+        opt.refresh_mask()
+    torch.cuda.synchronize()
+
+    # timed steps: fresh gradients each step (outside the timed window),
+    # inputs (~115 GB for llama500m) far larger than the 129 MB L2
+    opt.profile(True)
+    opt.profile_reset()
+    n_launch0 = opt.launch_count()
+    step_ms, wall = [], []
+    st = torch.cuda.current_stream()
+    with ClockSampler(local) as clk:
+        for _ in range(args.steps):
+            gen.next_into(grads)
+            barrier()
+            torch.cuda.synchronize()
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0 = time.perf_counter()
+            ev0.record(st)
+            opt.step(grads)
+            opt.refresh_mask()
+            ev1.record(st)
+            torch.cuda.synchronize()
+            wall.append(time.perf_counter() - t0)
+            barrier()
+            step_ms.append(ev0.elapsed_time(ev1))
+    launches = opt.launch_count() - n_launch0
+    opt.profile_collect()
+    prof = opt.profile_read()
+    opt.profile(False)
+    clocks = clk.summary()
+
+    my_ms = sum(step_ms) / len(step_ms)
+    t_max = my_ms
+    if ws > 1:
+        tt = torch.tensor([my_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_max = float(tt.item())
+    value = ws * P / (t_max / 1000.0)
+    alg = algorithmic_bytes(wl, opt.k)
+    peak, peak_kind = _peaks()
+
+    ef_ms, ef_n = prof["ef_compact"]
+    ef_avg = ef_ms / max(ef_n, 1)
+    ef_gbs = alg["ef_compact"] / (ef_avg / 1000.0) / 1e9
+    traffic = _ncu_traffic(wl.name)
+    kernels = {}
+    for name, (ms, n) in prof.items():
+        if n:
+            kernels[name] = {"launches": n, "ms_per_step": ms / args.steps,
+                             "share": ms / max(sum(m for m, _ in prof.values()), 1e-9)}
+    refresh_ms = sum(prof[k][0] for k in ("radix_hist0", "radix_hist1", "radix_hist2",
+                                          "radix_select", "tie_count", "tie_select", "mark",
+                                          "scan", "index")) / args.steps
+
+    # end to end through the C ABI from pinned host memory
+    e2e = None
+    if args.e2e_steps > 0:
+        e2e = bench_e2e(opt, wl, grads, args.e2e_steps, dev)
+
+    cpu = None
+    if rank == 0 and ws == 1 and args.cpu_steps > 0:
+        rate, secs, n = run_oracle_sample(wl, args.cpu_steps, device=dev)
+        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"one optimizer shard ({n} of {P} params, {W} workers), "
+                         f"{args.cpu_steps} lagged sparse steps + refreshes after an untimed "
+                         f"dense step, single-threaded C, {secs:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t_max, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": wl.name, "P": P, "W": W, "sparsity": wl.sparsity,
+                       "k": opt.k, "grad_dtype": wl.grad_dtype, "state_dtype": "f32",
+                       "l2": "inputs larger than L2 (gradients + residuals resident in HBM)",
+                       "parallelism": f"{ws} independent problems (weak)"},
+            "hbm_gbs": alg["total"] / (t_max / 1000.0) / 1e9,
+            "hbm_frac": alg["total"] / (t_max / 1000.0) / 1e9 / peak,
+            "alg_bytes_per_step": alg["total"],
+            "roofline": {"kernel": "ef_compact", "bound": "hbm", "achieved": ef_gbs,
+                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": ef_gbs / peak, "traffic": traffic,
+                         "alg_bytes_per_launch": alg["ef_compact"], "ms_per_launch": ef_avg},
+            "kernels": kernels,
+            "refresh_ms_per_step": refresh_ms,
+            "wall_ms_per_step": 1000.0 * sum(wall) / len(wall),
+            "gpu_launches": launches,
+            "clocks": clocks,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    opt.close()
+    return 0
+
+
+def bench_e2e(opt, wl, dev_grads, steps, dev):
+    """Same step through scape_step_host: per step the W gradients are copied
+    from pinned host memory, the step and refresh run, and w[P] is copied back."""
+    import torch
+
+    P, W = wl.P, wl.W
+    gdt = dev_grads[0].dtype
+    esz = dev_grads[0].element_size()
+    need = W * P * esz + 4 * P
+    if _mem_available() > 3 * need:
+        host = [torch.empty(P, dtype=gdt).pin_memory() for _ in range(W)]
+        shared = False
+    else:
+        # too little host memory for W distinct pinned buffers: one pinned
+        # buffer is the source of every worker (the same bytes are copied)
+        host = [torch.empty(P, dtype=gdt).pin_memory()] * W
+        shared = True
+    for h_, d in zip(host, dev_grads):
+        h_.copy_(d)
+    out = torch.empty(P, dtype=torch.float32).pin_memory()
+    st = torch.cuda.current_stream()
+    times = []
+    for _ in range(steps):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        opt.step_host(host, dev_grads, out)
+        st.synchronize()
+        times.append(time.perf_counter() - t0)
+    secs = sum(times) / len(times)
+    del host
+    return {"value": P / secs, "unit": UNIT, "h2d_bytes_per_step": W * P * esz,
+            "d2h_bytes_per_step": 4 * P, "ms_per_step": 1000 * secs,
+            "shared_host_source": shared}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="llama500m")
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-steps", type=int, default=2)
+    ap.add_argument("--P", type=int, default=None,
+                    help="with --workload custom: flat parameter count")
+    ap.add_argument("--workers", type=int, default=8, help="with --workload custom: W")
+    ap.add_argument("--sparsity", type=float, default=0.99, help="with --workload custom")
+    ap.add_argument("--grad-dtype", default="bf16", choices=["bf16", "f32"],
+                    help="with --workload custom")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    from sparse_communication_sharded_gb300 import synth
+    if args.workload == "custom":
+        if not args.P:
+            ap.error("--workload custom needs --P")
+        wl = synth.Workload(f"custom_p{args.P}_w{args.workers}_s{args.sparsity}",
+                            (("flat", args.P),), W=args.workers, sparsity=args.sparsity,
+                            steps=args.steps, grad_dtype=args.grad_dtype)
+    else:
+        wl = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return bench_reference(args, wl)
+    return bench_gpu(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

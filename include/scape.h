@@ -1,0 +1,219 @@
+/*
+ * scape.h -- C ABI of the SCAPE sharded sparse optimizer step on one GB300 (sm_103a).
+ *
+ * SCAPE ("SCAPE: Accurate and Efficient LLM Training with Extremely Sparse
+ * Communication", arXiv 2607.01678) is a momentum-masked, error-feedback,
+ * extreme-sparsity AdamS optimizer for sharded data parallelism.  This library
+ * runs its per-step update for W data-parallel workers held as W gradient
+ * slices on one GPU, so the cross-worker sparse reduce is an on-device sum and
+ * no collective runs.
+ *
+ * Citations below name the paper ("SCAPE", Chinese translation page, sections
+ * I and II-A..II-C) and the technical summary ("Sintesi Tecnica: SCAPE",
+ * gist.science, Sec. 2 "Metodologia").
+ *
+ * Conventions for every entry point
+ *   - Return value: SCAPE_OK (0) or a negative scape_status.  Nothing throws
+ *     across the ABI.  scape_last_error() returns a message for the last
+ *     failure on a handle (or, with a NULL handle, for the last failed
+ *     scape_create on the calling thread).
+ *   - Pointers are device pointers unless the name starts with host_.
+ *   - The caller owns every device buffer (parameters, first moment, residuals,
+ *     gradients, workspace).  The library keeps non-owning pointers and small
+ *     host metadata only; it never allocates device memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     All GPU work is enqueued asynchronously on it; a non-zero status reports
+ *     argument, state or launch errors only.  Faults of enqueued work surface
+ *     at the caller's next synchronisation.
+ *   - A handle is not thread-safe: one thread at a time per handle.
+ *
+ * Layout
+ *   P = sum of the layer sizes; parameters are one flat float32 vector w[P]
+ *   (layers concatenated in the order given).  Optimizer shard s of W covers
+ *   [floor(s*P/W), floor((s+1)*P/W)) ("SCAPE" Sec. II-A: the distributed
+ *   optimizer partitions states and parameters evenly over the workers), and
+ *   keeps k_s = ceil(n_s * (1 - sparsity)) coordinates (sparsity rounded to
+ *   parts per million); k = sum k_s is fixed for the life of the handle.
+ *   The global mask is a bitmap, bit (i % 32) of 32-bit word i / 32 set when
+ *   parameter i is selected; bits past P in the last word are zero.
+ */
+#ifndef SCAPE_H
+#define SCAPE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct scape scape_t;
+
+enum scape_status {
+    SCAPE_OK = 0,
+    SCAPE_EINVAL = -1, /* bad argument: null/misaligned pointer, size, range */
+    SCAPE_ECUDA = -2,  /* a CUDA runtime call or kernel launch failed */
+    SCAPE_ESTATE = -4  /* call out of order (e.g. step before bind) */
+};
+
+enum scape_dtype {
+    SCAPE_F32 = 0, /* gradients are float32 */
+    SCAPE_BF16 = 1 /* gradients are bfloat16 */
+};
+
+/* Upper bound on W (simulated workers = optimizer shards). */
+#define SCAPE_MAX_WORKERS 256
+
+/*
+ * Create a handle.  Host only: validates the arguments and computes the shard
+ * layout and k; no GPU work.
+ *   host_layer_numel  n_layers sizes (each >= 0, sum P in [1, 2^31 - 1])
+ *   W                 workers = optimizer shards, 1..SCAPE_MAX_WORKERS
+ *   sparsity          fraction of coordinates NOT sent per shard, in [0, 1)
+ *                     (90% and 99% in "SCAPE" abstract)
+ *   beta1, beta2      AdamS coefficients in [0, 1) ("SCAPE" Sec. II-C, Eq. 2)
+ *   lr                learning rate eta; eps > 0; weight_decay lambda >= 0
+ *   grad_dtype        SCAPE_F32 or SCAPE_BF16
+ * On success *out owns host memory only; release it with scape_destroy().
+ */
+int scape_create(scape_t **out, int n_layers, const int64_t *host_layer_numel, int W,
+                 double sparsity, float beta1, float beta2, float lr, float eps,
+                 float weight_decay, int grad_dtype);
+
+/* Release a handle (NULL is a no-op).  Does not free caller-owned memory. */
+void scape_destroy(scape_t *h);
+
+/* Message for the last failure (never NULL; "" when none). */
+const char *scape_last_error(const scape_t *h);
+
+/*
+ * Geometry of a handle: P, W, k and, when the host_ arrays are non-NULL, the
+ * W + 1 shard boundaries and the W per-shard k_s (partitioned mask: each
+ * worker selects only within its own optimizer shard, "Sintesi Tecnica:
+ * SCAPE" Sec. 2).  Any output pointer may be NULL.
+ */
+int scape_get_geometry(const scape_t *h, int64_t *P, int *W, int64_t *k,
+                       int64_t *host_shard_start, int64_t *host_shard_k);
+
+/* Bytes of device workspace scape_bind() needs (mask bitmap, packed index
+ * list, W packed buffers of k floats, the synchronised buffer, tile tables and
+ * mask-refresh scratch). */
+int scape_workspace_bytes(const scape_t *h, size_t *bytes);
+
+/*
+ * Bind caller-owned device memory.  Must precede every GPU call; may be
+ * called again to re-bind (the optimizer step count and the mask are reset to
+ * "no step taken").
+ *   params       float32 w[P], updated in place
+ *   m            float32 first moment m[P], updated in place (caller zeroes it
+ *                before the first step)
+ *   host_e_ptrs  host array of W device pointers, each float32 e^w[P]: the
+ *                per-worker error-feedback residual ("SCAPE" Sec. II-B; FP32,
+ *                same size as the gradient), updated in place (caller zeroes)
+ *   workspace    >= scape_workspace_bytes(), 256-byte aligned
+ * params, m and every e^w must be 16-byte aligned and must not overlap.
+ */
+int scape_bind(scape_t *h, float *params, float *m, float *const *host_e_ptrs,
+               void *workspace, size_t ws_bytes);
+
+/*
+ * One optimizer step t -> t + 1 on `stream`.
+ *   host_grad_ptrs  host array of W device pointers, each the worker's
+ *                   gradient g^w[P] of the bound dtype; read only.  Any
+ *                   alignment is accepted; 16-byte alignment of every
+ *                   gradient and residual selects the vectorised path.
+ * Step 1 is dense (mask of all ones): a^w = g^w + e^w, g_bar = mean_w a^w,
+ * AdamS on all P, e^w <- 0.  Every later step uses the mask of the most recent
+ * scape_refresh_mask() (built from m after the previous step: the one-step
+ * lagged mask of "Sintesi Tecnica: SCAPE" Sec. 2):
+ *   1. error feedback and compaction ("SCAPE" Sec. II-B): a^w = g^w + e^w; the
+ *      selected a^w are packed in ascending index order into worker w's
+ *      k-long buffer, e^w <- a^w - (sent part);
+ *   2. the W packed buffers are summed in worker order 0..W-1 and divided by
+ *      W: the single synchronised sparse buffer g_bar;
+ *   3. AdamS at the k selected coordinates from that one buffer ("SCAPE"
+ *      Sec. II-C Eq. 2, bias corrections 1 - beta^t; "Sintesi Tecnica:
+ *      SCAPE" Sec. 2, second moment rebuilt from the single buffer):
+ *      m' = b1 m + (1-b1) g;  v = b2 m^2 + (1-b2) g^2;
+ *      w <- w - lr (m'/bc1 / (sqrt(v/bc2) + eps) + wd w);  m <- m'.
+ *      Unselected w and m are left unchanged.
+ * Errors: SCAPE_ESTATE before scape_bind() or, for t >= 1, before the first
+ * scape_refresh_mask(); SCAPE_EINVAL for a NULL gradient pointer.
+ */
+int scape_step(scape_t *h, const void *const *host_grad_ptrs, void *stream);
+
+/*
+ * Build the mask for the next step from the current first moment: for each
+ * shard s independently, select the k_s coordinates with the largest |m|
+ * (key = IEEE bits of m with the sign cleared, compared as unsigned; equal
+ * keys go to the lower index), write them into the global bitmap (the shard
+ * masks land in disjoint ranges: the mask all-gather of "Sintesi Tecnica:
+ * SCAPE" Sec. 2), then the ascending packed index list and the per-tile rank
+ * table the next step's compaction uses.  The mask comes from first-moment
+ * statistics, not gradients ("SCAPE" Sec. I).
+ * Errors: SCAPE_ESTATE before the first step.
+ */
+int scape_refresh_mask(scape_t *h, void *stream);
+
+/* Learning rate for subsequent steps (schedules).  lr must be finite. */
+int scape_set_lr(scape_t *h, float lr);
+
+/*
+ * Current state: t = steps taken, k, and device pointers (inside the bound
+ * workspace) to the mask bitmap (ceil(P/32) words) and the packed index list
+ * (k uint32, ascending) that the NEXT step will use.  Pointers stay valid
+ * until re-bind.  Any output may be NULL.
+ */
+int scape_get_state(const scape_t *h, int64_t *t, int64_t *k, const uint32_t **bits,
+                    const uint32_t **idx);
+
+/*
+ * Device pointers to the last step's packed buffers (W rows of k floats,
+ * row w at pack + w * (*pack_stride)) and to the synchronised buffer g_bar
+ * (k floats).  Valid after a step t >= 2 (step 1 is dense and packs nothing).
+ */
+int scape_get_buffers(const scape_t *h, const float **pack, int64_t *pack_stride,
+                      const float **gbar);
+
+/*
+ * Resume from a checkpoint: set the step count t (>= 1) and the mask the next
+ * step uses from a caller bitmap (ceil(P/32) words, device), then rebuild the
+ * index list and rank table.  Synchronises `stream`; returns SCAPE_EINVAL if
+ * the bitmap does not hold exactly k_s set bits in each shard or has bits set
+ * past P.  Parameters, m and residuals are the caller's buffers: restore them
+ * before the next step.
+ */
+int scape_set_state(scape_t *h, int64_t t, const uint32_t *bits, void *stream);
+
+/*
+ * End-to-end step from host memory: copy each worker's gradient from host
+ * memory (pinned for asynchronous copies) into the caller's device gradient
+ * buffers, run scape_step() and scape_refresh_mask(), then copy w[P] back to
+ * host_params_out.  All on `stream`; the caller synchronises before reading
+ * host_params_out.
+ */
+int scape_step_host(scape_t *h, const void *const *host_grads_src,
+                    void *const *host_dev_grad_ptrs, float *host_params_out, void *stream);
+
+/*
+ * Per-kernel timing.  With profiling on, every kernel launch is bracketed by
+ * CUDA events on its stream.  scape_profile_collect() waits for the recorded
+ * events, adds their durations to per-kernel totals and clears the record;
+ * scape_profile_read() copies the totals (milliseconds and launch counts,
+ * SCAPE_NUM_KERNELS entries each) and scape_kernel_name() names entry i.
+ */
+#define SCAPE_NUM_KERNELS 15
+int scape_profile_enable(scape_t *h, int on);
+int scape_profile_collect(scape_t *h);
+int scape_profile_read(const scape_t *h, double *host_ms, int64_t *host_launches);
+int scape_profile_reset(scape_t *h);
+const char *scape_kernel_name(int i);
+
+/* Total kernel launches made through this handle since creation. */
+int64_t scape_launch_count(const scape_t *h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SCAPE_H */

@@ -1,0 +1,200 @@
+"""ctypes binding of the SCAPE C ABI (include/scape.h): argument marshalling only.
+
+Every step of the optimizer runs in the CUDA kernels of libscape.so; this module
+converts Python ints, lists and torch tensors into the pointers and sizes the
+C functions take.  Loading fails loudly when the library has not been built:
+there is no Python or CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+SCAPE_OK = 0
+SCAPE_EINVAL = -1
+SCAPE_ECUDA = -2
+SCAPE_ESTATE = -4
+SCAPE_F32 = 0
+SCAPE_BF16 = 1
+SCAPE_MAX_WORKERS = 256
+SCAPE_NUM_KERNELS = 15
+
+LIB_PATH = _build.LIB
+
+
+class ScapeError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"SCAPE error {code}: {msg}")
+        self.code = code
+
+
+_lib = None
+
+_vp, _i64, _i32, _f32, _f64 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float,
+                               ctypes.c_double)
+_PROTOS = {
+    "scape_create": (_i32, [ctypes.POINTER(_vp), _i32, _vp, _i32, _f64, _f32, _f32, _f32, _f32,
+                            _f32, _i32]),
+    "scape_destroy": (None, [_vp]),
+    "scape_last_error": (ctypes.c_char_p, [_vp]),
+    "scape_get_geometry": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp]),
+    "scape_workspace_bytes": (_i32, [_vp, _vp]),
+    "scape_bind": (_i32, [_vp, _vp, _vp, _vp, _vp, ctypes.c_size_t]),
+    "scape_step": (_i32, [_vp, _vp, _vp]),
+    "scape_refresh_mask": (_i32, [_vp, _vp]),
+    "scape_set_lr": (_i32, [_vp, _f32]),
+    "scape_get_state": (_i32, [_vp, _vp, _vp, _vp, _vp]),
+    "scape_get_buffers": (_i32, [_vp, _vp, _vp, _vp]),
+    "scape_set_state": (_i32, [_vp, _i64, _vp, _vp]),
+    "scape_step_host": (_i32, [_vp, _vp, _vp, _vp, _vp]),
+    "scape_profile_enable": (_i32, [_vp, _i32]),
+    "scape_profile_collect": (_i32, [_vp]),
+    "scape_profile_read": (_i32, [_vp, _vp, _vp]),
+    "scape_profile_reset": (_i32, [_vp]),
+    "scape_kernel_name": (ctypes.c_char_p, [_i32]),
+    "scape_launch_count": (_i64, [_vp]),
+}
+
+
+def load(path: str = LIB_PATH):
+    """Load libscape.so; raises if it is missing (build it first)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise ImportError(f"libscape.so not found at {path}: build it with "
+                              "`python -m sparse_communication_sharded_gb300.build`")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _PROTOS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def exported_symbols():
+    return list(_PROTOS)
+
+
+def _check(h, rc):
+    if rc != SCAPE_OK:
+        msg = load().scape_last_error(h)
+        raise ScapeError(rc, msg.decode() if msg else "")
+    return rc
+
+
+def _ptr_array(ptrs):
+    arr = (ctypes.c_void_p * len(ptrs))(*[int(p) for p in ptrs])
+    return arr
+
+
+# --------------------------------------------------------------- C ABI mirror
+def scape_create(layer_numel, W, sparsity, beta1, beta2, lr, eps, weight_decay, grad_dtype):
+    lib = load()
+    sizes = (ctypes.c_int64 * len(layer_numel))(*[int(n) for n in layer_numel])
+    h = ctypes.c_void_p()
+    rc = lib.scape_create(ctypes.byref(h), len(layer_numel), ctypes.addressof(sizes), int(W),
+                          float(sparsity), beta1, beta2, lr, eps, weight_decay, int(grad_dtype))
+    if rc != SCAPE_OK:
+        raise ScapeError(rc, lib.scape_last_error(None).decode())
+    return h
+
+
+def scape_destroy(h):
+    load().scape_destroy(h)
+
+
+def scape_last_error(h):
+    return load().scape_last_error(h).decode()
+
+
+def scape_get_geometry(h):
+    P, W, k = ctypes.c_int64(), ctypes.c_int(), ctypes.c_int64()
+    _check(h, load().scape_get_geometry(h, ctypes.byref(P), ctypes.byref(W), ctypes.byref(k),
+                                        None, None))
+    start = (ctypes.c_int64 * (W.value + 1))()
+    ks = (ctypes.c_int64 * W.value)()
+    _check(h, load().scape_get_geometry(h, None, None, None, ctypes.addressof(start),
+                                        ctypes.addressof(ks)))
+    return {"P": P.value, "W": W.value, "k": k.value, "shard_start": list(start),
+            "shard_k": list(ks)}
+
+
+def scape_workspace_bytes(h):
+    n = ctypes.c_size_t()
+    _check(h, load().scape_workspace_bytes(h, ctypes.byref(n)))
+    return n.value
+
+
+def scape_bind(h, params_ptr, m_ptr, e_ptrs, ws_ptr, ws_bytes):
+    arr = _ptr_array(e_ptrs)
+    _check(h, load().scape_bind(h, params_ptr, m_ptr, ctypes.addressof(arr), ws_ptr, ws_bytes))
+
+
+def scape_step(h, grad_ptrs, stream=0):
+    arr = _ptr_array(grad_ptrs)
+    _check(h, load().scape_step(h, ctypes.addressof(arr), stream))
+
+
+def scape_refresh_mask(h, stream=0):
+    _check(h, load().scape_refresh_mask(h, stream))
+
+
+def scape_set_lr(h, lr):
+    _check(h, load().scape_set_lr(h, lr))
+
+
+def scape_get_state(h):
+    t, k = ctypes.c_int64(), ctypes.c_int64()
+    bits, idx = ctypes.c_void_p(), ctypes.c_void_p()
+    _check(h, load().scape_get_state(h, ctypes.byref(t), ctypes.byref(k), ctypes.byref(bits),
+                                     ctypes.byref(idx)))
+    return t.value, k.value, bits.value, idx.value
+
+
+def scape_get_buffers(h):
+    pack, stride, gbar = ctypes.c_void_p(), ctypes.c_int64(), ctypes.c_void_p()
+    _check(h, load().scape_get_buffers(h, ctypes.byref(pack), ctypes.byref(stride),
+                                       ctypes.byref(gbar)))
+    return pack.value, stride.value, gbar.value
+
+
+def scape_set_state(h, t, bits_ptr, stream=0):
+    _check(h, load().scape_set_state(h, int(t), bits_ptr, stream))
+
+
+def scape_step_host(h, host_src_ptrs, dev_grad_ptrs, host_params_out_ptr, stream=0):
+    a = _ptr_array(host_src_ptrs)
+    b = _ptr_array(dev_grad_ptrs)
+    _check(h, load().scape_step_host(h, ctypes.addressof(a), ctypes.addressof(b),
+                                     host_params_out_ptr, stream))
+
+
+def scape_profile_enable(h, on=True):
+    _check(h, load().scape_profile_enable(h, 1 if on else 0))
+
+
+def scape_profile_collect(h):
+    _check(h, load().scape_profile_collect(h))
+
+
+def scape_profile_read(h):
+    ms = (ctypes.c_double * SCAPE_NUM_KERNELS)()
+    n = (ctypes.c_int64 * SCAPE_NUM_KERNELS)()
+    _check(h, load().scape_profile_read(h, ctypes.addressof(ms), ctypes.addressof(n)))
+    lib = load()
+    return {lib.scape_kernel_name(i).decode(): (ms[i], n[i]) for i in range(SCAPE_NUM_KERNELS)}
+
+
+def scape_profile_reset(h):
+    _check(h, load().scape_profile_reset(h))
+
+
+def scape_kernel_name(i):
+    return load().scape_kernel_name(i).decode()
+
+
+def scape_launch_count(h):
+    return load().scape_launch_count(h)

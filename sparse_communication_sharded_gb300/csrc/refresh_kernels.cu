@@ -1,0 +1,439 @@
+// refresh_kernels.cu -- partitioned top-k mask refresh of the SCAPE step.
+//
+// For every optimizer shard s independently ("Sintesi Tecnica: SCAPE" Sec. 2,
+// partitioned mask synchronisation), select the k_s parameters with the
+// largest first-moment magnitude (key = bits(m) & 0x7FFFFFFF, so the order of
+// the keys as unsigned integers is the order of |m|), equal keys going to the
+// lower index.  The selection is an exact radix select:
+//   hist<0>/select<0>   11-bit digit 30..20 of every key of the shard
+//   hist<1>/select<1>   11-bit digit 19..9 of the keys matching the prefix
+//   hist<2>/select<2>    9-bit digit  8..0 of the keys matching the prefix
+// which fixes the threshold key kstar and how many keys equal to it are
+// selected (need).  When fewer than all equal keys are selected, tie_count and
+// tie_select find the index istar of the need-th equal key in index order.
+// The mark kernel then writes the bitmap elementwise
+//   bit_i = key_i > kstar  ||  (key_i == kstar && i <= istar)
+// with per-tile popcounts; scan turns those into the per-tile rank table, and
+// index writes the ascending packed index list.
+#include "scape_internal.cuh"
+
+namespace scapek {
+namespace {
+
+
+// ------------------------------------------------------------------ histograms
+// One block per 4096-parameter segment of the flat vector.  A segment that
+// straddles shard boundaries is processed one shard piece at a time.
+template <int PASS>
+__global__ void __launch_bounds__(256)
+radix_hist_kernel(const float* __restrict__ m, int64_t P, int W,
+                  const int64_t* __restrict__ shard_start, const ShardSel* __restrict__ sel,
+                  uint32_t* __restrict__ hist) {
+  constexpr int NB = (PASS == 2) ? 512 : kBins;
+  __shared__ uint32_t sh[NB];
+  const int64_t seg0 = (int64_t)blockIdx.x * kSeg;
+  const int64_t seg1 = min(seg0 + (int64_t)kSeg, P);
+  int s = shard_of(seg0, P, W);
+  for (;;) {
+    const int64_t s_lo = __ldg(shard_start + s), s_hi = __ldg(shard_start + s + 1);
+    const int64_t lo = max(seg0, s_lo), hi = min(seg1, s_hi);
+    const uint32_t mode = (PASS == 0) ? (uint32_t)kSelSearch : sel[s].mode;
+    if (lo < hi && mode == kSelSearch) {
+      const uint32_t prefix = (PASS == 0) ? 0u : sel[s].prefix;
+      for (int b = threadIdx.x; b < NB; b += blockDim.x) sh[b] = 0;
+      __syncthreads();
+      if (lo == seg0 && hi - lo == kSeg) {
+        // whole segment in one shard: 16-byte loads, four per thread
+        const float4* p4 = reinterpret_cast<const float4*>(m + seg0);
+        float4 v[kSeg / 4 / 256];
+#pragma unroll
+        for (int r = 0; r < kSeg / 4 / 256; ++r) v[r] = __ldcs(p4 + threadIdx.x + 256 * r);
+#pragma unroll
+        for (int r = 0; r < kSeg / 4 / 256; ++r) {
+          const float x[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t key = magnitude_key(x[q]);
+            if (PASS == 0) atomicAdd(&sh[key >> kShift0], 1u);
+            if (PASS == 1 && (key >> kShift0) == prefix) atomicAdd(&sh[(key >> kShift1) & 0x7FFu], 1u);
+            if (PASS == 2 && (key >> kShift1) == prefix) atomicAdd(&sh[key & 0x1FFu], 1u);
+          }
+        }
+      } else {
+        for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+          const uint32_t key = magnitude_key(__ldcs(m + i));
+          if (PASS == 0) atomicAdd(&sh[key >> kShift0], 1u);
+          if (PASS == 1 && (key >> kShift0) == prefix) atomicAdd(&sh[(key >> kShift1) & 0x7FFu], 1u);
+          if (PASS == 2 && (key >> kShift1) == prefix) atomicAdd(&sh[key & 0x1FFu], 1u);
+        }
+      }
+      __syncthreads();
+      for (int b = threadIdx.x; b < NB; b += blockDim.x) {
+        const uint32_t c = sh[b];
+        if (c) atomicAdd(hist + (int64_t)s * kBins + b, c);
+      }
+      __syncthreads();
+    }
+    if (s_hi >= seg1 || s == W - 1) break;
+    ++s;
+  }
+}
+
+// ------------------------------------------------------------------ select
+// One block (256 threads) per shard: find the digit holding the krem-th
+// largest key among those matching the prefix, narrow the prefix, and clear
+// the histogram row for the next pass.
+template <int PASS>
+__global__ void __launch_bounds__(256)
+radix_select_kernel(const int64_t* __restrict__ shard_start, const int64_t* __restrict__ shard_k,
+                    ShardSel* __restrict__ sel, uint32_t* __restrict__ hist) {
+  constexpr int NB = (PASS == 2) ? 512 : kBins;
+  constexpr int PER = NB / 256;
+  __shared__ uint32_t warp_tot[8];
+  __shared__ uint32_t sh_digit, sh_above, sh_count;
+  const int s = blockIdx.x;
+  uint32_t* row = hist + (int64_t)s * kBins;
+  const int64_t s_lo = shard_start[s], s_hi = shard_start[s + 1];
+  const int64_t n = s_hi - s_lo, k = shard_k[s];
+
+  ShardSel st;
+  if (PASS == 0) {
+    st.prefix = 0;
+    st.krem = (uint32_t)k;
+    st.kstar = 0;
+    st.need = 0;
+    st.count_eq = 0;
+    st.istar = s_hi - 1;
+    if (n <= 0 || k <= 0) st.mode = kSelEmpty;
+    else if (k >= n) st.mode = kSelDone;  // every key selected: kstar = 0, istar = last
+    else st.mode = kSelSearch;
+  } else {
+    st = sel[s];
+  }
+  if (st.mode != kSelSearch) {
+    if (threadIdx.x == 0 && PASS == 0) sel[s] = st;
+    for (int b = threadIdx.x; b < kBins; b += blockDim.x) row[b] = 0;
+    return;
+  }
+
+  // thread t owns bins [NB - PER*(t+1), NB - PER*t): descending order
+  if (threadIdx.x == 0) {
+    sh_digit = 0;
+    sh_above = 0;
+    sh_count = 0;
+  }
+  uint32_t h[PER];
+  uint32_t local = 0;
+  const int top = NB - PER * (int)threadIdx.x - 1;
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    h[q] = row[top - q];
+    local += h[q];
+  }
+  uint32_t total;
+  const uint32_t excl = block_exclusive_scan<256>(local, warp_tot, &total);
+  if (excl < st.krem && st.krem <= excl + local) {
+    uint32_t cum = excl;
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      if (cum + h[q] >= st.krem) {
+        sh_digit = (uint32_t)(top - q);
+        sh_above = cum;
+        sh_count = h[q];
+        break;
+      }
+      cum += h[q];
+    }
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; b < kBins; b += blockDim.x) row[b] = 0;
+  if (threadIdx.x == 0) {
+    const int bitsw = (PASS == 2) ? 9 : 11;
+    st.prefix = (st.prefix << bitsw) | sh_digit;
+    st.krem -= sh_above;
+    if (PASS == 2) {
+      st.kstar = st.prefix;
+      st.need = st.krem;
+      st.count_eq = sh_count;
+      if (st.need == st.count_eq) {
+        st.istar = s_hi - 1;  // every key equal to kstar is selected
+        st.mode = kSelDone;
+      } else {
+        st.istar = -1;
+        st.mode = kSelTie;
+      }
+    }
+    sel[s] = st;
+  }
+}
+
+// ------------------------------------------------------------------ ties
+// Count keys equal to kstar per 4096-parameter chunk of each tied shard.
+__global__ void __launch_bounds__(256)
+tie_count_kernel(const float* __restrict__ m, const int64_t* __restrict__ shard_start,
+                 const ShardSel* __restrict__ sel, uint32_t* __restrict__ eqcnt, int64_t nchunk) {
+  __shared__ uint32_t warp_tot[8];
+  const int s = blockIdx.y;
+  const int64_t c = blockIdx.x;
+  if (sel[s].mode != kSelTie) return;
+  const int64_t lo = shard_start[s] + c * kTieChunk;
+  const int64_t hi = min(lo + (int64_t)kTieChunk, shard_start[s + 1]);
+  if (lo >= hi) return;
+  const uint32_t kstar = sel[s].kstar;
+  uint32_t cnt = 0;
+  for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x)
+    cnt += magnitude_key(__ldcs(m + i)) == kstar;
+  uint32_t total;
+  block_exclusive_scan<256>(cnt, warp_tot, &total);
+  if (threadIdx.x == 0) eqcnt[(int64_t)s * nchunk + c] = total;
+}
+
+// One block per tied shard: locate the chunk holding the need-th equal key,
+// then the key itself, scanning in index order.
+__global__ void __launch_bounds__(256)
+tie_select_kernel(const float* __restrict__ m, const int64_t* __restrict__ shard_start,
+                  ShardSel* __restrict__ sel, const uint32_t* __restrict__ eqcnt, int64_t nchunk) {
+  __shared__ uint32_t warp_tot[8];
+  __shared__ int64_t sh_chunk;
+  __shared__ uint32_t sh_before;
+  __shared__ int64_t sh_istar;
+  const int s = blockIdx.x;
+  ShardSel st = sel[s];
+  if (st.mode != kSelTie) return;
+  const int64_t s_lo = shard_start[s], s_hi = shard_start[s + 1];
+  const int64_t nch = (s_hi - s_lo + kTieChunk - 1) / kTieChunk;
+  const uint32_t* row = eqcnt + (int64_t)s * nchunk;
+
+  if (threadIdx.x == 0) {
+    sh_chunk = 0;
+    sh_before = 0;
+    sh_istar = s_hi - 1;
+  }
+  // 1) chunk: each thread sums a contiguous run of chunk counts
+  const int64_t per = (nch + 255) / 256;
+  const int64_t c0 = min(nch, per * threadIdx.x), c1 = min(nch, c0 + per);
+  uint32_t local = 0;
+  for (int64_t c = c0; c < c1; ++c) local += row[c];
+  uint32_t total;
+  const uint32_t excl = block_exclusive_scan<256>(local, warp_tot, &total);
+  if (excl < st.need && st.need <= excl + local) {
+    uint32_t cum = excl;
+    for (int64_t c = c0; c < c1; ++c) {
+      if (cum + row[c] >= st.need) {
+        sh_chunk = c;
+        sh_before = cum;
+        break;
+      }
+      cum += row[c];
+    }
+  }
+  __syncthreads();
+  const int64_t lo = s_lo + sh_chunk * kTieChunk;
+  const int64_t hi = min(lo + (int64_t)kTieChunk, s_hi);
+  uint32_t want = st.need - sh_before;  // 1-based rank among equal keys of this chunk
+  // 2) rounds of 256 parameters in index order
+  for (int64_t r0 = lo; r0 < hi; r0 += 256) {
+    const int64_t i = r0 + threadIdx.x;
+    const uint32_t eq = (i < hi) && magnitude_key(m[i]) == st.kstar;
+    __syncthreads();
+    uint32_t round_total;
+    const uint32_t before = block_exclusive_scan<256>(eq, warp_tot, &round_total);
+    if (eq && before + 1 == want) sh_istar = i;
+    __syncthreads();
+    if (round_total >= want) break;
+    want -= round_total;
+  }
+  if (threadIdx.x == 0) {
+    st.istar = sh_istar;
+    st.mode = kSelDone;
+    sel[s] = st;
+  }
+}
+
+// ------------------------------------------------------------------ mark
+// One block per 2048-parameter tile; warp q covers words 8q..8q+7 of the tile,
+// lane l decides parameter 32*word + l, a ballot assembles each word.
+__global__ void __launch_bounds__(256)
+mark_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __restrict__ shard_start,
+            const ShardSel* __restrict__ sel, uint32_t* __restrict__ bits,
+            uint32_t* __restrict__ tile_cnt) {
+  __shared__ uint32_t warp_tot[8];
+  const int64_t tile = blockIdx.x;
+  const int64_t t0 = tile * kTile;
+  const int64_t t1 = min(t0 + (int64_t)kTile, P);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int s = shard_of(t0, P, W);
+  const bool uniform = __ldg(shard_start + s + 1) >= t1;
+  uint32_t kstar = sel[s].kstar;
+  int64_t istar = sel[s].istar;
+
+  const int64_t wbase = tile * kTileWords + warp * 8;
+  float x[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int64_t i = (wbase + j) * 32 + lane;
+    x[j] = (i < P) ? __ldcs(m + i) : 0.f;
+  }
+  uint32_t myword = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int64_t i = (wbase + j) * 32 + lane;
+    bool on = false;
+    if (i < P) {
+      if (!uniform) {
+        int si = s;
+        while (si < W - 1 && i >= __ldg(shard_start + si + 1)) ++si;
+        kstar = sel[si].kstar;
+        istar = sel[si].istar;
+      }
+      const uint32_t key = magnitude_key(x[j]);
+      on = key > kstar || (key == kstar && i <= istar);
+    }
+    const uint32_t word = __ballot_sync(0xffffffffu, on);
+    if (lane == j) myword = word;
+  }
+  const int64_t nwords = (P + 31) / 32;
+  if (lane < 8 && wbase + lane < nwords) bits[wbase + lane] = myword;
+  uint32_t total;
+  block_exclusive_scan<256>(lane < 8 ? __popc(myword) : 0u, warp_tot, &total);
+  if (threadIdx.x == 0) tile_cnt[tile] = total;
+}
+
+// Per-tile popcount of an existing bitmap (checkpoint resume).
+__global__ void __launch_bounds__(64)
+tile_count_kernel(const uint32_t* __restrict__ bits, int64_t nwords, uint32_t* __restrict__ tile_cnt) {
+  const int64_t wi = (int64_t)blockIdx.x * kTileWords + threadIdx.x;
+  uint32_t c = wi < nwords ? __popc(bits[wi]) : 0u;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+  __shared__ uint32_t part[2];
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = c;
+  __syncthreads();
+  if (threadIdx.x == 0) tile_cnt[blockIdx.x] = part[0] + part[1];
+}
+
+// ------------------------------------------------------------------ scan
+// Exclusive scan of the per-tile counts in one block; tile_base[ntiles] = total.
+__global__ void __launch_bounds__(1024)
+scan_kernel(const uint32_t* __restrict__ cnt, int64_t n, uint32_t* __restrict__ base) {
+  __shared__ uint32_t warp_tot[32];
+  const int64_t per = (n + 1023) / 1024;
+  const int64_t c0 = min(n, per * threadIdx.x), c1 = min(n, c0 + per);
+  uint32_t local = 0;
+  for (int64_t c = c0; c < c1; ++c) local += cnt[c];
+  uint32_t total;
+  uint32_t run = block_exclusive_scan<1024>(local, warp_tot, &total);
+  for (int64_t c = c0; c < c1; ++c) {
+    const uint32_t v = cnt[c];
+    base[c] = run;
+    run += v;
+  }
+  if (threadIdx.x == 0) base[n] = total;
+}
+
+// ------------------------------------------------------------------ index
+// idx[rank] = i for every set bit, ranks ascending: one block per tile,
+// 8 parameters (one bitmap byte) per thread.
+__global__ void __launch_bounds__(kTileThreads)
+index_kernel(const uint32_t* __restrict__ bits, int64_t P, const uint32_t* __restrict__ tile_base,
+             uint32_t* __restrict__ idx) {
+  __shared__ uint32_t warp_tot[kTileThreads / 32];
+  const int64_t tile = blockIdx.x;
+  const int64_t i0 = tile * kTile + (int64_t)threadIdx.x * 8;
+  uint32_t byte = 0;
+  if (i0 < P) byte = (__ldg(bits + (i0 >> 5)) >> (uint32_t)(i0 & 31)) & 0xFFu;
+  uint32_t total;
+  const uint32_t excl = block_exclusive_scan<kTileThreads>(__popc(byte), warp_tot, &total);
+  uint32_t* out = idx + __ldg(tile_base + tile) + excl;
+  int r = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    if ((byte >> j) & 1u) out[r++] = (uint32_t)(i0 + j);
+}
+
+// Per-shard popcount of a bitmap plus the count of bits set past P (in
+// counts[W]); used to validate a restored mask.
+__global__ void __launch_bounds__(256)
+shard_count_kernel(const uint32_t* __restrict__ bits, int64_t P, int64_t nwords, int W,
+                   uint32_t* __restrict__ counts) {
+  const int64_t wi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (wi >= nwords) return;
+  uint32_t word = bits[wi];
+  while (word) {
+    const int b = __ffs(word) - 1;
+    word &= word - 1;
+    const int64_t i = wi * 32 + b;
+    if (i >= P) atomicAdd(counts + W, 1u);
+    else atomicAdd(counts + shard_of(i, P, W), 1u);
+  }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ launchers
+cudaError_t launch_hist(int pass, const float* m, int64_t P, int W, const int64_t* shard_start,
+                        const ShardSel* sel, uint32_t* hist, cudaStream_t st) {
+  const unsigned grid = (unsigned)((P + kSeg - 1) / kSeg);
+  if (pass == 0) radix_hist_kernel<0><<<grid, 256, 0, st>>>(m, P, W, shard_start, sel, hist);
+  else if (pass == 1) radix_hist_kernel<1><<<grid, 256, 0, st>>>(m, P, W, shard_start, sel, hist);
+  else radix_hist_kernel<2><<<grid, 256, 0, st>>>(m, P, W, shard_start, sel, hist);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_select(int pass, int W, const int64_t* shard_start, const int64_t* shard_k,
+                          ShardSel* sel, uint32_t* hist, cudaStream_t st) {
+  if (pass == 0) radix_select_kernel<0><<<W, 256, 0, st>>>(shard_start, shard_k, sel, hist);
+  else if (pass == 1) radix_select_kernel<1><<<W, 256, 0, st>>>(shard_start, shard_k, sel, hist);
+  else radix_select_kernel<2><<<W, 256, 0, st>>>(shard_start, shard_k, sel, hist);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tie_count(const float* m, int W, const int64_t* shard_start,
+                             const ShardSel* sel, uint32_t* eqcnt, int64_t nchunk,
+                             cudaStream_t st) {
+  dim3 grid((unsigned)nchunk, (unsigned)W);
+  tie_count_kernel<<<grid, 256, 0, st>>>(m, shard_start, sel, eqcnt, nchunk);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tie_select(const float* m, int W, const int64_t* shard_start, ShardSel* sel,
+                              const uint32_t* eqcnt, int64_t nchunk, cudaStream_t st) {
+  tie_select_kernel<<<W, 256, 0, st>>>(m, shard_start, sel, eqcnt, nchunk);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mark(const float* m, int64_t P, int W, const int64_t* shard_start,
+                        const ShardSel* sel, uint32_t* bits, uint32_t* tile_cnt,
+                        cudaStream_t st) {
+  const unsigned grid = (unsigned)((P + kTile - 1) / kTile);
+  mark_kernel<<<grid, 256, 0, st>>>(m, P, W, shard_start, sel, bits, tile_cnt);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tile_count(const uint32_t* bits, int64_t P, uint32_t* tile_cnt,
+                              cudaStream_t st) {
+  const unsigned grid = (unsigned)((P + kTile - 1) / kTile);
+  tile_count_kernel<<<grid, kTileWords, 0, st>>>(bits, (P + 31) / 32, tile_cnt);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scan(const uint32_t* tile_cnt, int64_t ntiles, uint32_t* tile_base,
+                        cudaStream_t st) {
+  scan_kernel<<<1, 1024, 0, st>>>(tile_cnt, ntiles, tile_base);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_index(const uint32_t* bits, int64_t P, const uint32_t* tile_base,
+                         uint32_t* idx, cudaStream_t st) {
+  const unsigned grid = (unsigned)((P + kTile - 1) / kTile);
+  index_kernel<<<grid, kTileThreads, 0, st>>>(bits, P, tile_base, idx);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_shard_count(const uint32_t* bits, int64_t P, int64_t nwords, int W,
+                               uint32_t* counts, cudaStream_t st) {
+  shard_count_kernel<<<(unsigned)((nwords + 255) / 256), 256, 0, st>>>(bits, P, nwords, W, counts);
+  return cudaGetLastError();
+}
+
+}  // namespace scapek

@@ -1,0 +1,548 @@
+// scape_api.cu -- host implementation of the SCAPE C ABI (include/scape.h).
+//
+// Holds the shard layout, the caller-bound device pointers, the step count and
+// the carve-up of the caller's workspace; enqueues the kernels of
+// step_kernels.cu and refresh_kernels.cu on the caller's stream.  Never
+// allocates device memory.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "scape_internal.cuh"
+
+using namespace scapek;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+thread_local std::string g_create_error;
+
+const char* const kKernelNames[kNumKernels] = {
+    "dense_step", "ef_compact", "reduce",      "adams_sparse", "radix_hist0",
+    "radix_hist1", "radix_hist2", "radix_select", "tie_count",   "tie_select",
+    "mark",        "scan",        "index",        "shard_count", "tile_count"};
+
+struct ProfRec {
+  int kid;
+  cudaEvent_t a, b;
+};
+
+}  // namespace
+
+struct scape {
+  // configuration
+  int64_t P = 0;
+  int W = 0;
+  int64_t ppm = 0;
+  float beta1 = 0, beta2 = 0, lr = 0, eps = 0, wd = 0;
+  int dtype = SCAPE_BF16;
+  std::vector<int64_t> shard_start, shard_k;
+  int64_t k = 0;
+  int64_t ntiles = 0, nwords = 0, kstride = 0, nchunk = 0;
+  bool all_dense = false;  // every shard keeps all of its coordinates
+  // workspace offsets (bytes)
+  size_t off_bits = 0, off_idx = 0, off_tbase = 0, off_tcnt = 0, off_pack = 0, off_gbar = 0,
+         off_hist = 0, off_sel = 0, off_eqcnt = 0, off_sstart = 0, off_sk = 0, off_counts = 0,
+         ws_need = 0;
+  // bound memory
+  bool bound = false;
+  float* w = nullptr;
+  float* m = nullptr;
+  std::vector<float*> e;
+  char* ws = nullptr;
+  // state
+  int64_t t = 0;
+  bool mask_ready = false;
+  bool buffers_valid = false;
+  int64_t launches = 0;
+  // profiling
+  bool prof = false;
+  std::vector<ProfRec> pending;
+  std::vector<cudaEvent_t> pool;
+  double prof_ms[kNumKernels] = {};
+  int64_t prof_n[kNumKernels] = {};
+  std::string err;
+
+  template <class T>
+  T* at(size_t off) const { return reinterpret_cast<T*>(ws + off); }
+  uint32_t* bits() const { return at<uint32_t>(off_bits); }
+  uint32_t* idx() const { return at<uint32_t>(off_idx); }
+  uint32_t* tile_base() const { return at<uint32_t>(off_tbase); }
+  uint32_t* tile_cnt() const { return at<uint32_t>(off_tcnt); }
+  float* pack() const { return at<float>(off_pack); }
+  float* gbar() const { return at<float>(off_gbar); }
+  uint32_t* hist() const { return at<uint32_t>(off_hist); }
+  ShardSel* sel() const { return at<ShardSel>(off_sel); }
+  uint32_t* eqcnt() const { return at<uint32_t>(off_eqcnt); }
+  int64_t* d_shard_start() const { return at<int64_t>(off_sstart); }
+  int64_t* d_shard_k() const { return at<int64_t>(off_sk); }
+  uint32_t* counts() const { return at<uint32_t>(off_counts); }
+};
+
+namespace {
+
+int fail(scape_t* h, int code, const std::string& msg) {
+  if (h) h->err = msg;
+  return code;
+}
+
+int cuda_fail(scape_t* h, cudaError_t e, const char* what) {
+  return fail(h, SCAPE_ECUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+cudaEvent_t take_event(scape_t* h) {
+  if (!h->pool.empty()) {
+    cudaEvent_t ev = h->pool.back();
+    h->pool.pop_back();
+    return ev;
+  }
+  cudaEvent_t ev = nullptr;
+  if (cudaEventCreate(&ev) != cudaSuccess) return nullptr;
+  return ev;
+}
+
+// Enqueue one kernel through `fn` (which returns the launch status), with
+// optional event bracketing for per-kernel timing.
+template <class F>
+int run_kernel(scape_t* h, int kid, cudaStream_t st, F&& fn) {
+  cudaEvent_t a = nullptr, b = nullptr;
+  if (h->prof) {
+    a = take_event(h);
+    b = take_event(h);
+    if (a && b) cudaEventRecord(a, st);
+  }
+  const cudaError_t e = fn();
+  h->launches++;
+  if (h->prof && a && b) {
+    cudaEventRecord(b, st);
+    h->pending.push_back({kid, a, b});
+  }
+  if (e != cudaSuccess) return cuda_fail(h, e, kKernelNames[kid]);
+  return SCAPE_OK;
+}
+
+AdamsConst make_const(const scape_t* h, int64_t t) {
+  AdamsConst c;
+  c.beta1 = h->beta1;
+  c.beta2 = h->beta2;
+  c.one_minus_b1 = 1.0f - h->beta1;
+  c.one_minus_b2 = 1.0f - h->beta2;
+  c.bc1 = (float)(1.0 - std::pow((double)h->beta1, (double)t));
+  c.bc2 = (float)(1.0 - std::pow((double)h->beta2, (double)t));
+  c.lr = h->lr;
+  c.eps = h->eps;
+  c.wd = h->wd;
+  return c;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Rank table and index list from the bitmap already in the workspace.
+int rebuild_from_bits(scape_t* h, cudaStream_t st, bool counts_ready) {
+  int rc;
+  if (!counts_ready) {
+    rc = run_kernel(h, kKTileCount, st,
+                    [&] { return launch_tile_count(h->bits(), h->P, h->tile_cnt(), st); });
+    if (rc) return rc;
+  }
+  rc = run_kernel(h, kKScan, st,
+                  [&] { return launch_scan(h->tile_cnt(), h->ntiles, h->tile_base(), st); });
+  if (rc) return rc;
+  return run_kernel(h, kKIndex, st,
+                    [&] { return launch_index(h->bits(), h->P, h->tile_base(), h->idx(), st); });
+}
+
+}  // namespace
+
+extern "C" {
+
+int scape_create(scape_t** out, int n_layers, const int64_t* host_layer_numel, int W,
+                 double sparsity, float beta1, float beta2, float lr, float eps,
+                 float weight_decay, int grad_dtype) {
+  g_create_error.clear();
+  auto bad = [&](const char* msg) {
+    g_create_error = msg;
+    return SCAPE_EINVAL;
+  };
+  if (!out) return bad("out is NULL");
+  *out = nullptr;
+  if (n_layers < 1 || !host_layer_numel) return bad("need at least one layer size");
+  int64_t P = 0;
+  for (int i = 0; i < n_layers; ++i) {
+    if (host_layer_numel[i] < 0) return bad("negative layer size");
+    P += host_layer_numel[i];
+    if (P > 2147483647LL) return bad("P exceeds 2^31 - 1");
+  }
+  if (P < 1) return bad("P must be >= 1");
+  if (W < 1 || W > SCAPE_MAX_WORKERS) return bad("W out of range [1, SCAPE_MAX_WORKERS]");
+  if (!(sparsity >= 0.0 && sparsity < 1.0)) return bad("sparsity must be in [0, 1)");
+  const int64_t ppm = std::llround(sparsity * 1e6);
+  if (ppm >= 1000000) return bad("sparsity rounds to 1 (nothing would be sent)");
+  if (!(beta1 >= 0.f && beta1 < 1.f) || !(beta2 >= 0.f && beta2 < 1.f))
+    return bad("betas must be in [0, 1)");
+  if (!(eps > 0.f) || !std::isfinite(eps)) return bad("eps must be finite and > 0");
+  if (!std::isfinite(lr)) return bad("lr must be finite");
+  if (!(weight_decay >= 0.f) || !std::isfinite(weight_decay))
+    return bad("weight_decay must be finite and >= 0");
+  if (grad_dtype != SCAPE_F32 && grad_dtype != SCAPE_BF16) return bad("unknown grad dtype");
+
+  scape_t* h = new (std::nothrow) scape_t();
+  if (!h) return bad("out of host memory");
+  h->P = P;
+  h->W = W;
+  h->ppm = ppm;
+  h->beta1 = beta1;
+  h->beta2 = beta2;
+  h->lr = lr;
+  h->eps = eps;
+  h->wd = weight_decay;
+  h->dtype = grad_dtype;
+  h->shard_start.resize(W + 1);
+  h->shard_k.resize(W);
+  int64_t nmax = 0;
+  h->all_dense = true;
+  for (int s = 0; s <= W; ++s) h->shard_start[s] = ((int64_t)s * P) / W;
+  for (int s = 0; s < W; ++s) {
+    const int64_t n = h->shard_start[s + 1] - h->shard_start[s];
+    h->shard_k[s] = (n * (1000000 - ppm) + 999999) / 1000000;
+    h->k += h->shard_k[s];
+    nmax = n > nmax ? n : nmax;
+    if (h->shard_k[s] != n) h->all_dense = false;
+  }
+  h->ntiles = (P + kTile - 1) / kTile;
+  h->nwords = (P + 31) / 32;
+  h->kstride = (int64_t)align_up((size_t)(h->k > 0 ? h->k : 1), 64);
+  h->nchunk = (nmax + kTieChunk - 1) / kTieChunk;
+  if (h->nchunk < 1) h->nchunk = 1;
+
+  size_t off = 0;
+  auto carve = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, kAlign);
+    return o;
+  };
+  h->off_bits = carve(align_up((size_t)h->nwords, 64) * 4);
+  h->off_idx = carve((size_t)h->kstride * 4);
+  h->off_tbase = carve((size_t)(h->ntiles + 1) * 4);
+  h->off_tcnt = carve((size_t)h->ntiles * 4);
+  h->off_pack = carve((size_t)W * h->kstride * 4);
+  h->off_gbar = carve((size_t)h->kstride * 4);
+  h->off_hist = carve((size_t)W * kBins * 4);
+  h->off_sel = carve((size_t)W * sizeof(ShardSel));
+  h->off_eqcnt = carve((size_t)W * h->nchunk * 4);
+  h->off_sstart = carve((size_t)(W + 1) * 8);
+  h->off_sk = carve((size_t)W * 8);
+  h->off_counts = carve((size_t)(W + 1) * 4);
+  h->ws_need = off;
+  *out = h;
+  return SCAPE_OK;
+}
+
+void scape_destroy(scape_t* h) {
+  if (!h) return;
+  for (auto& r : h->pending) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  for (auto ev : h->pool) cudaEventDestroy(ev);
+  delete h;
+}
+
+const char* scape_last_error(const scape_t* h) {
+  return h ? h->err.c_str() : g_create_error.c_str();
+}
+
+int scape_get_geometry(const scape_t* h, int64_t* P, int* W, int64_t* k, int64_t* host_shard_start,
+                       int64_t* host_shard_k) {
+  if (!h) return SCAPE_EINVAL;
+  if (P) *P = h->P;
+  if (W) *W = h->W;
+  if (k) *k = h->k;
+  if (host_shard_start)
+    std::memcpy(host_shard_start, h->shard_start.data(), sizeof(int64_t) * (h->W + 1));
+  if (host_shard_k) std::memcpy(host_shard_k, h->shard_k.data(), sizeof(int64_t) * h->W);
+  return SCAPE_OK;
+}
+
+int scape_workspace_bytes(const scape_t* h, size_t* bytes) {
+  if (!h || !bytes) return SCAPE_EINVAL;
+  *bytes = h->ws_need;
+  return SCAPE_OK;
+}
+
+int scape_bind(scape_t* h, float* params, float* m, float* const* host_e_ptrs, void* workspace,
+               size_t ws_bytes) {
+  if (!h) return SCAPE_EINVAL;
+  if (!params || !m || !host_e_ptrs || !workspace)
+    return fail(h, SCAPE_EINVAL, "scape_bind: NULL pointer");
+  if (ws_bytes < h->ws_need) return fail(h, SCAPE_EINVAL, "scape_bind: workspace too small");
+  if ((reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0)
+    return fail(h, SCAPE_EINVAL, "scape_bind: workspace must be 256-byte aligned");
+  if (!aligned16(params) || !aligned16(m))
+    return fail(h, SCAPE_EINVAL, "scape_bind: params and m must be 16-byte aligned");
+  h->e.assign(h->W, nullptr);
+  for (int w = 0; w < h->W; ++w) {
+    if (!host_e_ptrs[w]) return fail(h, SCAPE_EINVAL, "scape_bind: NULL residual pointer");
+    if (!aligned16(host_e_ptrs[w]))
+      return fail(h, SCAPE_EINVAL, "scape_bind: residuals must be 16-byte aligned");
+    h->e[w] = host_e_ptrs[w];
+  }
+  h->w = params;
+  h->m = m;
+  h->ws = static_cast<char*>(workspace);
+  // the small shard table lives in the workspace for the kernels
+  cudaError_t e = cudaMemcpy(h->d_shard_start(), h->shard_start.data(), 8 * (h->W + 1),
+                             cudaMemcpyHostToDevice);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(h->d_shard_k(), h->shard_k.data(), 8 * h->W, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(h, e, "scape_bind: shard table upload");
+  h->bound = true;
+  h->t = 0;
+  h->mask_ready = false;
+  h->buffers_valid = false;
+  return SCAPE_OK;
+}
+
+int scape_step(scape_t* h, const void* const* host_grad_ptrs, void* stream) {
+  if (!h) return SCAPE_EINVAL;
+  if (!h->bound) return fail(h, SCAPE_ESTATE, "scape_step: call scape_bind first");
+  if (!host_grad_ptrs) return fail(h, SCAPE_EINVAL, "scape_step: NULL gradient table");
+  if (h->t >= 1 && !h->mask_ready)
+    return fail(h, SCAPE_ESTATE, "scape_step: no mask yet; call scape_refresh_mask after step 1");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  WorkerPtrs p;
+  std::memset(&p, 0, sizeof p);
+  bool vec = true;
+  for (int w = 0; w < h->W; ++w) {
+    if (!host_grad_ptrs[w]) return fail(h, SCAPE_EINVAL, "scape_step: NULL gradient pointer");
+    p.g[w] = host_grad_ptrs[w];
+    p.e[w] = h->e[w];
+    vec = vec && aligned16(host_grad_ptrs[w]);
+  }
+  const int64_t t = h->t + 1;
+  const AdamsConst c = make_const(h, t);
+  int rc;
+  if (t == 1) {
+    rc = run_kernel(h, kKDenseStep, st, [&] {
+      return launch_dense_step(p, h->W, h->P, h->dtype, vec, h->w, h->m, c, st);
+    });
+    if (rc) return rc;
+    h->buffers_valid = false;
+  } else {
+    rc = run_kernel(h, kKEfCompact, st, [&] {
+      return launch_ef_compact(p, h->W, h->P, h->dtype, vec, h->bits(), h->tile_base(), h->pack(),
+                               h->kstride, st);
+    });
+    if (rc) return rc;
+    rc = run_kernel(h, kKReduce, st, [&] {
+      return launch_reduce(h->pack(), h->kstride, h->W, h->k, h->gbar(), st);
+    });
+    if (rc) return rc;
+    rc = run_kernel(h, kKAdamsSparse, st, [&] {
+      return launch_adams_sparse(h->idx(), h->gbar(), h->k, h->w, h->m, c, st);
+    });
+    if (rc) return rc;
+    h->buffers_valid = true;
+  }
+  h->t = t;
+  return SCAPE_OK;
+}
+
+int scape_refresh_mask(scape_t* h, void* stream) {
+  if (!h) return SCAPE_EINVAL;
+  if (!h->bound) return fail(h, SCAPE_ESTATE, "scape_refresh_mask: call scape_bind first");
+  if (h->t < 1) return fail(h, SCAPE_ESTATE, "scape_refresh_mask: no step taken yet");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int rc;
+  if (!h->all_dense) {
+    cudaError_t e = cudaMemsetAsync(h->hist(), 0, (size_t)h->W * kBins * 4, st);
+    if (e != cudaSuccess) return cuda_fail(h, e, "scape_refresh_mask: histogram clear");
+    rc = run_kernel(h, kKHist0, st, [&] {
+      return launch_hist(0, h->m, h->P, h->W, h->d_shard_start(), h->sel(), h->hist(), st);
+    });
+    if (rc) return rc;
+  }
+  rc = run_kernel(h, kKSelect, st, [&] {
+    return launch_select(0, h->W, h->d_shard_start(), h->d_shard_k(), h->sel(), h->hist(), st);
+  });
+  if (rc) return rc;
+  if (!h->all_dense) {
+    for (int pass = 1; pass <= 2; ++pass) {
+      rc = run_kernel(h, pass == 1 ? kKHist1 : kKHist2, st, [&] {
+        return launch_hist(pass, h->m, h->P, h->W, h->d_shard_start(), h->sel(), h->hist(), st);
+      });
+      if (rc) return rc;
+      rc = run_kernel(h, kKSelect, st, [&] {
+        return launch_select(pass, h->W, h->d_shard_start(), h->d_shard_k(), h->sel(), h->hist(),
+                             st);
+      });
+      if (rc) return rc;
+    }
+    rc = run_kernel(h, kKTieCount, st, [&] {
+      return launch_tie_count(h->m, h->W, h->d_shard_start(), h->sel(), h->eqcnt(), h->nchunk, st);
+    });
+    if (rc) return rc;
+    rc = run_kernel(h, kKTieSelect, st, [&] {
+      return launch_tie_select(h->m, h->W, h->d_shard_start(), h->sel(), h->eqcnt(), h->nchunk,
+                               st);
+    });
+    if (rc) return rc;
+  }
+  rc = run_kernel(h, kKMark, st, [&] {
+    return launch_mark(h->m, h->P, h->W, h->d_shard_start(), h->sel(), h->bits(), h->tile_cnt(),
+                       st);
+  });
+  if (rc) return rc;
+  rc = rebuild_from_bits(h, st, true);
+  if (rc) return rc;
+  h->mask_ready = true;
+  return SCAPE_OK;
+}
+
+int scape_set_lr(scape_t* h, float lr) {
+  if (!h) return SCAPE_EINVAL;
+  if (!std::isfinite(lr)) return fail(h, SCAPE_EINVAL, "scape_set_lr: lr must be finite");
+  h->lr = lr;
+  return SCAPE_OK;
+}
+
+int scape_get_state(const scape_t* h, int64_t* t, int64_t* k, const uint32_t** bits,
+                    const uint32_t** idx) {
+  if (!h) return SCAPE_EINVAL;
+  if (t) *t = h->t;
+  if (k) *k = h->k;
+  if (bits) *bits = h->bound ? h->bits() : nullptr;
+  if (idx) *idx = h->bound ? h->idx() : nullptr;
+  return SCAPE_OK;
+}
+
+int scape_get_buffers(const scape_t* h, const float** pack, int64_t* pack_stride,
+                      const float** gbar) {
+  if (!h) return SCAPE_EINVAL;
+  if (!h->bound || !h->buffers_valid) {
+    const_cast<scape_t*>(h)->err = "scape_get_buffers: no sparse step taken since bind";
+    return SCAPE_ESTATE;
+  }
+  if (pack) *pack = h->pack();
+  if (pack_stride) *pack_stride = h->kstride;
+  if (gbar) *gbar = h->gbar();
+  return SCAPE_OK;
+}
+
+int scape_set_state(scape_t* h, int64_t t, const uint32_t* bits, void* stream) {
+  if (!h) return SCAPE_EINVAL;
+  if (!h->bound) return fail(h, SCAPE_ESTATE, "scape_set_state: call scape_bind first");
+  if (t < 1 || !bits) return fail(h, SCAPE_EINVAL, "scape_set_state: need t >= 1 and a bitmap");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(h->bits(), bits, (size_t)h->nwords * 4, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(h->counts(), 0, (size_t)(h->W + 1) * 4, st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "scape_set_state: copy");
+  int rc = run_kernel(h, kKShardCount, st, [&] {
+    return launch_shard_count(h->bits(), h->P, h->nwords, h->W, h->counts(), st);
+  });
+  if (rc) return rc;
+  std::vector<uint32_t> cnt(h->W + 1);
+  e = cudaMemcpyAsync(cnt.data(), h->counts(), (size_t)(h->W + 1) * 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "scape_set_state: count readback");
+  if (cnt[h->W] != 0) {
+    h->mask_ready = false;
+    return fail(h, SCAPE_EINVAL, "scape_set_state: bitmap has bits set past P");
+  }
+  for (int s = 0; s < h->W; ++s) {
+    if ((int64_t)cnt[s] != h->shard_k[s]) {
+      h->mask_ready = false;
+      char buf[160];
+      std::snprintf(buf, sizeof buf, "scape_set_state: shard %d has %u set bits, expected %lld", s,
+                    cnt[s], (long long)h->shard_k[s]);
+      return fail(h, SCAPE_EINVAL, buf);
+    }
+  }
+  rc = rebuild_from_bits(h, st, false);
+  if (rc) return rc;
+  h->t = t;
+  h->mask_ready = true;
+  h->buffers_valid = false;
+  return SCAPE_OK;
+}
+
+int scape_step_host(scape_t* h, const void* const* host_grads_src, void* const* host_dev_grad_ptrs,
+                    float* host_params_out, void* stream) {
+  if (!h) return SCAPE_EINVAL;
+  if (!h->bound) return fail(h, SCAPE_ESTATE, "scape_step_host: call scape_bind first");
+  if (!host_grads_src || !host_dev_grad_ptrs || !host_params_out)
+    return fail(h, SCAPE_EINVAL, "scape_step_host: NULL pointer");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t gbytes = (size_t)h->P * (h->dtype == SCAPE_BF16 ? 2 : 4);
+  for (int w = 0; w < h->W; ++w) {
+    if (!host_grads_src[w] || !host_dev_grad_ptrs[w])
+      return fail(h, SCAPE_EINVAL, "scape_step_host: NULL gradient pointer");
+    cudaError_t e = cudaMemcpyAsync(host_dev_grad_ptrs[w], host_grads_src[w], gbytes,
+                                    cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(h, e, "scape_step_host: gradient upload");
+  }
+  int rc = scape_step(h, reinterpret_cast<const void* const*>(host_dev_grad_ptrs), stream);
+  if (rc) return rc;
+  rc = scape_refresh_mask(h, stream);
+  if (rc) return rc;
+  cudaError_t e = cudaMemcpyAsync(host_params_out, h->w, (size_t)h->P * 4, cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "scape_step_host: parameter download");
+  return SCAPE_OK;
+}
+
+int scape_profile_enable(scape_t* h, int on) {
+  if (!h) return SCAPE_EINVAL;
+  h->prof = on != 0;
+  return SCAPE_OK;
+}
+
+int scape_profile_collect(scape_t* h) {
+  if (!h) return SCAPE_EINVAL;
+  int rc = SCAPE_OK;
+  for (auto& r : h->pending) {
+    cudaError_t e = cudaEventSynchronize(r.b);
+    float ms = 0.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.a, r.b);
+    if (e != cudaSuccess) {
+      rc = cuda_fail(h, e, "scape_profile_collect");
+    } else {
+      h->prof_ms[r.kid] += ms;
+      h->prof_n[r.kid] += 1;
+    }
+    h->pool.push_back(r.a);
+    h->pool.push_back(r.b);
+  }
+  h->pending.clear();
+  return rc;
+}
+
+int scape_profile_read(const scape_t* h, double* host_ms, int64_t* host_launches) {
+  if (!h) return SCAPE_EINVAL;
+  for (int i = 0; i < kNumKernels; ++i) {
+    if (host_ms) host_ms[i] = h->prof_ms[i];
+    if (host_launches) host_launches[i] = h->prof_n[i];
+  }
+  return SCAPE_OK;
+}
+
+int scape_profile_reset(scape_t* h) {
+  if (!h) return SCAPE_EINVAL;
+  for (int i = 0; i < kNumKernels; ++i) {
+    h->prof_ms[i] = 0;
+    h->prof_n[i] = 0;
+  }
+  return SCAPE_OK;
+}
+
+const char* scape_kernel_name(int i) {
+  return (i >= 0 && i < kNumKernels) ? kKernelNames[i] : "";
+}
+
+int64_t scape_launch_count(const scape_t* h) { return h ? h->launches : -1; }
+
+}  // extern "C"

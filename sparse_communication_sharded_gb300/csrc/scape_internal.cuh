@@ -1,0 +1,164 @@
+// scape_internal.cuh -- types, constants and device helpers shared by the
+// SCAPE library's translation units (kernels and the C ABI host code).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "scape.h"
+
+namespace scapek {
+
+// Compaction tile: 2048 parameters = 64 bitmap words, 256 threads x 8 elements.
+// The per-tile rank table built by the mask refresh is indexed by this tile.
+constexpr int kTile = 2048;
+constexpr int kTileThreads = 256;
+constexpr int kTileWords = kTile / 32;
+
+// Radix select over 31-bit magnitude keys: digits of 11, 11 and 9 bits.
+constexpr int kBins = 2048;
+constexpr int kShift0 = 20;  // pass 0: key bits 30..20
+constexpr int kShift1 = 9;   // pass 1: key bits 19..9
+// pass 2: key bits 8..0 (512 bins)
+
+// Segment of m read by one block of a histogram pass.
+constexpr int kSeg = 4096;
+// Chunk of a shard scanned by one block when resolving equal keys.
+constexpr int kTieChunk = 4096;
+
+struct WorkerPtrs {
+  const void* g[SCAPE_MAX_WORKERS];
+  float* e[SCAPE_MAX_WORKERS];
+};
+
+// Per-shard state of the radix select.
+enum SelMode : uint32_t {
+  kSelEmpty = 0,   // shard holds no parameter
+  kSelDone = 1,    // threshold final (kstar, istar valid)
+  kSelSearch = 2,  // radix passes still narrowing the threshold
+  kSelTie = 3      // kstar final, istar to be found among equal keys
+};
+
+struct ShardSel {
+  uint32_t mode;
+  uint32_t prefix;    // key bits fixed by the passes so far
+  uint32_t krem;      // selections still owed among keys matching prefix
+  uint32_t kstar;     // threshold key: every key > kstar is selected
+  uint32_t need;      // how many keys == kstar are selected (lowest indices)
+  uint32_t count_eq;  // how many keys == kstar the shard holds
+  int64_t istar;      // keys == kstar with index <= istar are selected
+};
+
+// AdamS constants of one step; all computed on the host in float.
+struct AdamsConst {
+  float beta1, beta2, one_minus_b1, one_minus_b2, bc1, bc2, lr, eps, wd;
+};
+
+// Profiling ids; must stay in sync with kKernelNames in scape_api.cu.
+enum KernelId {
+  kKDenseStep = 0,
+  kKEfCompact,
+  kKReduce,
+  kKAdamsSparse,
+  kKHist0,
+  kKHist1,
+  kKHist2,
+  kKSelect,
+  kKTieCount,
+  kKTieSelect,
+  kKMark,
+  kKScan,
+  kKIndex,
+  kKShardCount,
+  kKTileCount,
+  kNumKernels
+};
+static_assert(kNumKernels == SCAPE_NUM_KERNELS, "kernel table size");
+
+// ---------------------------------------------------------------- device helpers
+__device__ __forceinline__ uint32_t magnitude_key(float x) {
+  return __float_as_uint(x) & 0x7FFFFFFFu;
+}
+
+// Shard owning parameter i (0 <= i < P): the largest s with floor(s*P/W) <= i.
+__device__ __forceinline__ int shard_of(int64_t i, int64_t P, int W) {
+  return (int)(((i + 1) * (int64_t)W - 1) / P);
+}
+
+// Exclusive prefix sum over a block of NT threads (NT a multiple of 32).
+// `warp_tot` holds NT/32 words of shared memory; callers __syncthreads()
+// before reusing it.  *total receives the block sum.
+template <int NT>
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_tot,
+                                                         uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  uint32_t off = 0, tot = 0;
+#pragma unroll
+  for (int i = 0; i < NT / 32; ++i) {
+    uint32_t t = warp_tot[i];
+    off += (i < warp) ? t : 0u;
+    tot += t;
+  }
+  *total = tot;
+  return off + x - v;
+}
+
+// AdamS update of one coordinate ("SCAPE" Sec. II-C, Eq. 2 with bias
+// corrections), one IEEE binary32 operation at a time in a fixed order so
+// that results do not depend on compiler contraction.
+__device__ __forceinline__ void adams_update(float g, float& w, float& m, const AdamsConst& c) {
+  const float m_prev = m, w_prev = w;
+  const float m_new = __fadd_rn(__fmul_rn(c.beta1, m_prev), __fmul_rn(c.one_minus_b1, g));
+  const float v = __fadd_rn(__fmul_rn(c.beta2, __fmul_rn(m_prev, m_prev)),
+                            __fmul_rn(c.one_minus_b2, __fmul_rn(g, g)));
+  const float m_hat = __fdiv_rn(m_new, c.bc1);
+  const float v_hat = __fdiv_rn(v, c.bc2);
+  const float denom = __fadd_rn(__fsqrt_rn(v_hat), c.eps);
+  const float upd = __fadd_rn(__fdiv_rn(m_hat, denom), __fmul_rn(c.wd, w_prev));
+  w = __fsub_rn(w_prev, __fmul_rn(c.lr, upd));
+  m = m_new;
+}
+
+// ---------------------------------------------------------------- launchers
+// Each returns cudaGetLastError() after enqueueing on `st`.
+cudaError_t launch_dense_step(const WorkerPtrs& p, int W, int64_t P, int dtype, bool vec,
+                              float* w, float* m, const AdamsConst& c, cudaStream_t st);
+cudaError_t launch_ef_compact(const WorkerPtrs& p, int W, int64_t P, int dtype, bool vec,
+                              const uint32_t* bits, const uint32_t* tile_base, float* pack,
+                              int64_t pack_stride, cudaStream_t st);
+cudaError_t launch_reduce(const float* pack, int64_t pack_stride, int W, int64_t k, float* gbar,
+                          cudaStream_t st);
+cudaError_t launch_adams_sparse(const uint32_t* idx, const float* gbar, int64_t k, float* w,
+                                float* m, const AdamsConst& c, cudaStream_t st);
+
+cudaError_t launch_hist(int pass, const float* m, int64_t P, int W, const int64_t* shard_start,
+                        const ShardSel* sel, uint32_t* hist, cudaStream_t st);
+cudaError_t launch_select(int pass, int W, const int64_t* shard_start, const int64_t* shard_k,
+                          ShardSel* sel, uint32_t* hist, cudaStream_t st);
+cudaError_t launch_tie_count(const float* m, int W, const int64_t* shard_start,
+                             const ShardSel* sel, uint32_t* eqcnt, int64_t nchunk,
+                             cudaStream_t st);
+cudaError_t launch_tie_select(const float* m, int W, const int64_t* shard_start, ShardSel* sel,
+                              const uint32_t* eqcnt, int64_t nchunk, cudaStream_t st);
+cudaError_t launch_mark(const float* m, int64_t P, int W, const int64_t* shard_start,
+                        const ShardSel* sel, uint32_t* bits, uint32_t* tile_cnt,
+                        cudaStream_t st);
+cudaError_t launch_tile_count(const uint32_t* bits, int64_t P, uint32_t* tile_cnt,
+                              cudaStream_t st);
+cudaError_t launch_scan(const uint32_t* tile_cnt, int64_t ntiles, uint32_t* tile_base,
+                        cudaStream_t st);
+cudaError_t launch_index(const uint32_t* bits, int64_t P, const uint32_t* tile_base,
+                         uint32_t* idx, cudaStream_t st);
+cudaError_t launch_shard_count(const uint32_t* bits, int64_t P, int64_t nwords, int W,
+                               uint32_t* counts, cudaStream_t st);
+
+}  // namespace scapek

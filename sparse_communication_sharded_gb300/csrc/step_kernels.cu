@@ -1,0 +1,305 @@
+// step_kernels.cu -- the per-step kernels of the SCAPE optimizer step.
+//
+//   dense_step   step 1 (mask of all ones): error-feedback add, ordered mean
+//                over workers, AdamS on every coordinate, residual <- 0.
+//   ef_compact   error-feedback add + lagged-mask compaction + residual
+//                ("SCAPE" Sec. II-B: sent = TopK(g + e) through the mask,
+//                e <- g + e - sent), one pass over every worker's g and e.
+//   reduce       ordered sum of the W packed buffers / W: the single
+//                synchronised sparse buffer ("Sintesi Tecnica: SCAPE" Sec. 2).
+//   adams_sparse unpack + AdamS ("SCAPE" Sec. II-C, Eq. 2) at the k selected
+//                coordinates, m and v both from that one buffer.
+#include "scape_internal.cuh"
+
+namespace scapek {
+namespace {
+
+template <typename GT>
+struct GradIO;
+
+template <>
+struct GradIO<float> {
+  // 8 consecutive gradients starting at a 32-byte multiple of the base.
+  static __device__ __forceinline__ void load8(const void* base, int64_t i0, float (&g)[8]) {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + i0);
+    float4 a = __ldcs(p), b = __ldcs(p + 1);
+    g[0] = a.x; g[1] = a.y; g[2] = a.z; g[3] = a.w;
+    g[4] = b.x; g[5] = b.y; g[6] = b.z; g[7] = b.w;
+  }
+  static __device__ __forceinline__ float load1(const void* base, int64_t i) {
+    return __ldcs(static_cast<const float*>(base) + i);
+  }
+};
+
+template <>
+struct GradIO<__nv_bfloat16> {
+  static __device__ __forceinline__ void load8(const void* base, int64_t i0, float (&g)[8]) {
+    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + i0);
+    uint4 v = __ldcs(p);
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      // bfloat16 is the high half of a binary32: widening is exact.
+      g[2 * q] = __uint_as_float(u[q] << 16);
+      g[2 * q + 1] = __uint_as_float(u[q] & 0xFFFF0000u);
+    }
+  }
+  static __device__ __forceinline__ float load1(const void* base, int64_t i) {
+    const unsigned short h =
+        __ldcs(reinterpret_cast<const unsigned short*>(static_cast<const __nv_bfloat16*>(base) + i));
+    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+  }
+};
+
+__device__ __forceinline__ void load8_f32(const float* p, float (&x)[8]) {
+  const float4* q = reinterpret_cast<const float4*>(p);
+  float4 a = __ldcs(q), b = __ldcs(q + 1);
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+__device__ __forceinline__ void store8_f32(float* p, const float (&x)[8]) {
+  float4* q = reinterpret_cast<float4*>(p);
+  __stcs(q, make_float4(x[0], x[1], x[2], x[3]));
+  __stcs(q + 1, make_float4(x[4], x[5], x[6], x[7]));
+}
+
+// ------------------------------------------------------------------ ef_compact
+// One block per 2048-parameter tile; each thread owns 8 consecutive parameters
+// (one byte of the mask bitmap).  The rank of every selected parameter in the
+// packed buffers is the tile's base (from the refresh's rank table) plus the
+// block-exclusive popcount prefix, computed once and reused for all W workers.
+constexpr int kWorkerUnroll = 2;
+
+__device__ __forceinline__ void ef_select8(const float (&g)[8], const float (&e)[8], uint32_t byte,
+                                           float* __restrict__ prow, float (&out)[8]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float a = __fadd_rn(g[j], e[j]);  // error-feedback add
+    float sent = 0.f;
+    if ((byte >> j) & 1u) {
+      sent = a;
+      prow[__popc(byte & ((1u << j) - 1u))] = a;
+    }
+    out[j] = __fsub_rn(a, sent);  // residual: g + e - sent
+  }
+}
+
+template <typename GT, bool VEC>
+__global__ void __launch_bounds__(kTileThreads, 3)
+ef_compact_kernel(const __grid_constant__ WorkerPtrs ptrs, int W, int64_t P,
+                  const uint32_t* __restrict__ bits, const uint32_t* __restrict__ tile_base,
+                  float* __restrict__ pack, int64_t pack_stride) {
+  __shared__ uint32_t warp_tot[kTileThreads / 32];
+  const int64_t tile = blockIdx.x;
+  const int64_t i0 = tile * kTile + (int64_t)threadIdx.x * 8;
+  uint32_t byte = 0;
+  if (i0 < P) byte = (__ldg(bits + (i0 >> 5)) >> (uint32_t)(i0 & 31)) & 0xFFu;
+  uint32_t total;
+  const uint32_t excl = block_exclusive_scan<kTileThreads>(__popc(byte), warp_tot, &total);
+  float* const pbase = pack + (int64_t)__ldg(tile_base + tile) + excl;
+
+  if (VEC && (tile + 1) * kTile <= P) {
+    // full tile: 16-byte loads and stores; the loads of a worker pair are
+    // issued before either pair member is stored
+    for (int w0 = 0; w0 < W; w0 += kWorkerUnroll) {
+      float g[kWorkerUnroll][8], e[kWorkerUnroll][8];
+#pragma unroll
+      for (int u = 0; u < kWorkerUnroll; ++u) {
+        if (w0 + u < W) {
+          GradIO<GT>::load8(ptrs.g[w0 + u], i0, g[u]);
+          load8_f32(ptrs.e[w0 + u] + i0, e[u]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kWorkerUnroll; ++u) {
+        if (w0 + u < W) {
+          float out[8];
+          ef_select8(g[u], e[u], byte, pbase + (int64_t)(w0 + u) * pack_stride, out);
+          store8_f32(ptrs.e[w0 + u] + i0, out);
+        }
+      }
+    }
+  } else {
+    // ragged last tile, or unaligned buffers: element by element
+    for (int wk = 0; wk < W; ++wk) {
+      float g[8], e[8], out[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const bool in = i0 + j < P;
+        g[j] = in ? GradIO<GT>::load1(ptrs.g[wk], i0 + j) : 0.f;
+        e[j] = in ? __ldcs(ptrs.e[wk] + i0 + j) : 0.f;
+      }
+      ef_select8(g, e, byte, pbase + (int64_t)wk * pack_stride, out);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (i0 + j < P) __stcs(ptrs.e[wk] + i0 + j, out[j]);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ dense_step
+// Step 1: every coordinate is selected, so the synchronised buffer is the
+// ordered mean of all a^w = g^w + e^w and the residuals become a - a.
+template <typename GT, bool VEC>
+__global__ void __launch_bounds__(256)
+dense_step_kernel(const __grid_constant__ WorkerPtrs ptrs, int W, int64_t P,
+                  float* __restrict__ wts, float* __restrict__ mom, AdamsConst c) {
+  const int64_t i0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  if (i0 >= P) return;
+  const bool full = VEC && (i0 + 8 <= P);
+  const int n = full ? 8 : (int)(P - i0 < 8 ? P - i0 : 8);
+  float sum[8];
+  for (int wk = 0; wk < W; ++wk) {
+    float g[8], e[8], z[8];
+    if (full) {
+      GradIO<GT>::load8(ptrs.g[wk], i0, g);
+      load8_f32(ptrs.e[wk] + i0, e);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        g[j] = j < n ? GradIO<GT>::load1(ptrs.g[wk], i0 + j) : 0.f;
+        e[j] = j < n ? ptrs.e[wk][i0 + j] : 0.f;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float a = __fadd_rn(g[j], e[j]);
+      sum[j] = (wk == 0) ? a : __fadd_rn(sum[j], a);
+      z[j] = __fsub_rn(a, a);
+    }
+    if (full) {
+      store8_f32(ptrs.e[wk] + i0, z);
+    } else {
+      for (int j = 0; j < n; ++j) ptrs.e[wk][i0 + j] = z[j];
+    }
+  }
+  const float fw = (float)W;
+  for (int j = 0; j < n; ++j) {
+    float wv = wts[i0 + j], mv = mom[i0 + j];
+    adams_update(__fdiv_rn(sum[j], fw), wv, mv, c);
+    wts[i0 + j] = wv;
+    mom[i0 + j] = mv;
+  }
+}
+
+// ------------------------------------------------------------------ reduce
+// g_bar[j] = (((p_0 + p_1) + p_2) + ... + p_{W-1}) / W, 4 slots per thread.
+__global__ void __launch_bounds__(256)
+reduce_kernel(const float* __restrict__ pack, int64_t stride, int W, int64_t k,
+              float* __restrict__ gbar) {
+  const int64_t j0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (j0 >= k) return;
+  const float fw = (float)W;
+  if (j0 + 4 <= k) {
+    float4 s = __ldg(reinterpret_cast<const float4*>(pack + j0));
+#pragma unroll 8
+    for (int wk = 1; wk < W; ++wk) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(pack + (int64_t)wk * stride + j0));
+      s.x = __fadd_rn(s.x, v.x);
+      s.y = __fadd_rn(s.y, v.y);
+      s.z = __fadd_rn(s.z, v.z);
+      s.w = __fadd_rn(s.w, v.w);
+    }
+    *reinterpret_cast<float4*>(gbar + j0) =
+        make_float4(__fdiv_rn(s.x, fw), __fdiv_rn(s.y, fw), __fdiv_rn(s.z, fw), __fdiv_rn(s.w, fw));
+  } else {
+    for (int64_t j = j0; j < k; ++j) {
+      float s = pack[j];
+      for (int wk = 1; wk < W; ++wk) s = __fadd_rn(s, pack[(int64_t)wk * stride + j]);
+      gbar[j] = __fdiv_rn(s, fw);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ adams_sparse
+// For the k selected coordinates i = idx[j]: AdamS with g = g_bar[j].
+__global__ void __launch_bounds__(256)
+adams_sparse_kernel(const uint32_t* __restrict__ idx, const float* __restrict__ gbar, int64_t k,
+                    float* __restrict__ wts, float* __restrict__ mom, AdamsConst c) {
+  const int64_t j0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (j0 >= k) return;
+  if (j0 + 4 <= k) {
+    const uint4 iv = __ldg(reinterpret_cast<const uint4*>(idx + j0));
+    const float4 gv = __ldg(reinterpret_cast<const float4*>(gbar + j0));
+    const uint32_t ii[4] = {iv.x, iv.y, iv.z, iv.w};
+    const float gg[4] = {gv.x, gv.y, gv.z, gv.w};
+    float wv[4], mv[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      wv[q] = wts[ii[q]];
+      mv[q] = mom[ii[q]];
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      adams_update(gg[q], wv[q], mv[q], c);
+      wts[ii[q]] = wv[q];
+      mom[ii[q]] = mv[q];
+    }
+  } else {
+    for (int64_t j = j0; j < k; ++j) {
+      const uint32_t i = idx[j];
+      float wv = wts[i], mv = mom[i];
+      adams_update(gbar[j], wv, mv, c);
+      wts[i] = wv;
+      mom[i] = mv;
+    }
+  }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ launchers
+cudaError_t launch_dense_step(const WorkerPtrs& p, int W, int64_t P, int dtype, bool vec,
+                              float* w, float* m, const AdamsConst& c, cudaStream_t st) {
+  const int64_t threads = (P + 7) / 8;
+  const unsigned grid = (unsigned)((threads + 255) / 256);
+  if (dtype == SCAPE_BF16) {
+    if (vec) dense_step_kernel<__nv_bfloat16, true><<<grid, 256, 0, st>>>(p, W, P, w, m, c);
+    else dense_step_kernel<__nv_bfloat16, false><<<grid, 256, 0, st>>>(p, W, P, w, m, c);
+  } else {
+    if (vec) dense_step_kernel<float, true><<<grid, 256, 0, st>>>(p, W, P, w, m, c);
+    else dense_step_kernel<float, false><<<grid, 256, 0, st>>>(p, W, P, w, m, c);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ef_compact(const WorkerPtrs& p, int W, int64_t P, int dtype, bool vec,
+                              const uint32_t* bits, const uint32_t* tile_base, float* pack,
+                              int64_t pack_stride, cudaStream_t st) {
+  const unsigned grid = (unsigned)((P + kTile - 1) / kTile);
+  if (dtype == SCAPE_BF16) {
+    if (vec)
+      ef_compact_kernel<__nv_bfloat16, true>
+          <<<grid, kTileThreads, 0, st>>>(p, W, P, bits, tile_base, pack, pack_stride);
+    else
+      ef_compact_kernel<__nv_bfloat16, false>
+          <<<grid, kTileThreads, 0, st>>>(p, W, P, bits, tile_base, pack, pack_stride);
+  } else {
+    if (vec)
+      ef_compact_kernel<float, true>
+          <<<grid, kTileThreads, 0, st>>>(p, W, P, bits, tile_base, pack, pack_stride);
+    else
+      ef_compact_kernel<float, false>
+          <<<grid, kTileThreads, 0, st>>>(p, W, P, bits, tile_base, pack, pack_stride);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce(const float* pack, int64_t pack_stride, int W, int64_t k, float* gbar,
+                          cudaStream_t st) {
+  if (k <= 0) return cudaSuccess;
+  const int64_t threads = (k + 3) / 4;
+  reduce_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(pack, pack_stride, W, k, gbar);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_adams_sparse(const uint32_t* idx, const float* gbar, int64_t k, float* w,
+                                float* m, const AdamsConst& c, cudaStream_t st) {
+  if (k <= 0) return cudaSuccess;
+  const int64_t threads = (k + 3) / 4;
+  adams_sparse_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(idx, gbar, k, w, m, c);
+  return cudaGetLastError();
+}
+
+}  // namespace scapek

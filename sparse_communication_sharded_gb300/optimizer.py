@@ -1,0 +1,123 @@
+"""SCAPE optimizer over torch-allocated device memory.
+
+PyTorch provides the device buffers (parameters, first moment, per-worker
+residuals, workspace) and the stream; every computation is a kernel of
+libscape.so reached through the C ABI.  W data-parallel workers are held as W
+gradient tensors on one GPU.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _scape as C
+
+
+class Scape:
+    """One SCAPE instance bound to `params` (float32, CUDA, flat)."""
+
+    def __init__(self, params: torch.Tensor, W: int, sparsity: float, *, layer_numel=None,
+                 lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1,
+                 grad_dtype=torch.bfloat16):
+        if not params.is_cuda or params.dtype != torch.float32 or not params.is_contiguous():
+            raise ValueError("params must be a contiguous float32 CUDA tensor")
+        P = params.numel()
+        layer_numel = [P] if layer_numel is None else list(layer_numel)
+        if sum(layer_numel) != P:
+            raise ValueError("layer sizes must sum to params.numel()")
+        self.grad_dtype = grad_dtype
+        dt = C.SCAPE_BF16 if grad_dtype == torch.bfloat16 else C.SCAPE_F32
+        if grad_dtype not in (torch.bfloat16, torch.float32):
+            raise ValueError("grad_dtype must be torch.bfloat16 or torch.float32")
+        self.h = C.scape_create(layer_numel, W, sparsity, beta1, beta2, lr, eps, weight_decay, dt)
+        geo = C.scape_get_geometry(self.h)
+        self.P, self.W, self.k = geo["P"], geo["W"], geo["k"]
+        self.shard_start, self.shard_k = geo["shard_start"], geo["shard_k"]
+        dev = params.device
+        self.params = params
+        self.m = torch.zeros(P, dtype=torch.float32, device=dev)
+        self.e = [torch.zeros(P, dtype=torch.float32, device=dev) for _ in range(W)]
+        self.ws_bytes = C.scape_workspace_bytes(self.h)
+        self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        C.scape_bind(self.h, params.data_ptr(), self.m.data_ptr(), [x.data_ptr() for x in self.e],
+                     self.workspace.data_ptr(), self.ws_bytes)
+
+    # ----------------------------------------------------------- hot path
+    @staticmethod
+    def _stream():
+        return torch.cuda.current_stream().cuda_stream
+
+    def step(self, grads):
+        if len(grads) != self.W:
+            raise ValueError(f"expected {self.W} gradients")
+        for g in grads:
+            if g.dtype != self.grad_dtype or g.numel() != self.P or not g.is_cuda:
+                raise ValueError("gradient dtype/size/device mismatch")
+        C.scape_step(self.h, [g.data_ptr() for g in grads], self._stream())
+
+    def refresh_mask(self):
+        C.scape_refresh_mask(self.h, self._stream())
+
+    def step_host(self, host_grads, dev_grads, host_params_out):
+        C.scape_step_host(self.h, [g.data_ptr() for g in host_grads],
+                          [g.data_ptr() for g in dev_grads], host_params_out.data_ptr(),
+                          self._stream())
+
+    def set_lr(self, lr):
+        C.scape_set_lr(self.h, lr)
+
+    # ----------------------------------------------------------- state views
+    def _view(self, ptr, n, dtype):
+        off = ptr - self.workspace.data_ptr()
+        esz = torch.empty(0, dtype=dtype).element_size()
+        return self.workspace[off:off + n * esz].view(dtype)
+
+    @property
+    def t(self):
+        return C.scape_get_state(self.h)[0]
+
+    def bits(self):
+        _, _, bits, _ = C.scape_get_state(self.h)
+        return self._view(bits, (self.P + 31) // 32, torch.int32)
+
+    def idx(self):
+        _, k, _, idx = C.scape_get_state(self.h)
+        return self._view(idx, k, torch.int32)
+
+    def pack(self):
+        ptr, stride, _ = C.scape_get_buffers(self.h)
+        full = self._view(ptr, stride * self.W, torch.float32).view(self.W, stride)
+        return full[:, :self.k]
+
+    def gbar(self):
+        _, _, ptr = C.scape_get_buffers(self.h)
+        return self._view(ptr, self.k, torch.float32)
+
+    def set_state(self, t, bits: torch.Tensor):
+        C.scape_set_state(self.h, t, bits.data_ptr(), self._stream())
+
+    # ----------------------------------------------------------- profiling
+    def profile(self, on=True):
+        C.scape_profile_enable(self.h, on)
+
+    def profile_collect(self):
+        C.scape_profile_collect(self.h)
+
+    def profile_read(self):
+        return C.scape_profile_read(self.h)
+
+    def profile_reset(self):
+        C.scape_profile_reset(self.h)
+
+    def launch_count(self):
+        return C.scape_launch_count(self.h)
+
+    def close(self):
+        if getattr(self, "h", None) is not None:
+            C.scape_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,154 @@
+"""Helpers for the GPU parity tests: run the CUDA path and the CPU oracle on the
+same seeded inputs and compare them."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import oracle as O
+from sparse_communication_sharded_gb300 import Scape, synth
+
+HP = O.Hyper(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1)
+RTOL, ATOL = 1e-5, 1e-7          # float states after the trajectory
+MAX_FLIP_FRACTION = 1e-4         # threshold-boundary mask flips
+
+
+def u32(t: torch.Tensor) -> np.ndarray:
+    a = t.detach().cpu().contiguous().numpy()
+    return a.view(np.uint32)
+
+
+def bits_to_bool(bits: np.ndarray, lo: int, hi: int) -> np.ndarray:
+    i = np.arange(lo, hi)
+    return ((bits[i // 32] >> (i % 32).astype(np.uint32)) & 1).astype(bool)
+
+
+def make_opt(params, W, s, grad_dtype):
+    return Scape(params, W, s, lr=HP.lr, beta1=HP.beta1, beta2=HP.beta2, eps=HP.eps,
+                 weight_decay=HP.weight_decay, grad_dtype=grad_dtype)
+
+
+def assert_close_f32(got: np.ndarray, want: np.ndarray, what: str):
+    got = np.asarray(got, np.float32)
+    want = np.asarray(want, np.float32)
+    bad = ~np.isclose(got, want, rtol=RTOL, atol=ATOL)
+    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} outside rtol={RTOL} atol={ATOL}; "
+                           f"max abs diff {np.abs(got - want).max():.3e}")
+
+
+class Report:
+    """Per-run parity facts the tests assert on and print."""
+
+    def __init__(self):
+        self.flips = 0
+        self.mask_bits = 0
+        self.exact = True
+
+    def note(self, equal: bool):
+        self.exact = self.exact and bool(equal)
+
+
+def run_full_trajectory(wl: synth.Workload, device, steps: int, seed: int = 0,
+                        grad_offset_elems: int = 0):
+    """Whole problem on both sides (small sizes): compare every step."""
+    P, W, s = wl.P, wl.W, wl.sparsity
+    gdt = torch.bfloat16 if wl.grad_dtype == "bf16" else torch.float32
+    w0 = synth.init_params(P, seed=seed)
+    gen = synth.GradientStream(wl, seed=seed, device="cpu")
+    params = w0.to(device)
+    opt = make_opt(params, W, s, gdt)
+    st = O.new_state(w0.numpy(), W, s, HP)
+    rep = Report()
+    # optional misaligned gradient buffers (scalar path)
+    dev_bufs = [torch.empty(P + grad_offset_elems, dtype=gdt, device=device) for _ in range(W)]
+    for t in range(1, steps + 1):
+        grads = gen.next()
+        dg = []
+        for buf, g in zip(dev_bufs, grads):
+            view = buf[grad_offset_elems:grad_offset_elems + P]
+            view.copy_(g.to(device))
+            dg.append(view)
+        opt.step(dg)
+        rec = O.advance(st, [synth.to_numpy_grad(g) for g in grads])
+        if t >= 2:
+            torch.cuda.synchronize()
+            pack = u32(opt.pack())
+            gbar = u32(opt.gbar())
+            assert pack.shape == rec["pack"].shape
+            rep.note(np.array_equal(pack, rec["pack"].view(np.uint32)))
+            rep.note(np.array_equal(gbar, rec["gbar"].view(np.uint32)))
+        opt.refresh_mask()
+        torch.cuda.synchronize()
+        gb = u32(opt.bits())
+        flips = int(np.unpackbits((gb ^ rec["bits"]).view(np.uint8)).sum())
+        rep.flips += flips
+        rep.mask_bits += P
+        if flips == 0:
+            assert np.array_equal(u32(opt.idx()), rec["idx"].view(np.uint32)), "idx mismatch"
+        rep.note(flips == 0)
+    torch.cuda.synchronize()
+    assert_close_f32(params.cpu().numpy(), st.w, "w")
+    assert_close_f32(opt.m.cpu().numpy(), st.m, "m")
+    for w in range(W):
+        assert_close_f32(opt.e[w].cpu().numpy(), st.e[w], f"e[{w}]")
+    rep.note(np.array_equal(u32(params), st.w.view(np.uint32)))
+    rep.note(np.array_equal(u32(opt.m), st.m.view(np.uint32)))
+    for w in range(W):
+        rep.note(np.array_equal(u32(opt.e[w]), st.e[w].view(np.uint32)))
+    assert rep.flips <= MAX_FLIP_FRACTION * rep.mask_bits, f"{rep.flips} mask flips"
+    opt.close()
+    return rep
+
+
+def run_sampled_shards(wl: synth.Workload, device, steps: int, shards, seed: int = 0):
+    """Full-size problem on the GPU; the oracle runs each sampled shard as an
+    independent sub-problem (shards share nothing but the step count)."""
+    P, W, s = wl.P, wl.W, wl.sparsity
+    gdt = torch.bfloat16 if wl.grad_dtype == "bf16" else torch.float32
+    w0 = synth.init_params(P, seed=seed, device=device)
+    gen = synth.GradientStream(wl, seed=seed, device=device)
+    params = w0.clone()
+    opt = make_opt(params, W, s, gdt)
+    start, ks = opt.shard_start, opt.shard_k
+    kofs = np.concatenate([[0], np.cumsum(ks)])
+    subs = {}
+    for sh in shards:
+        lo, hi = start[sh], start[sh + 1]
+        subs[sh] = O.new_state(w0[lo:hi].cpu().numpy(), W, s, HP,
+                               shard_start=np.array([0, hi - lo], np.int64),
+                               shard_k=np.array([ks[sh]], np.int64))
+    bufs = gen.alloc()
+    rep = Report()
+    for t in range(1, steps + 1):
+        gen.next_into(bufs)
+        opt.step(bufs)
+        opt.refresh_mask()
+        torch.cuda.synchronize()
+        gbits = u32(opt.bits())
+        pack = opt.pack().cpu().numpy() if t >= 2 else None
+        gbar = opt.gbar().cpu().numpy() if t >= 2 else None
+        for sh in shards:
+            lo, hi = start[sh], start[sh + 1]
+            rec = O.advance(subs[sh], [synth.to_numpy_grad(b[lo:hi]) for b in bufs])
+            if t >= 2:
+                k0, k1 = kofs[sh], kofs[sh + 1]
+                rep.note(np.array_equal(pack[:, k0:k1].view(np.uint32), rec["pack"].view(np.uint32)))
+                rep.note(np.array_equal(gbar[k0:k1].view(np.uint32), rec["gbar"].view(np.uint32)))
+            want = bits_to_bool(rec["bits"], 0, hi - lo)
+            got = bits_to_bool(gbits, lo, hi)
+            rep.flips += int((want != got).sum())
+            rep.mask_bits += hi - lo
+            rep.note(bool((want == got).all()))
+    for sh in shards:
+        lo, hi = start[sh], start[sh + 1]
+        sub = subs[sh]
+        assert_close_f32(params[lo:hi].cpu().numpy(), sub.w, f"w shard {sh}")
+        assert_close_f32(opt.m[lo:hi].cpu().numpy(), sub.m, f"m shard {sh}")
+        rep.note(np.array_equal(u32(params[lo:hi]), sub.w.view(np.uint32)))
+        rep.note(np.array_equal(u32(opt.m[lo:hi]), sub.m.view(np.uint32)))
+        for w in (0, W - 1):
+            assert_close_f32(opt.e[w][lo:hi].cpu().numpy(), sub.e[w], f"e[{w}] shard {sh}")
+            rep.note(np.array_equal(u32(opt.e[w][lo:hi]), sub.e[w].view(np.uint32)))
+    assert rep.flips <= MAX_FLIP_FRACTION * rep.mask_bits, f"{rep.flips} mask flips"
+    opt.close()
+    return rep

@@ -1,0 +1,120 @@
+"""The C-ABI library loads on a host without a GPU, exports every entry point
+include/scape.h declares, and its host-only logic (argument validation, shard
+layout, k, workspace size, call-order errors) behaves -- no GPU work is done."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import oracle as O
+from sparse_communication_sharded_gb300 import _scape as C
+from sparse_communication_sharded_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return C.load()
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", fn)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names |= set(re.findall(r"\b(scape_\w+)\s*\(", txt))
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared()
+    assert len(declared) >= 19
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert declared == set(C.exported_symbols())
+
+
+def _create(P=4096, W=4, s=0.9, beta1=0.9, beta2=0.95, lr=1e-3, eps=1e-8, wd=0.1, dt=C.SCAPE_F32):
+    return C.scape_create([P] if isinstance(P, int) else P, W, s, beta1, beta2, lr, eps, wd, dt)
+
+
+@pytest.mark.parametrize("kw", [dict(P=0), dict(W=0), dict(W=C.SCAPE_MAX_WORKERS + 1),
+                                dict(s=1.0), dict(s=-0.1), dict(s=0.9999999), dict(beta1=1.0),
+                                dict(beta2=-0.5), dict(eps=0.0), dict(wd=-1.0), dict(dt=7),
+                                dict(lr=float("nan")), dict(P=[1 << 30, 1 << 30, 1 << 30])])
+def test_create_rejects_bad_arguments(lib, kw):
+    with pytest.raises(C.ScapeError) as ei:
+        _create(**kw)
+    assert ei.value.code == C.SCAPE_EINVAL
+    assert C.scape_last_error(None) != ""
+
+
+@pytest.mark.parametrize("P,W,s", [(4096, 4, 0.9), (569570560, 32, 0.99), (354871296, 8, 0.9),
+                                   (1364297728, 8, 0.99), (5, 8, 0.5), (1 << 20, 32, 0.999),
+                                   (1000, 7, 0.0)])
+def test_geometry_matches_oracle_layout(lib, P, W, s):
+    h = _create(P=P, W=W, s=s)
+    geo = C.scape_get_geometry(h)
+    start, ks = O.layout(P, W, s)
+    assert geo["shard_start"] == start.tolist()
+    assert geo["shard_k"] == ks.tolist()
+    assert geo["k"] == int(ks.sum()) and geo["P"] == P and geo["W"] == W
+    ws = C.scape_workspace_bytes(h)
+    # the W packed buffers dominate the workspace
+    assert ws >= 4 * W * geo["k"] + 4 * geo["k"] + (P + 31) // 32 * 4
+    C.scape_destroy(h)
+
+
+def test_layers_concatenate(lib):
+    h = C.scape_create([10, 0, 30], 2, 0.5, 0.9, 0.95, 1e-3, 1e-8, 0.1, C.SCAPE_BF16)
+    assert C.scape_get_geometry(h)["P"] == 40
+    C.scape_destroy(h)
+
+
+def test_call_order_errors_without_gpu(lib):
+    h = _create()
+    with pytest.raises(C.ScapeError) as ei:
+        C.scape_step(h, [0] * 4)
+    assert ei.value.code == C.SCAPE_ESTATE
+    with pytest.raises(C.ScapeError) as ei:
+        C.scape_refresh_mask(h)
+    assert ei.value.code == C.SCAPE_ESTATE
+    with pytest.raises(C.ScapeError) as ei:
+        C.scape_bind(h, 0, 0, [0] * 4, 0, 0)
+    assert ei.value.code == C.SCAPE_EINVAL
+    with pytest.raises(C.ScapeError) as ei:
+        C.scape_get_buffers(h)
+    assert ei.value.code == C.SCAPE_ESTATE
+    with pytest.raises(C.ScapeError):
+        C.scape_set_lr(h, float("inf"))
+    C.scape_set_lr(h, 5e-4)
+    t, k, bits, idx = C.scape_get_state(h)
+    assert t == 0 and k == 412 and bits is None and idx is None
+    assert C.scape_launch_count(h) == 0
+    C.scape_destroy(h)
+
+
+def test_bind_validates_before_any_cuda_call(lib):
+    h = _create()
+    ws = C.scape_workspace_bytes(h)
+    with pytest.raises(C.ScapeError) as ei:        # workspace too small
+        C.scape_bind(h, 256, 512, [1024] * 4, 4096, ws - 1)
+    assert ei.value.code == C.SCAPE_EINVAL
+    with pytest.raises(C.ScapeError) as ei:        # misaligned workspace
+        C.scape_bind(h, 256, 512, [1024] * 4, 4096 + 8, ws)
+    assert ei.value.code == C.SCAPE_EINVAL
+    with pytest.raises(C.ScapeError) as ei:        # misaligned residual
+        C.scape_bind(h, 256, 512, [1024, 1028, 2048, 4096], 8192, ws)
+    assert ei.value.code == C.SCAPE_EINVAL
+    C.scape_destroy(h)
+
+
+def test_kernel_names(lib):
+    names = [C.scape_kernel_name(i) for i in range(C.SCAPE_NUM_KERNELS)]
+    assert len(set(names)) == C.SCAPE_NUM_KERNELS and all(names)
+    assert C.scape_kernel_name(C.SCAPE_NUM_KERNELS) == ""

@@ -1,0 +1,248 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, element by
+element, on identical seeded inputs.
+
+Bars: masks, packed indices and packed values bit-exact given identical
+inputs; float states within 1e-5 relative / 1e-7 absolute after the
+trajectory, with at most 1e-4 of the mask bits flipped at the threshold.  (The
+kernels follow the oracle's operation order, so in practice every value is
+bit-identical; `rep.exact` records that and is asserted too.)
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+from sparse_communication_sharded_gb300 import ScapeError, synth
+from tests._harness import HP, bits_to_bool, make_opt, run_full_trajectory, run_sampled_shards, u32
+
+pytestmark = pytest.mark.gpu
+
+
+def _wl(P, W, s, dtype, steps=10, quant=False, noise="gauss"):
+    return synth.Workload(f"p{P}", (("flat", P),), W=W, sparsity=s, steps=steps,
+                          grad_dtype=dtype, noise=noise,
+                          quantum=2.0 ** -15 if quant else None)
+
+
+# ------------------------------------------------------------ whole-problem trajectories
+TRAJ = [
+    # (P, W, sparsity, grad dtype, quantised)
+    (4096, 4, 0.90, "f32", False),      # the tiny workload
+    (5003, 3, 0.90, "f32", False),      # ragged tail, non-power-of-two W
+    (100003, 8, 0.99, "bf16", False),   # several tiles, ragged, bf16
+    (65536, 1, 0.90, "bf16", False),    # single worker
+    (20000, 8, 0.0, "f32", False),      # sparsity 0: dense AdamS every step
+    (50000, 32, 0.999, "f32", True),    # 256-level gradients: massive ties
+    (33333, 7, 0.99, "f32", True),      # ties + shard boundaries mid-word
+    (5, 8, 0.5, "f32", False),          # P < W: empty shards
+    (2048 * 3, 2, 0.75, "bf16", False),  # exact multiple of the tile
+]
+
+
+@pytest.mark.parametrize("P,W,s,dtype,quant", TRAJ)
+def test_trajectory_matches_oracle(cuda_device, P, W, s, dtype, quant):
+    rep = run_full_trajectory(_wl(P, W, s, dtype, quant=quant), cuda_device, steps=10)
+    assert rep.exact, "trajectory not bit-identical to the oracle"
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_unaligned_gradients_scalar_path(cuda_device, dtype):
+    rep = run_full_trajectory(_wl(30001, 4, 0.9, dtype), cuda_device, steps=5, grad_offset_elems=1)
+    assert rep.exact
+
+
+def test_flat_sweep_small_points(cuda_device):
+    """The flat sweep's 2^20 point at every W and sparsity (256-level gradients)."""
+    for W in (1, 8, 32):
+        for s in (0.0, 0.9, 0.99, 0.999):
+            rep = run_full_trajectory(synth.flat_workload(1 << 20, W, s), cuda_device, steps=5)
+            assert rep.exact, (W, s)
+
+
+# ------------------------------------------------------------ mask refresh on identical m
+def _refresh_on(cuda_device, m_host: np.ndarray, W: int, s: float):
+    P = m_host.size
+    params = torch.zeros(P, device=cuda_device)
+    opt = make_opt(params, W, s, torch.float32)
+    grads = [torch.zeros(P, device=cuda_device) for _ in range(W)]
+    opt.step(grads)                       # t = 1 so a refresh is legal
+    opt.m.copy_(torch.from_numpy(m_host))
+    opt.refresh_mask()
+    torch.cuda.synchronize()
+    start, ks = O.layout(P, W, s)
+    bits, idx = O.topk_mask(m_host, start, ks)
+    got_bits, got_idx = u32(opt.bits()), u32(opt.idx())
+    opt.close()
+    return got_bits, got_idx, bits, idx
+
+
+M_CASES = {
+    "gauss": lambda r, n: (r.standard_normal(n) * 1e-3).astype(np.float32),
+    "all_equal": lambda r, n: np.full(n, 0.25, np.float32),
+    "levels": lambda r, n: (r.integers(-128, 128, n) * 2.0 ** -15).astype(np.float32),
+    "signed_zero": lambda r, n: np.where(r.random(n) < 0.5, -0.0, 0.0).astype(np.float32),
+    "denormal": lambda r, n: (r.standard_normal(n) * 1e-41).astype(np.float32),
+    "huge": lambda r, n: (r.standard_normal(n) * 1e37).astype(np.float32),
+    "few_levels": lambda r, n: r.choice(np.array([1.0, -1.0, 0.5, 0.0], np.float32), n),
+}
+
+
+@pytest.mark.parametrize("case", sorted(M_CASES))
+@pytest.mark.parametrize("P,W,s", [(70001, 5, 0.9), (4096, 4, 0.99), (300000, 32, 0.999),
+                                   (1000, 1, 0.5)])
+def test_refresh_bit_exact_on_same_m(cuda_device, case, P, W, s):
+    m = M_CASES[case](np.random.default_rng(P + W), P)
+    got_bits, got_idx, bits, idx = _refresh_on(cuda_device, m, W, s)
+    assert np.array_equal(got_bits, bits)
+    assert np.array_equal(got_idx, idx.view(np.uint32))
+
+
+# ------------------------------------------------------------ lag, checkpoint, host path
+def test_lag_step_uses_previous_refresh(cuda_device):
+    P, W, s = 40000, 4, 0.9
+    wl = _wl(P, W, s, "f32")
+    gen = synth.GradientStream(wl, seed=3, device=cuda_device)
+    params = synth.init_params(P, seed=3, device=cuda_device)
+    opt = make_opt(params, W, s, torch.float32)
+    bufs = gen.alloc()
+    gen.next_into(bufs)
+    opt.step(bufs)
+    opt.refresh_mask()
+    for _ in range(3):
+        idx_built = opt.idx().clone()
+        e_before = [x.clone() for x in opt.e]
+        gen.next_into(bufs)
+        opt.step(bufs)
+        torch.cuda.synchronize()
+        used = idx_built.long().cpu().numpy()
+        for w in range(W):
+            a = bufs[w].cpu().numpy() + e_before[w].cpu().numpy()      # fl(g + e)
+            assert np.array_equal(u32(opt.pack()[w]), a[used].view(np.uint32))
+        opt.refresh_mask()
+    opt.close()
+
+
+def test_checkpoint_resume_bit_identical(cuda_device):
+    P, W, s = 60000, 4, 0.99
+    wl = _wl(P, W, s, "bf16")
+
+    def run(split):
+        gen = synth.GradientStream(wl, seed=5, device=cuda_device)
+        params = synth.init_params(P, seed=5, device=cuda_device)
+        opt = make_opt(params, W, s, torch.bfloat16)
+        bufs = gen.alloc()
+        for t in range(10):
+            if t == split:
+                saved = (params.clone(), opt.m.clone(), [x.clone() for x in opt.e],
+                         opt.bits().clone(), opt.t)
+                opt.close()
+                params = saved[0]
+                opt = make_opt(params, W, s, torch.bfloat16)
+                opt.m.copy_(saved[1])
+                for dst, src in zip(opt.e, saved[2]):
+                    dst.copy_(src)
+                opt.set_state(saved[4], saved[3])
+            gen.next_into(bufs)
+            opt.step(bufs)
+            opt.refresh_mask()
+        torch.cuda.synchronize()
+        out = (u32(params), u32(opt.m), [u32(x) for x in opt.e], u32(opt.bits()))
+        opt.close()
+        return out
+
+    a, b = run(None), run(5)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    assert all(np.array_equal(x, y) for x, y in zip(a[2], b[2]))
+    assert np.array_equal(a[3], b[3])
+
+
+def test_set_state_rejects_wrong_counts(cuda_device):
+    P, W, s = 10000, 4, 0.9
+    params = torch.zeros(P, device=cuda_device)
+    opt = make_opt(params, W, s, torch.float32)
+    bad = torch.zeros((P + 31) // 32, dtype=torch.int32, device=cuda_device)
+    with pytest.raises(ScapeError):
+        opt.set_state(1, bad)
+    opt.close()
+
+
+def test_host_buffer_path_matches_device_path(cuda_device):
+    P, W, s = 50000, 4, 0.9
+    wl = _wl(P, W, s, "bf16")
+    outs = []
+    for host in (False, True):
+        gen = synth.GradientStream(wl, seed=9, device="cpu")
+        params = synth.init_params(P, seed=9).to(cuda_device)
+        opt = make_opt(params, W, s, torch.bfloat16)
+        dev = [torch.empty(P, dtype=torch.bfloat16, device=cuda_device) for _ in range(W)]
+        pin = [torch.empty(P, dtype=torch.bfloat16).pin_memory() for _ in range(W)]
+        out = torch.empty(P, dtype=torch.float32).pin_memory()
+        for _ in range(4):
+            grads = gen.next()
+            if host:
+                for p_, g in zip(pin, grads):
+                    p_.copy_(g)
+                opt.step_host(pin, dev, out)
+            else:
+                for d, g in zip(dev, grads):
+                    d.copy_(g)
+                opt.step(dev)
+                opt.refresh_mask()
+                out.copy_(params)
+        torch.cuda.synchronize()
+        outs.append(out.numpy().copy())
+        opt.close()
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+
+
+def test_state_errors(cuda_device):
+    P, W = 1000, 2
+    params = torch.zeros(P, device=cuda_device)
+    opt = make_opt(params, W, 0.9, torch.float32)
+    with pytest.raises(ScapeError):
+        opt.refresh_mask()                         # nothing to build a mask from
+    g = [torch.zeros(P, device=cuda_device) for _ in range(W)]
+    opt.step(g)
+    with pytest.raises(ScapeError):
+        opt.step(g)                                # no mask built after step 1
+    opt.close()
+
+
+def test_profiling_counts_launches(cuda_device):
+    P, W = 100000, 4
+    params = torch.zeros(P, device=cuda_device)
+    opt = make_opt(params, W, 0.9, torch.float32)
+    g = [torch.randn(P, device=cuda_device) * 1e-3 for _ in range(W)]
+    opt.profile(True)
+    n0 = opt.launch_count()
+    for _ in range(3):
+        opt.step(g)
+        opt.refresh_mask()
+    torch.cuda.synchronize()
+    opt.profile_collect()
+    prof = opt.profile_read()
+    assert prof["ef_compact"][1] == 2 and prof["dense_step"][1] == 1
+    assert prof["ef_compact"][0] > 0
+    assert opt.launch_count() - n0 == sum(n for _, n in prof.values())
+    opt.close()
+
+
+# ------------------------------------------------------------ full-size workloads, sampled shards
+@pytest.mark.parametrize("name,steps,shards", [
+    ("gpt345m", 3, (0, 7)),
+    ("llama500m", 3, (0, 17, 31)),
+    ("llama1p8b", 2, (3,)),
+])
+def test_full_size_sampled_shards(cuda_device, name, steps, shards):
+    wl = synth.WORKLOADS[name]
+    free, _ = torch.cuda.mem_get_info()
+    rep = run_sampled_shards(wl, cuda_device, steps, shards)
+    assert rep.exact
+    torch.cuda.empty_cache()
+
+
+def test_flat_sweep_largest_point_sampled(cuda_device):
+    wl = synth.flat_workload(1 << 30, 8, 0.99)
+    rep = run_sampled_shards(wl, cuda_device, 3, (0, 7))
+    assert rep.exact
+    torch.cuda.empty_cache()
