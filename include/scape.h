@@ -212,6 +212,36 @@ const char *scape_kernel_name(int i);
 /* Total kernel launches made through this handle since creation. */
 int64_t scape_launch_count(const scape_t *h);
 
+/*
+ * Per-shard top-k mask that allocates nothing.  The SCAPE pages have no
+ * counterpart to this entry point; it exists for callers that cannot call
+ * cudaMalloc where they need a mask -- code running inside a custom device
+ * allocator or memory-pool callback (allocating would re-enter it), plug-ins
+ * handed only input and output buffers, loops that cannot take cudaMalloc's
+ * implicit device synchronisation -- and so cannot supply the workspace of
+ * scape_bind().
+ *
+ * Computes the same mask as scape_refresh_mask() does for a handle with this
+ * P, W and sparsity: bits[ceil(P/32)] (bit i % 32 of word i / 32) and the
+ * ascending index list idx[k], k = sum_s k_s.  m (float32, P, 16-byte
+ * aligned), bits and idx are the caller's device buffers.  Scratch lives in
+ * one fixed __device__ array inside the library (under 1 MiB, held by every
+ * GPU that loads the library until the process exits); no call allocates
+ * device or host memory.  All calls share that array and it keeps the last
+ * call's contents: calls that overlap on the GPU race and must be ordered by
+ * the caller.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.
+ * Limits: 1 <= P <= SCAPE_STATIC_MAX_P, 1 <= W <= SCAPE_STATIC_MAX_WORKERS;
+ * larger sizes, NULL pointers, a misaligned m or sparsity outside [0, 1)
+ * return SCAPE_EINVAL without touching the GPU; CUDA failures return
+ * SCAPE_ECUDA.  Work is enqueued on `stream`.
+ */
+#define SCAPE_STATIC_MAX_P (1LL << 26)
+#define SCAPE_STATIC_MAX_WORKERS 64
+int scape_topk_mask_static(const float *m, int64_t P, int W, double sparsity, uint32_t *bits,
+                           uint32_t *idx, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

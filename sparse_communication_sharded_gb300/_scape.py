@@ -55,6 +55,7 @@ _PROTOS = {
     "scape_profile_reset": (_i32, [_vp]),
     "scape_kernel_name": (ctypes.c_char_p, [_i32]),
     "scape_launch_count": (_i64, [_vp]),
+    "scape_topk_mask_static": (_i32, [_vp, _i64, _i32, _f64, _vp, _vp, _vp]),
 }
 
 
@@ -198,3 +199,13 @@ def scape_kernel_name(i):
 
 def scape_launch_count(h):
     return load().scape_launch_count(h)
+
+
+SCAPE_STATIC_MAX_P = 1 << 26
+SCAPE_STATIC_MAX_WORKERS = 64
+
+
+def scape_topk_mask_static(m_ptr, P, W, sparsity, bits_ptr, idx_ptr, stream=0):
+    """Allocation-free per-shard top-k mask; returns the status code."""
+    return load().scape_topk_mask_static(m_ptr, int(P), int(W), float(sparsity), bits_ptr,
+                                         idx_ptr, stream)
