@@ -299,9 +299,8 @@ def bench_gpu(args, wl):
         if n:
             kernels[name] = {"launches": n, "ms_per_step": ms / args.steps,
                              "share": ms / max(sum(m for m, _ in prof.values()), 1e-9)}
-    refresh_ms = sum(prof[k][0] for k in ("radix_hist0", "radix_hist1", "radix_hist2",
-                                          "radix_select", "tie_count", "tie_select", "mark",
-                                          "scan", "index")) / args.steps
+    step_kernels = ("dense_step", "ef_compact", "reduce", "adams_sparse")
+    refresh_ms = sum(ms for name, (ms, _) in prof.items() if name not in step_kernels) / args.steps
 
     # end to end through the C ABI from pinned host memory
     e2e = None

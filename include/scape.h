@@ -202,7 +202,7 @@ int scape_step_host(scape_t *h, const void *const *host_grads_src,
  * scape_profile_read() copies the totals (milliseconds and launch counts,
  * SCAPE_NUM_KERNELS entries each) and scape_kernel_name() names entry i.
  */
-#define SCAPE_NUM_KERNELS 15
+#define SCAPE_NUM_KERNELS 13
 int scape_profile_enable(scape_t *h, int on);
 int scape_profile_collect(scape_t *h);
 int scape_profile_read(const scape_t *h, double *host_ms, int64_t *host_launches);

@@ -104,6 +104,9 @@ radix_select_kernel(const int64_t* __restrict__ shard_start, const int64_t* __re
     st.need = 0;
     st.count_eq = 0;
     st.istar = s_hi - 1;
+    st.cprefix = 0;
+    st.guess = kNoGuess;
+    st.flags = 0;
     if (n <= 0 || k <= 0) st.mode = kSelEmpty;
     else if (k >= n) st.mode = kSelDone;  // every key selected: kstar = 0, istar = last
     else st.mode = kSelSearch;
@@ -251,52 +254,81 @@ tie_select_kernel(const float* __restrict__ m, const int64_t* __restrict__ shard
 }
 
 // ------------------------------------------------------------------ mark
-// One block per 2048-parameter tile; warp q covers words 8q..8q+7 of the tile,
-// lane l decides parameter 32*word + l, a ballot assembles each word.
-__global__ void __launch_bounds__(256)
+// One 128-thread block per 2048-parameter tile.  Warp q covers parameters
+// [512q, 512q + 512) of the tile in four rounds of 128: lane l decides the four
+// parameters of one 16-byte load, the 4-bit pieces of 8 neighbouring lanes are
+// OR-ed into one 32-bit word by shuffles, and lane 8g writes word g of the round.
+__global__ void __launch_bounds__(128)
 mark_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __restrict__ shard_start,
             const ShardSel* __restrict__ sel, uint32_t* __restrict__ bits,
             uint32_t* __restrict__ tile_cnt) {
-  __shared__ uint32_t warp_tot[8];
+  __shared__ uint32_t warp_cnt[4];
   const int64_t tile = blockIdx.x;
   const int64_t t0 = tile * kTile;
   const int64_t t1 = min(t0 + (int64_t)kTile, P);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int s = shard_of(t0, P, W);
+  const int s = shard_of(t0, P, W);
   const bool uniform = __ldg(shard_start + s + 1) >= t1;
-  uint32_t kstar = sel[s].kstar;
-  int64_t istar = sel[s].istar;
+  const uint32_t kstar_s = sel[s].kstar;
+  const int64_t istar_s = sel[s].istar;
+  const int64_t wb = t0 + warp * 512;
+  const bool full = t0 + kTile <= P;
 
-  const int64_t wbase = tile * kTileWords + warp * 8;
-  float x[8];
+  float4 v[4];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int64_t i = (wbase + j) * 32 + lane;
-    x[j] = (i < P) ? __ldcs(m + i) : 0.f;
-  }
-  uint32_t myword = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int64_t i = (wbase + j) * 32 + lane;
-    bool on = false;
-    if (i < P) {
-      if (!uniform) {
-        int si = s;
-        while (si < W - 1 && i >= __ldg(shard_start + si + 1)) ++si;
-        kstar = sel[si].kstar;
-        istar = sel[si].istar;
-      }
-      const uint32_t key = magnitude_key(x[j]);
-      on = key > kstar || (key == kstar && i <= istar);
+  for (int r = 0; r < 4; ++r) {
+    const int64_t i0 = wb + 128 * r + 4 * lane;
+    if (full) {
+      v[r] = __ldcs(reinterpret_cast<const float4*>(m + i0));
+    } else {
+      v[r].x = i0 < P ? __ldcs(m + i0) : 0.f;
+      v[r].y = i0 + 1 < P ? __ldcs(m + i0 + 1) : 0.f;
+      v[r].z = i0 + 2 < P ? __ldcs(m + i0 + 2) : 0.f;
+      v[r].w = i0 + 3 < P ? __ldcs(m + i0 + 3) : 0.f;
     }
-    const uint32_t word = __ballot_sync(0xffffffffu, on);
-    if (lane == j) myword = word;
   }
   const int64_t nwords = (P + 31) / 32;
-  if (lane < 8 && wbase + lane < nwords) bits[wbase + lane] = myword;
-  uint32_t total;
-  block_exclusive_scan<256>(lane < 8 ? __popc(myword) : 0u, warp_tot, &total);
-  if (threadIdx.x == 0) tile_cnt[tile] = total;
+  uint32_t cnt = 0;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int64_t i0 = wb + 128 * r + 4 * lane;
+    const float x[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+    uint32_t nib = 0;
+    if (uniform && full) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t key = magnitude_key(x[q]);
+        nib |= (uint32_t)(key > kstar_s || (key == kstar_s && i0 + q <= istar_s)) << q;
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int64_t i = i0 + q;
+        if (i < P) {
+          int si = s;
+          while (si < W - 1 && i >= __ldg(shard_start + si + 1)) ++si;
+          const uint32_t kstar = sel[si].kstar;
+          const int64_t istar = sel[si].istar;
+          const uint32_t key = magnitude_key(x[q]);
+          nib |= (uint32_t)(key > kstar || (key == kstar && i <= istar)) << q;
+        }
+      }
+    }
+    uint32_t word = nib << (4 * (lane & 7));
+    word |= __shfl_xor_sync(0xffffffffu, word, 1);
+    word |= __shfl_xor_sync(0xffffffffu, word, 2);
+    word |= __shfl_xor_sync(0xffffffffu, word, 4);
+    const int64_t widx = (wb + 128 * r) / 32 + (lane >> 3);
+    if ((lane & 7) == 0) {
+      if (widx < nwords) bits[widx] = word;
+      cnt += __popc(word);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  if (lane == 0) warp_cnt[warp] = cnt;
+  __syncthreads();
+  if (threadIdx.x == 0) tile_cnt[tile] = warp_cnt[0] + warp_cnt[1] + warp_cnt[2] + warp_cnt[3];
 }
 
 // Per-tile popcount of an existing bitmap (checkpoint resume).
@@ -313,42 +345,79 @@ tile_count_kernel(const uint32_t* __restrict__ bits, int64_t nwords, uint32_t* _
 }
 
 // ------------------------------------------------------------------ scan
-// Exclusive scan of the per-tile counts in one block; tile_base[ntiles] = total.
-__global__ void __launch_bounds__(1024)
-scan_kernel(const uint32_t* __restrict__ cnt, int64_t n, uint32_t* __restrict__ base) {
-  __shared__ uint32_t warp_tot[32];
-  const int64_t per = (n + 1023) / 1024;
-  const int64_t c0 = min(n, per * threadIdx.x), c1 = min(n, c0 + per);
-  uint32_t local = 0;
-  for (int64_t c = c0; c < c1; ++c) local += cnt[c];
-  uint32_t total;
-  uint32_t run = block_exclusive_scan<1024>(local, warp_tot, &total);
-  for (int64_t c = c0; c < c1; ++c) {
-    const uint32_t v = cnt[c];
-    base[c] = run;
-    run += v;
+// Exclusive scan of the per-tile counts into the rank table, in three
+// launches: local scans of 2048-tile chunks, a scan of the chunk totals
+// (at most 512 chunks for P < 2^31), and the chunk offsets added back.
+constexpr int kScanChunk = 2048;
+
+__global__ void __launch_bounds__(256)
+scan_local_kernel(const uint32_t* __restrict__ cnt, int64_t n, uint32_t* __restrict__ base,
+                  uint32_t* __restrict__ chunk_tot) {
+  __shared__ uint32_t warp_tot[8];
+  const int64_t c0 = (int64_t)blockIdx.x * kScanChunk + threadIdx.x * 8;
+  uint32_t v[8], local = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    v[j] = c0 + j < n ? cnt[c0 + j] : 0u;
+    local += v[j];
   }
-  if (threadIdx.x == 0) base[n] = total;
+  uint32_t total;
+  uint32_t run = block_exclusive_scan<256>(local, warp_tot, &total);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (c0 + j < n) base[c0 + j] = run;
+    run += v[j];
+  }
+  if (threadIdx.x == 0) chunk_tot[blockIdx.x] = total;
+}
+
+__global__ void __launch_bounds__(1024)
+scan_top_kernel(const uint32_t* __restrict__ chunk_tot, int64_t nchunks,
+                uint32_t* __restrict__ chunk_base, uint32_t* __restrict__ base_total) {
+  __shared__ uint32_t warp_tot[32];
+  const uint32_t v = threadIdx.x < nchunks ? chunk_tot[threadIdx.x] : 0u;
+  uint32_t total;
+  const uint32_t ex = block_exclusive_scan<1024>(v, warp_tot, &total);
+  if (threadIdx.x < nchunks) chunk_base[threadIdx.x] = ex;
+  if (threadIdx.x == 0) *base_total = total;
+}
+
+__global__ void __launch_bounds__(256)
+scan_add_kernel(uint32_t* __restrict__ base, int64_t n, const uint32_t* __restrict__ chunk_base) {
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t < n) base[t] += chunk_base[t / kScanChunk];
 }
 
 // ------------------------------------------------------------------ index
-// idx[rank] = i for every set bit, ranks ascending: one block per tile,
-// 8 parameters (one bitmap byte) per thread.
-__global__ void __launch_bounds__(kTileThreads)
-index_kernel(const uint32_t* __restrict__ bits, int64_t P, const uint32_t* __restrict__ tile_base,
-             uint32_t* __restrict__ idx) {
-  __shared__ uint32_t warp_tot[kTileThreads / 32];
-  const int64_t tile = blockIdx.x;
-  const int64_t i0 = tile * kTile + (int64_t)threadIdx.x * 8;
-  uint32_t byte = 0;
-  if (i0 < P) byte = (__ldg(bits + (i0 >> 5)) >> (uint32_t)(i0 & 31)) & 0xFFu;
-  uint32_t total;
-  const uint32_t excl = block_exclusive_scan<kTileThreads>(__popc(byte), warp_tot, &total);
-  uint32_t* out = idx + __ldg(tile_base + tile) + excl;
-  int r = 0;
+// idx[rank] = i for every set bit, ranks ascending.  One warp per tile (eight
+// tiles per block); lane l owns bitmap words 2l and 2l + 1 of its tile.
+__global__ void __launch_bounds__(256)
+index_kernel(const uint32_t* __restrict__ bits, int64_t P, int64_t ntiles,
+             const uint32_t* __restrict__ tile_base, uint32_t* __restrict__ idx) {
+  const int lane = threadIdx.x & 31;
+  const int64_t tile = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (tile >= ntiles) return;
+  const int64_t nwords = (P + 31) / 32;
+  const int64_t w0 = tile * kTileWords + 2 * lane;
+  uint32_t a = w0 < nwords ? __ldg(bits + w0) : 0u;
+  uint32_t b = w0 + 1 < nwords ? __ldg(bits + w0 + 1) : 0u;
+  const uint32_t c = __popc(a) + __popc(b);
+  uint32_t x = c;
 #pragma unroll
-  for (int j = 0; j < 8; ++j)
-    if ((byte >> j) & 1u) out[r++] = (uint32_t)(i0 + j);
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  uint32_t* out = idx + __ldg(tile_base + tile) + (x - c);
+  const uint32_t ia = (uint32_t)(w0 * 32), ib = ia + 32;
+  while (a) {
+    *out++ = ia + (uint32_t)(__ffs(a) - 1);
+    a &= a - 1;
+  }
+  while (b) {
+    *out++ = ib + (uint32_t)(__ffs(b) - 1);
+    b &= b - 1;
+  }
 }
 
 // Per-shard popcount of a bitmap plus the count of bits set past P (in
@@ -406,7 +475,7 @@ cudaError_t launch_mark(const float* m, int64_t P, int W, const int64_t* shard_s
                         const ShardSel* sel, uint32_t* bits, uint32_t* tile_cnt,
                         cudaStream_t st) {
   const unsigned grid = (unsigned)((P + kTile - 1) / kTile);
-  mark_kernel<<<grid, 256, 0, st>>>(m, P, W, shard_start, sel, bits, tile_cnt);
+  mark_kernel<<<grid, 128, 0, st>>>(m, P, W, shard_start, sel, bits, tile_cnt);
   return cudaGetLastError();
 }
 
@@ -417,16 +486,28 @@ cudaError_t launch_tile_count(const uint32_t* bits, int64_t P, uint32_t* tile_cn
   return cudaGetLastError();
 }
 
+int64_t scan_scratch_words(int64_t ntiles) { return 2 * ((ntiles + kScanChunk - 1) / kScanChunk); }
+
 cudaError_t launch_scan(const uint32_t* tile_cnt, int64_t ntiles, uint32_t* tile_base,
-                        cudaStream_t st) {
-  scan_kernel<<<1, 1024, 0, st>>>(tile_cnt, ntiles, tile_base);
+                        uint32_t* scratch, cudaStream_t st) {
+  const int64_t nchunks = (ntiles + kScanChunk - 1) / kScanChunk;
+  if (nchunks > 1024) return cudaErrorInvalidValue;
+  uint32_t* chunk_tot = scratch;
+  uint32_t* chunk_base = scratch + nchunks;
+  scan_local_kernel<<<(unsigned)nchunks, 256, 0, st>>>(tile_cnt, ntiles, tile_base, chunk_tot);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  scan_top_kernel<<<1, 1024, 0, st>>>(chunk_tot, nchunks, chunk_base, tile_base + ntiles);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  scan_add_kernel<<<(unsigned)((ntiles + 255) / 256), 256, 0, st>>>(tile_base, ntiles, chunk_base);
   return cudaGetLastError();
 }
 
 cudaError_t launch_index(const uint32_t* bits, int64_t P, const uint32_t* tile_base,
                          uint32_t* idx, cudaStream_t st) {
-  const unsigned grid = (unsigned)((P + kTile - 1) / kTile);
-  index_kernel<<<grid, kTileThreads, 0, st>>>(bits, P, tile_base, idx);
+  const int64_t ntiles = (P + kTile - 1) / kTile;
+  index_kernel<<<(unsigned)((ntiles + 7) / 8), 256, 0, st>>>(bits, P, ntiles, tile_base, idx);
   return cudaGetLastError();
 }
 

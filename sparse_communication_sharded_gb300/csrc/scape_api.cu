@@ -23,12 +23,13 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 thread_local std::string g_create_error;
 
 const char* const kKernelNames[kNumKernels] = {
-    "dense_step", "ef_compact", "reduce",      "adams_sparse", "radix_hist0",
-    "radix_hist1", "radix_hist2", "radix_select", "tie_count",   "tie_select",
-    "mark",        "scan",        "index",        "shard_count", "tile_count"};
+    "dense_step",  "ef_compact", "reduce", "adams_sparse", "cand_hist0", "cand_select",
+    "cand_collect", "cand_hist",  "mark",   "scan",         "index",      "shard_count",
+    "tile_count"};
 
 struct ProfRec {
   int kid;
+  int nlaunch;
   cudaEvent_t a, b;
 };
 
@@ -43,11 +44,13 @@ struct scape {
   int dtype = SCAPE_BF16;
   std::vector<int64_t> shard_start, shard_k;
   int64_t k = 0;
-  int64_t ntiles = 0, nwords = 0, kstride = 0, nchunk = 0;
+  int64_t ntiles = 0, nwords = 0, kstride = 0;
+  int cand_blocks = 1;  // blocks per shard of the candidate histogram passes
   bool all_dense = false;  // every shard keeps all of its coordinates
   // workspace offsets (bytes)
   size_t off_bits = 0, off_idx = 0, off_tbase = 0, off_tcnt = 0, off_pack = 0, off_gbar = 0,
-         off_hist = 0, off_sel = 0, off_eqcnt = 0, off_sstart = 0, off_sk = 0, off_counts = 0,
+         off_hist = 0, off_sel = 0, off_cand = 0, off_ccnt = 0, off_scan = 0, off_sstart = 0,
+         off_sk = 0, off_counts = 0,
          ws_need = 0;
   // bound memory
   bool bound = false;
@@ -78,7 +81,9 @@ struct scape {
   float* gbar() const { return at<float>(off_gbar); }
   uint32_t* hist() const { return at<uint32_t>(off_hist); }
   ShardSel* sel() const { return at<ShardSel>(off_sel); }
-  uint32_t* eqcnt() const { return at<uint32_t>(off_eqcnt); }
+  uint2* cand() const { return at<uint2>(off_cand); }
+  uint32_t* cand_cnt() const { return at<uint32_t>(off_ccnt); }
+  uint32_t* scan_scratch() const { return at<uint32_t>(off_scan); }
   int64_t* d_shard_start() const { return at<int64_t>(off_sstart); }
   int64_t* d_shard_k() const { return at<int64_t>(off_sk); }
   uint32_t* counts() const { return at<uint32_t>(off_counts); }
@@ -109,7 +114,7 @@ cudaEvent_t take_event(scape_t* h) {
 // Enqueue one kernel through `fn` (which returns the launch status), with
 // optional event bracketing for per-kernel timing.
 template <class F>
-int run_kernel(scape_t* h, int kid, cudaStream_t st, F&& fn) {
+int run_kernel(scape_t* h, int kid, cudaStream_t st, F&& fn, int nlaunch = 1) {
   cudaEvent_t a = nullptr, b = nullptr;
   if (h->prof) {
     a = take_event(h);
@@ -117,10 +122,10 @@ int run_kernel(scape_t* h, int kid, cudaStream_t st, F&& fn) {
     if (a && b) cudaEventRecord(a, st);
   }
   const cudaError_t e = fn();
-  h->launches++;
+  h->launches += nlaunch;
   if (h->prof && a && b) {
     cudaEventRecord(b, st);
-    h->pending.push_back({kid, a, b});
+    h->pending.push_back({kid, nlaunch, a, b});
   }
   if (e != cudaSuccess) return cuda_fail(h, e, kKernelNames[kid]);
   return SCAPE_OK;
@@ -150,8 +155,10 @@ int rebuild_from_bits(scape_t* h, cudaStream_t st, bool counts_ready) {
                     [&] { return launch_tile_count(h->bits(), h->P, h->tile_cnt(), st); });
     if (rc) return rc;
   }
-  rc = run_kernel(h, kKScan, st,
-                  [&] { return launch_scan(h->tile_cnt(), h->ntiles, h->tile_base(), st); });
+  rc = run_kernel(
+      h, kKScan, st,
+      [&] { return launch_scan(h->tile_cnt(), h->ntiles, h->tile_base(), h->scan_scratch(), st); },
+      kScanLaunches);
   if (rc) return rc;
   return run_kernel(h, kKIndex, st,
                     [&] { return launch_index(h->bits(), h->P, h->tile_base(), h->idx(), st); });
@@ -217,8 +224,9 @@ int scape_create(scape_t** out, int n_layers, const int64_t* host_layer_numel, i
   h->ntiles = (P + kTile - 1) / kTile;
   h->nwords = (P + 31) / 32;
   h->kstride = (int64_t)align_up((size_t)(h->k > 0 ? h->k : 1), 64);
-  h->nchunk = (nmax + kTieChunk - 1) / kTieChunk;
-  if (h->nchunk < 1) h->nchunk = 1;
+  // candidate passes: about 1200 blocks in total, at least one per shard
+  h->cand_blocks = W >= 1200 ? 1 : 1200 / W;
+  (void)nmax;
 
   size_t off = 0;
   auto carve = [&](size_t bytes) {
@@ -232,9 +240,12 @@ int scape_create(scape_t** out, int n_layers, const int64_t* host_layer_numel, i
   h->off_tcnt = carve((size_t)h->ntiles * 4);
   h->off_pack = carve((size_t)W * h->kstride * 4);
   h->off_gbar = carve((size_t)h->kstride * 4);
-  h->off_hist = carve((size_t)W * kBins * 4);
+  h->off_hist = carve((size_t)W * kCandBins0 * 4);
   h->off_sel = carve((size_t)W * sizeof(ShardSel));
-  h->off_eqcnt = carve((size_t)W * h->nchunk * 4);
+  // candidates of shard s live in [shard_start[s], shard_start[s+1]): capacity = shard size
+  h->off_cand = carve((size_t)P * sizeof(uint2));
+  h->off_ccnt = carve((size_t)W * 4);
+  h->off_scan = carve((size_t)scan_scratch_words(h->ntiles) * 4);
   h->off_sstart = carve((size_t)(W + 1) * 8);
   h->off_sk = carve((size_t)W * 8);
   h->off_counts = carve((size_t)(W + 1) * 4);
@@ -301,6 +312,9 @@ int scape_bind(scape_t* h, float* params, float* m, float* const* host_e_ptrs, v
   if (e == cudaSuccess)
     e = cudaMemcpy(h->d_shard_k(), h->shard_k.data(), 8 * h->W, cudaMemcpyHostToDevice);
   if (e != cudaSuccess) return cuda_fail(h, e, "scape_bind: shard table upload");
+  // no previous mask: every shard starts without a bucket guess
+  e = cudaMemset(h->sel(), 0xFF, sizeof(ShardSel) * h->W);
+  if (e != cudaSuccess) return cuda_fail(h, e, "scape_bind: select state reset");
   h->bound = true;
   h->t = 0;
   h->mask_ready = false;
@@ -360,38 +374,38 @@ int scape_refresh_mask(scape_t* h, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int rc;
   if (!h->all_dense) {
-    cudaError_t e = cudaMemsetAsync(h->hist(), 0, (size_t)h->W * kBins * 4, st);
+    cudaError_t e = cudaMemsetAsync(h->hist(), 0, (size_t)h->W * kCandBins0 * 4, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->cand_cnt(), 0, (size_t)h->W * 4, st);
     if (e != cudaSuccess) return cuda_fail(h, e, "scape_refresh_mask: histogram clear");
-    rc = run_kernel(h, kKHist0, st, [&] {
-      return launch_hist(0, h->m, h->P, h->W, h->d_shard_start(), h->sel(), h->hist(), st);
+    rc = run_kernel(h, kKCandHist0, st, [&] {
+      return launch_chist0(h->m, h->P, h->W, h->d_shard_start(), h->sel(), h->hist(), h->cand(),
+                           h->cand_cnt(), st);
     });
     if (rc) return rc;
   }
-  rc = run_kernel(h, kKSelect, st, [&] {
-    return launch_select(0, h->W, h->d_shard_start(), h->d_shard_k(), h->sel(), h->hist(), st);
+  rc = run_kernel(h, kKCandSelect, st, [&] {
+    return launch_cselect(0, h->W, h->d_shard_start(), h->d_shard_k(), h->sel(), h->hist(),
+                          h->cand_cnt(), st);
   });
   if (rc) return rc;
   if (!h->all_dense) {
-    for (int pass = 1; pass <= 2; ++pass) {
-      rc = run_kernel(h, pass == 1 ? kKHist1 : kKHist2, st, [&] {
-        return launch_hist(pass, h->m, h->P, h->W, h->d_shard_start(), h->sel(), h->hist(), st);
+    rc = run_kernel(h, kKCandCollect, st, [&] {
+      return launch_collect(h->m, h->P, h->W, h->d_shard_start(), h->sel(), h->cand(),
+                            h->cand_cnt(), st);
+    });
+    if (rc) return rc;
+    for (int pass = 1; pass <= 5; ++pass) {
+      rc = run_kernel(h, kKCandHist, st, [&] {
+        return launch_chist(pass, h->W, h->cand_blocks, h->d_shard_start(), h->sel(), h->cand(),
+                            h->cand_cnt(), h->hist(), st);
       });
       if (rc) return rc;
-      rc = run_kernel(h, kKSelect, st, [&] {
-        return launch_select(pass, h->W, h->d_shard_start(), h->d_shard_k(), h->sel(), h->hist(),
-                             st);
+      rc = run_kernel(h, kKCandSelect, st, [&] {
+        return launch_cselect(pass, h->W, h->d_shard_start(), h->d_shard_k(), h->sel(), h->hist(),
+                              h->cand_cnt(), st);
       });
       if (rc) return rc;
     }
-    rc = run_kernel(h, kKTieCount, st, [&] {
-      return launch_tie_count(h->m, h->W, h->d_shard_start(), h->sel(), h->eqcnt(), h->nchunk, st);
-    });
-    if (rc) return rc;
-    rc = run_kernel(h, kKTieSelect, st, [&] {
-      return launch_tie_select(h->m, h->W, h->d_shard_start(), h->sel(), h->eqcnt(), h->nchunk,
-                               st);
-    });
-    if (rc) return rc;
   }
   rc = run_kernel(h, kKMark, st, [&] {
     return launch_mark(h->m, h->P, h->W, h->d_shard_start(), h->sel(), h->bits(), h->tile_cnt(),
@@ -512,7 +526,7 @@ int scape_profile_collect(scape_t* h) {
       rc = cuda_fail(h, e, "scape_profile_collect");
     } else {
       h->prof_ms[r.kid] += ms;
-      h->prof_n[r.kid] += 1;
+      h->prof_n[r.kid] += r.nlaunch;
     }
     h->pool.push_back(r.a);
     h->pool.push_back(r.b);

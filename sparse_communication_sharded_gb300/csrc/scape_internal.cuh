@@ -48,7 +48,12 @@ struct ShardSel {
   uint32_t need;      // how many keys == kstar are selected (lowest indices)
   uint32_t count_eq;  // how many keys == kstar the shard holds
   int64_t istar;      // keys == kstar with index <= istar are selected
+  uint64_t cprefix;   // composite-key bits fixed so far (candidate select)
+  uint32_t guess;     // first-digit bucket of the previous refresh (0xFFFFFFFF: none)
+  uint32_t flags;     // kSelNeedCollect: candidates must be gathered by a second pass
 };
+constexpr uint32_t kNoGuess = 0xFFFFFFFFu;
+constexpr uint32_t kSelNeedCollect = 1u;
 
 // AdamS constants of one step; all computed on the host in float.
 struct AdamsConst {
@@ -61,12 +66,10 @@ enum KernelId {
   kKEfCompact,
   kKReduce,
   kKAdamsSparse,
-  kKHist0,
-  kKHist1,
-  kKHist2,
-  kKSelect,
-  kKTieCount,
-  kKTieSelect,
+  kKCandHist0,
+  kKCandSelect,
+  kKCandCollect,
+  kKCandHist,
   kKMark,
   kKScan,
   kKIndex,
@@ -154,10 +157,25 @@ cudaError_t launch_mark(const float* m, int64_t P, int W, const int64_t* shard_s
                         cudaStream_t st);
 cudaError_t launch_tile_count(const uint32_t* bits, int64_t P, uint32_t* tile_cnt,
                               cudaStream_t st);
+// Three launches; `scratch` holds scan_scratch_words(ntiles) words.
+int64_t scan_scratch_words(int64_t ntiles);
 cudaError_t launch_scan(const uint32_t* tile_cnt, int64_t ntiles, uint32_t* tile_base,
-                        cudaStream_t st);
+                        uint32_t* scratch, cudaStream_t st);
+constexpr int kScanLaunches = 3;
 cudaError_t launch_index(const uint32_t* bits, int64_t P, const uint32_t* tile_base,
                          uint32_t* idx, cudaStream_t st);
+// candidate-based exact top-k threshold (topk_kernels.cu)
+constexpr int kCandBins0 = 4096;
+cudaError_t launch_chist0(const float* m, int64_t P, int W, const int64_t* shard_start,
+                          const ShardSel* sel, uint32_t* hist, uint2* cand, uint32_t* cand_cnt,
+                          cudaStream_t st);
+cudaError_t launch_cselect(int pass, int W, const int64_t* shard_start, const int64_t* shard_k,
+                           ShardSel* sel, uint32_t* hist, uint32_t* cand_cnt, cudaStream_t st);
+cudaError_t launch_collect(const float* m, int64_t P, int W, const int64_t* shard_start,
+                           const ShardSel* sel, uint2* cand, uint32_t* cand_cnt, cudaStream_t st);
+cudaError_t launch_chist(int pass, int W, int blocks_per_shard, const int64_t* shard_start,
+                         const ShardSel* sel, const uint2* cand, const uint32_t* cand_cnt,
+                         uint32_t* hist, cudaStream_t st);
 cudaError_t launch_shard_count(const uint32_t* bits, int64_t P, int64_t nwords, int W,
                                uint32_t* counts, cudaStream_t st);
 

@@ -39,6 +39,7 @@ constexpr size_t kTileCntBytes = up((size_t)(kStaticMaxP / kTile + 1) * 4);
 constexpr size_t kTileBaseBytes = up((size_t)(kStaticMaxP / kTile + 2) * 4);
 constexpr size_t kStartBytes = up((size_t)(kStaticMaxW + 1) * 8);
 constexpr size_t kKBytes = up((size_t)kStaticMaxW * 8);
+constexpr size_t kScanBytes = up((size_t)(2 * (kStaticMaxP / kTile / 2048 + 1)) * 4);
 
 constexpr size_t kOffHist = 0;
 constexpr size_t kOffSel = kOffHist + kHistBytes;
@@ -47,7 +48,8 @@ constexpr size_t kOffTileCnt = kOffEq + kEqBytes;
 constexpr size_t kOffTileBase = kOffTileCnt + kTileCntBytes;
 constexpr size_t kOffStart = kOffTileBase + kTileBaseBytes;
 constexpr size_t kOffK = kOffStart + kStartBytes;
-constexpr size_t kScratchBytes = kOffK + kKBytes;
+constexpr size_t kOffScan = kOffK + kKBytes;
+constexpr size_t kScratchBytes = kOffScan + kScanBytes;
 static_assert(kScratchBytes < (1u << 20), "static scratch must stay under 1 MiB");
 
 __device__ __align__(256) unsigned char g_static_scratch[kScratchBytes];
@@ -124,6 +126,7 @@ extern "C" int scape_topk_mask_static(const float* m, int64_t P, int W, double s
   uint32_t* tile_base = reinterpret_cast<uint32_t*>(base + kOffTileBase);
   const int64_t* start = reinterpret_cast<const int64_t*>(base + kOffStart);
   const int64_t* ks = reinterpret_cast<const int64_t*>(base + kOffK);
+  uint32_t* scan_scratch = reinterpret_cast<uint32_t*>(base + kOffScan);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   // the histogram rows must start at zero; everything else is rewritten
@@ -145,7 +148,8 @@ extern "C" int scape_topk_mask_static(const float* m, int64_t P, int W, double s
       return SCAPE_ECUDA;
   }
   if ((e = launch_mark(m, P, W, start, sel, bits, tile_cnt, st)) != cudaSuccess) return SCAPE_ECUDA;
-  if ((e = launch_scan(tile_cnt, ntiles, tile_base, st)) != cudaSuccess) return SCAPE_ECUDA;
+  if ((e = launch_scan(tile_cnt, ntiles, tile_base, scan_scratch, st)) != cudaSuccess)
+    return SCAPE_ECUDA;
   if ((e = launch_index(bits, P, tile_base, idx, st)) != cudaSuccess) return SCAPE_ECUDA;
   return SCAPE_OK;
 }
