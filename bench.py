@@ -59,10 +59,16 @@ def algorithmic_bytes(wl, k):
 
 
 def _kernel_source_hash():
-    h = hashlib.sha256()
-    for name in ("step_kernels.cu", "scape_internal.cuh"):
-        with open(os.path.join(ROOT, "sparse_communication_sharded_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+    """Hash of the ef_compact kernel's own source (its section of
+    step_kernels.cu) and of the shared header it includes."""
+    csrc = os.path.join(ROOT, "sparse_communication_sharded_gb300", "csrc")
+    with open(os.path.join(csrc, "step_kernels.cu")) as f:
+        src = f.read()
+    a = src.index("// ------------------------------------------------------------------ ef_compact")
+    b = src.index("// ------------------------------------------------------------------ dense_step")
+    h = hashlib.sha256(src[a:b].encode())
+    with open(os.path.join(csrc, "scape_internal.cuh"), "rb") as f:
+        h.update(f.read())
     return h.hexdigest()[:16]
 
 

@@ -189,8 +189,12 @@ int scape_set_state(scape_t *h, int64_t t, const uint32_t *bits, void *stream);
  * End-to-end step from host memory: copy each worker's gradient from host
  * memory (pinned for asynchronous copies) into the caller's device gradient
  * buffers, run scape_step() and scape_refresh_mask(), then copy w[P] back to
- * host_params_out.  All on `stream`; the caller synchronises before reading
- * host_params_out.
+ * host_params_out.  From step 2 on, the uploads run on an internal copy stream
+ * in up to 8 worker groups and each group's compaction starts on `stream` as
+ * soon as its gradients have landed; the parameter download overlaps the mask
+ * refresh.  All of the call's work is ordered before later work on `stream`:
+ * synchronise `stream` before reading host_params_out or reusing the host
+ * gradient buffers.  The first call creates the copy stream and its events.
  */
 int scape_step_host(scape_t *h, const void *const *host_grads_src,
                     void *const *host_dev_grad_ptrs, float *host_params_out, void *stream);

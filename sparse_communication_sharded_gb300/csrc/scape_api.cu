@@ -63,6 +63,12 @@ struct scape {
   bool mask_ready = false;
   bool buffers_valid = false;
   int64_t launches = 0;
+  // end-to-end pipelining (created on the first scape_step_host call)
+  static constexpr int kMaxGroups = 8;
+  bool aux_ready = false;
+  cudaStream_t copy_stream = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_updated = nullptr, ev_done = nullptr;
+  cudaEvent_t ev_group[kMaxGroups] = {};
   // profiling
   bool prof = false;
   std::vector<ProfRec> pending;
@@ -146,6 +152,31 @@ AdamsConst make_const(const scape_t* h, int64_t t) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Compaction of workers [w0, w1) into rows w0.. of the packed buffers.
+int enqueue_compact(scape_t* h, const WorkerPtrs& all, int w0, int w1, bool vec, cudaStream_t st) {
+  WorkerPtrs p;
+  std::memset(&p, 0, sizeof p);
+  for (int w = w0; w < w1; ++w) {
+    p.g[w - w0] = all.g[w];
+    p.e[w - w0] = all.e[w];
+  }
+  return run_kernel(h, kKEfCompact, st, [&] {
+    return launch_ef_compact(p, w1 - w0, h->P, h->dtype, vec, h->bits(), h->tile_base(),
+                             h->pack() + (int64_t)w0 * h->kstride, h->kstride, st);
+  });
+}
+
+// The ordered sum of the packed buffers and the sparse AdamS update.
+int enqueue_update(scape_t* h, const AdamsConst& c, cudaStream_t st) {
+  int rc = run_kernel(h, kKReduce, st, [&] {
+    return launch_reduce(h->pack(), h->kstride, h->W, h->k, h->gbar(), st);
+  });
+  if (rc) return rc;
+  return run_kernel(h, kKAdamsSparse, st, [&] {
+    return launch_adams_sparse(h->idx(), h->gbar(), h->k, h->w, h->m, c, st);
+  });
+}
 
 // Rank table and index list from the bitmap already in the workspace.
 int rebuild_from_bits(scape_t* h, cudaStream_t st, bool counts_ready) {
@@ -261,6 +292,13 @@ void scape_destroy(scape_t* h) {
     cudaEventDestroy(r.b);
   }
   for (auto ev : h->pool) cudaEventDestroy(ev);
+  if (h->aux_ready) {
+    for (auto ev : h->ev_group) cudaEventDestroy(ev);
+    cudaEventDestroy(h->ev_start);
+    cudaEventDestroy(h->ev_updated);
+    cudaEventDestroy(h->ev_done);
+    cudaStreamDestroy(h->copy_stream);
+  }
   delete h;
 }
 
@@ -348,18 +386,9 @@ int scape_step(scape_t* h, const void* const* host_grad_ptrs, void* stream) {
     if (rc) return rc;
     h->buffers_valid = false;
   } else {
-    rc = run_kernel(h, kKEfCompact, st, [&] {
-      return launch_ef_compact(p, h->W, h->P, h->dtype, vec, h->bits(), h->tile_base(), h->pack(),
-                               h->kstride, st);
-    });
+    rc = enqueue_compact(h, p, 0, h->W, vec, st);
     if (rc) return rc;
-    rc = run_kernel(h, kKReduce, st, [&] {
-      return launch_reduce(h->pack(), h->kstride, h->W, h->k, h->gbar(), st);
-    });
-    if (rc) return rc;
-    rc = run_kernel(h, kKAdamsSparse, st, [&] {
-      return launch_adams_sparse(h->idx(), h->gbar(), h->k, h->w, h->m, c, st);
-    });
+    rc = enqueue_update(h, c, st);
     if (rc) return rc;
     h->buffers_valid = true;
   }
@@ -491,21 +520,81 @@ int scape_step_host(scape_t* h, const void* const* host_grads_src, void* const* 
   if (!h->bound) return fail(h, SCAPE_ESTATE, "scape_step_host: call scape_bind first");
   if (!host_grads_src || !host_dev_grad_ptrs || !host_params_out)
     return fail(h, SCAPE_EINVAL, "scape_step_host: NULL pointer");
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const size_t gbytes = (size_t)h->P * (h->dtype == SCAPE_BF16 ? 2 : 4);
-  for (int w = 0; w < h->W; ++w) {
+  for (int w = 0; w < h->W; ++w)
     if (!host_grads_src[w] || !host_dev_grad_ptrs[w])
       return fail(h, SCAPE_EINVAL, "scape_step_host: NULL gradient pointer");
-    cudaError_t e = cudaMemcpyAsync(host_dev_grad_ptrs[w], host_grads_src[w], gbytes,
-                                    cudaMemcpyHostToDevice, st);
+  if (h->t >= 1 && !h->mask_ready)
+    return fail(h, SCAPE_ESTATE, "scape_step_host: no mask yet; refresh after step 1");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t gbytes = (size_t)h->P * (h->dtype == SCAPE_BF16 ? 2 : 4);
+  cudaError_t e = cudaSuccess;
+  if (h->t == 0) {
+    // dense first step: every worker is needed at once
+    for (int w = 0; w < h->W && e == cudaSuccess; ++w)
+      e = cudaMemcpyAsync(host_dev_grad_ptrs[w], host_grads_src[w], gbytes, cudaMemcpyHostToDevice,
+                          st);
     if (e != cudaSuccess) return cuda_fail(h, e, "scape_step_host: gradient upload");
+    int rc = scape_step(h, reinterpret_cast<const void* const*>(host_dev_grad_ptrs), stream);
+    if (rc) return rc;
+    rc = scape_refresh_mask(h, stream);
+    if (rc) return rc;
+    e = cudaMemcpyAsync(host_params_out, h->w, (size_t)h->P * 4, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return cuda_fail(h, e, "scape_step_host: parameter download");
+    return SCAPE_OK;
   }
-  int rc = scape_step(h, reinterpret_cast<const void* const*>(host_dev_grad_ptrs), stream);
+  if (!h->aux_ready) {
+    e = cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking);
+    for (auto* ev : {&h->ev_start, &h->ev_updated, &h->ev_done})
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    for (int g = 0; g < scape_t::kMaxGroups && e == cudaSuccess; ++g)
+      e = cudaEventCreateWithFlags(&h->ev_group[g], cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(h, e, "scape_step_host: stream/event setup");
+    h->aux_ready = true;
+  }
+  // Worker groups: group g's uploads run on the copy stream while the
+  // compaction of the groups before it runs on `stream`.
+  const int G = h->W < scape_t::kMaxGroups ? h->W : scape_t::kMaxGroups;
+  cudaStream_t cp = h->copy_stream;
+  e = cudaEventRecord(h->ev_start, st);  // earlier users of the gradient buffers
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(cp, h->ev_start, 0);
+  for (int g = 0; g < G && e == cudaSuccess; ++g) {
+    for (int w = g * h->W / G; w < (g + 1) * h->W / G && e == cudaSuccess; ++w)
+      e = cudaMemcpyAsync(host_dev_grad_ptrs[w], host_grads_src[w], gbytes, cudaMemcpyHostToDevice,
+                          cp);
+    if (e == cudaSuccess) e = cudaEventRecord(h->ev_group[g], cp);
+  }
+  if (e != cudaSuccess) return cuda_fail(h, e, "scape_step_host: gradient upload");
+  WorkerPtrs p;
+  std::memset(&p, 0, sizeof p);
+  bool vec = true;
+  for (int w = 0; w < h->W; ++w) {
+    p.g[w] = host_dev_grad_ptrs[w];
+    p.e[w] = h->e[w];
+    vec = vec && aligned16(host_dev_grad_ptrs[w]);
+  }
+  const int64_t t = h->t + 1;
+  const AdamsConst c = make_const(h, t);
+  for (int g = 0; g < G; ++g) {
+    e = cudaStreamWaitEvent(st, h->ev_group[g], 0);
+    if (e != cudaSuccess) return cuda_fail(h, e, "scape_step_host: stream wait");
+    const int rc = enqueue_compact(h, p, g * h->W / G, (g + 1) * h->W / G, vec, st);
+    if (rc) return rc;
+  }
+  int rc = enqueue_update(h, c, st);
   if (rc) return rc;
+  h->t = t;
+  h->buffers_valid = true;
+  // the parameter download overlaps the mask refresh
+  e = cudaEventRecord(h->ev_updated, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(cp, h->ev_updated, 0);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(host_params_out, h->w, (size_t)h->P * 4, cudaMemcpyDeviceToHost, cp);
+  if (e == cudaSuccess) e = cudaEventRecord(h->ev_done, cp);
+  if (e != cudaSuccess) return cuda_fail(h, e, "scape_step_host: parameter download");
   rc = scape_refresh_mask(h, stream);
   if (rc) return rc;
-  cudaError_t e = cudaMemcpyAsync(host_params_out, h->w, (size_t)h->P * 4, cudaMemcpyDeviceToHost, st);
-  if (e != cudaSuccess) return cuda_fail(h, e, "scape_step_host: parameter download");
+  e = cudaStreamWaitEvent(st, h->ev_done, 0);
+  if (e != cudaSuccess) return cuda_fail(h, e, "scape_step_host: stream wait");
   return SCAPE_OK;
 }
 

@@ -31,8 +31,8 @@ __device__ __forceinline__ uint64_t composite(uint32_t key, uint32_t i) {
 
 // ------------------------------------------------------------------ passes over m
 // One kernel for both reads of m.  Blocks are persistent: block b walks a
-// contiguous run of 2048-parameter segments, so it meets at most a few shard
-// boundaries.  Per shard piece it
+// contiguous run of 2048-parameter segments, following the shard boundaries
+// incrementally, so it meets at most a few of them.  Per shard piece it
 //   HIST:    adds the 12-bit first digit of every key to a shared-memory
 //            histogram (flushed to the shard's row when the shard changes), and
 //            stages candidates whose digit lies within one bucket of the
@@ -40,10 +40,11 @@ __device__ __forceinline__ uint64_t composite(uint32_t key, uint32_t i) {
 //            to step, so that bucket usually still holds the threshold;
 //   COLLECT: (second pass, only for shards whose guess missed) stages every
 //            parameter whose digit equals the bucket just selected.
-// Staged candidates go to the shard's range of `cand` with one global atomic
-// per flush of the 3072-entry shared buffer.
-constexpr int kMSeg = 2048;   // parameters per segment (256 threads x 2 x float4)
-constexpr int kStage = 3072;  // staged candidates; flushed when a segment might not fit
+// Each warp stages its candidates in a private shared-memory buffer (ballot
+// append) and flushes it to the shard's range of `cand` with one global
+// atomic, so segments need no block-wide barrier.
+constexpr int kMSeg = 2048;       // parameters per segment (256 threads x 2 x float4)
+constexpr int kWarpStage = 384;   // staged candidates per warp
 
 template <bool HIST>
 __global__ void __launch_bounds__(256)
@@ -51,114 +52,139 @@ mpass_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __res
              const ShardSel* __restrict__ sel, uint32_t* __restrict__ hist,
              uint2* __restrict__ cand, uint32_t* __restrict__ cand_cnt, int64_t segs_per_block) {
   __shared__ uint32_t sh[HIST ? kCBins0 : 1];
-  __shared__ uint2 sbuf[kStage];
-  __shared__ uint32_t s_n, s_base;
+  __shared__ uint2 wbuf[8][kWarpStage];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t nseg = (P + kMSeg - 1) / kMSeg;
   const int64_t g0 = (int64_t)blockIdx.x * segs_per_block;
   const int64_t g1 = min(g0 + segs_per_block, nseg);
   if (g0 >= g1) return;
-  if (HIST)
+  const int64_t r0 = g0 * kMSeg, r1 = min(g1 * kMSeg, P);
+  int s = shard_of(r0, P, W);
+  if (!HIST) {
+    // nothing to do unless a shard of this block's range must be collected
+    bool any = false;
+    for (int q = s; q < W && __ldg(shard_start + q) < r1; ++q)
+      any |= sel[q].mode == kSelSearch && (sel[q].flags & kSelNeedCollect);
+    if (!any) return;
+  }
+  if (HIST) {
     for (int b = threadIdx.x; b < kCBins0; b += blockDim.x) sh[b] = 0;
-  if (threadIdx.x == 0) s_n = 0;
-  __syncthreads();
-
-  int cur = -1;               // shard whose histogram / staged candidates are pending
-  bool active = false;        // whether parameters of `cur` are examined at all
-  uint32_t wlo = 1, whi = 0;  // candidate window of first digits (empty when wlo > whi)
-
-  // Every call site is reached by all threads of the block with the same
-  // arguments, after a barrier that made s_n final.
-  auto flush_cand = [&](int shard) {
-    const uint32_t n = s_n;
-    if (n) {
-      if (threadIdx.x == 0) s_base = atomicAdd(cand_cnt + shard, n);
-      __syncthreads();
-      uint2* out = cand + __ldg(shard_start + shard) + s_base;
-      for (uint32_t j = threadIdx.x; j < n; j += blockDim.x) out[j] = sbuf[j];
-      __syncthreads();
-      if (threadIdx.x == 0) s_n = 0;
-      __syncthreads();
-    }
-  };
-  auto flush_hist = [&](int shard) {
-    if (!HIST) return;
-    uint32_t* row = hist + (int64_t)shard * kCBins0;
-    for (int b = threadIdx.x; b < kCBins0; b += blockDim.x) {
-      const uint32_t c = sh[b];
-      if (c) {
-        atomicAdd(row + b, c);
-        sh[b] = 0;
-      }
-    }
     __syncthreads();
-  };
-  auto consider = [&](uint32_t key, int64_t i) {
-    const uint32_t d = key >> 19;
-    if (HIST) atomicAdd(&sh[d], 1u);
-    if (d >= wlo && d <= whi) {
-      const uint32_t pos = atomicAdd(&s_n, 1u);
-      sbuf[pos] = make_uint2(key, (uint32_t)i);
-    }
+  }
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  uint2* const mybuf = wbuf[warp];
+  uint32_t wn = 0;  // entries in this warp's buffer (same value in every lane)
+
+  auto flush_warp = [&](int shard) {
+    if (wn == 0) return;
+    __syncwarp();
+    uint32_t base = 0;
+    if (lane == 0) base = atomicAdd(cand_cnt + shard, wn);
+    base = __shfl_sync(0xffffffffu, base, 0);
+    uint2* out = cand + __ldg(shard_start + shard) + base;
+    for (uint32_t j = lane; j < wn; j += 32) out[j] = mybuf[j];
+    __syncwarp();
+    wn = 0;
   };
 
+  int64_t s_hi = __ldg(shard_start + s + 1);
+  uint32_t wlo = 0xFFFFFFFFu, wwid = 0;  // window of digits: d - wlo <= wwid (unsigned)
+  bool active = false;
+  int cur = -1;
   for (int64_t g = g0; g < g1; ++g) {
     const int64_t seg0 = g * kMSeg;
     const int64_t seg1 = min(seg0 + (int64_t)kMSeg, P);
-    int s = shard_of(seg0, P, W);
     for (;;) {
-      const int64_t s_lo = __ldg(shard_start + s), s_hi = __ldg(shard_start + s + 1);
-      const int64_t lo = max(seg0, s_lo), hi = min(seg1, s_hi);
-      if (lo < hi) {
-        if (s != cur) {
-          if (cur >= 0) {
-            flush_cand(cur);
-            if (active) flush_hist(cur);
-          }
-          cur = s;
-          const ShardSel ss = sel[s];
+      while (seg0 >= s_hi && s < W - 1) s_hi = __ldg(shard_start + (++s) + 1);
+      if (s != cur) {
+        if (cur >= 0) {
+          flush_warp(cur);
           if (HIST) {
-            active = true;
-            wlo = 1;
-            whi = 0;
-            if (ss.guess != kNoGuess) {
-              wlo = ss.guess > 0 ? ss.guess - 1 : 0;
-              whi = ss.guess + 1;
+            __syncthreads();
+            uint32_t* row = hist + (int64_t)cur * kCBins0;
+            for (int b = threadIdx.x; b < kCBins0; b += blockDim.x) {
+              const uint32_t c = sh[b];
+              if (c) {
+                atomicAdd(row + b, c);
+                sh[b] = 0;
+              }
             }
-          } else {
-            active = ss.mode == kSelSearch && (ss.flags & kSelNeedCollect);
-            wlo = whi = (uint32_t)ss.cprefix;
+            __syncthreads();
           }
         }
-        if (active) {
-          if (lo == seg0 && hi - lo == kMSeg) {
-            const float4* p4 = reinterpret_cast<const float4*>(m + seg0);
-            float4 v[kMSeg / 4 / 256];
-#pragma unroll
-            for (int r = 0; r < kMSeg / 4 / 256; ++r) v[r] = __ldcs(p4 + threadIdx.x + 256 * r);
-#pragma unroll
-            for (int r = 0; r < kMSeg / 4 / 256; ++r) {
-              const int64_t i0 = seg0 + 4 * ((int64_t)threadIdx.x + 256 * r);
-              consider(magnitude_key(v[r].x), i0);
-              consider(magnitude_key(v[r].y), i0 + 1);
-              consider(magnitude_key(v[r].z), i0 + 2);
-              consider(magnitude_key(v[r].w), i0 + 3);
-            }
-          } else {
-            for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x)
-              consider(magnitude_key(__ldcs(m + i)), i);
+        cur = s;
+        const ShardSel ss = sel[s];
+        if (HIST) {
+          active = true;
+          wlo = 0xFFFFFFFFu;
+          wwid = 0;
+          if (ss.guess != kNoGuess) {
+            wlo = ss.guess > 0 ? ss.guess - 1 : 0;
+            wwid = ss.guess + 1 - wlo;
           }
-          __syncthreads();
-          // keep room for a whole segment in the staging buffer
-          if (s_n > (uint32_t)(kStage - kMSeg)) flush_cand(cur);
+        } else {
+          active = ss.mode == kSelSearch && (ss.flags & kSelNeedCollect);
+          wlo = (uint32_t)ss.cprefix;
+          wwid = 0;
+        }
+      }
+      const int64_t lo = max(seg0, __ldg(shard_start + s)), hi = min(seg1, s_hi);
+      if (active && lo < hi) {
+        if (lo == seg0 && hi - lo == kMSeg) {
+          const float4* p4 = reinterpret_cast<const float4*>(m + seg0);
+          float4 v[kMSeg / 4 / 256];
+#pragma unroll
+          for (int r = 0; r < kMSeg / 4 / 256; ++r) v[r] = __ldcs(p4 + threadIdx.x + 256 * r);
+#pragma unroll
+          for (int r = 0; r < kMSeg / 4 / 256; ++r) {
+            const uint32_t i0 = (uint32_t)(seg0 + 4 * (threadIdx.x + 256 * r));
+            const float x[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint32_t key = magnitude_key(x[q]);
+              const uint32_t d = key >> 19;
+              if (HIST) atomicAdd(&sh[d], 1u);
+              const bool hit = d - wlo <= wwid;
+              const uint32_t ball = __ballot_sync(0xffffffffu, hit);
+              if (ball) {
+                if (hit) mybuf[wn + __popc(ball & lt_mask)] = make_uint2(key, i0 + q);
+                wn += __popc(ball);
+                if (wn > kWarpStage - 32) flush_warp(s);
+              }
+            }
+          }
+        } else {
+          // shard piece: warp-uniform trip count so ballots see every lane
+          for (int64_t b0 = lo; b0 < hi; b0 += 256) {
+            const int64_t i = b0 + threadIdx.x;
+            const bool in = i < hi;
+            const uint32_t key = in ? magnitude_key(__ldcs(m + i)) : 0u;
+            const uint32_t d = key >> 19;
+            if (HIST && in) atomicAdd(&sh[d], 1u);
+            const bool hit = in && d - wlo <= wwid;
+            const uint32_t ball = __ballot_sync(0xffffffffu, hit);
+            if (ball) {
+              if (hit) mybuf[wn + __popc(ball & lt_mask)] = make_uint2(key, (uint32_t)i);
+              wn += __popc(ball);
+              if (wn > kWarpStage - 32) flush_warp(s);
+            }
+          }
         }
       }
       if (s_hi >= seg1 || s == W - 1) break;
-      ++s;
+      s_hi = __ldg(shard_start + (++s) + 1);
     }
   }
   if (cur >= 0) {
-    flush_cand(cur);
-    if (active) flush_hist(cur);
+    flush_warp(cur);
+    if (HIST) {
+      __syncthreads();
+      uint32_t* row = hist + (int64_t)cur * kCBins0;
+      for (int b = threadIdx.x; b < kCBins0; b += blockDim.x) {
+        const uint32_t c = sh[b];
+        if (c) atomicAdd(row + b, c);
+      }
+    }
   }
 }
 
