@@ -62,7 +62,14 @@ def _load():
         lib.oracle_topk_mask.argtypes = [vp, i64, i32, vp, vp, vp, vp, vp]
         lib.oracle_step.argtypes = [i64, i64, i32, i32, vp, vp, vp, vp, vp, vp, i64,
                                     f32, f32, f32, f32, f32, vp, vp]
-        for fn in (lib.oracle_layout, lib.oracle_topk_mask, lib.oracle_step):
+        lib.oracle_step_variant.argtypes = [i64, i64, i32, i32, vp, vp, vp, vp, vp, vp, i64,
+                                            f32, f32, f32, f32, f32, i32, vp, vp]
+        lib.oracle_dense_adams_step.argtypes = [i64, i64, i32, i32, vp, vp, vp,
+                                                f32, f32, f32, f32, f32]
+        lib.oracle_adamw_step.argtypes = [i64, i64, i32, i32, vp, vp, vp, vp,
+                                          f32, f32, f32, f32, f32]
+        for fn in (lib.oracle_layout, lib.oracle_topk_mask, lib.oracle_step,
+                   lib.oracle_step_variant, lib.oracle_dense_adams_step, lib.oracle_adamw_step):
             fn.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -136,6 +143,53 @@ def step(t: int, grads, e, w: np.ndarray, m: np.ndarray, bits: np.ndarray,
     return pack[:, :k], gbar[:k]
 
 
+# variant readings (flags, combinable)
+DENSE_OFFMASK = 1   # unselected coordinates take the AdamS update with a zero gradient
+MOMENT_SYNC = 2     # the synchronised buffer holds first moments; g is recovered from it
+
+
+def step_variant(t: int, grads, e, w, m, bits, idx, hp: Hyper, variant: int):
+    """step() under a variant reading; returns (pack, synchronised buffer)."""
+    W = len(grads)
+    P = w.size
+    dtype = BF16 if grads[0].dtype == np.uint16 else F32
+    k = idx.size
+    pack = np.zeros((W, max(k, 1)), np.float32)
+    gbar = np.zeros(max(k, 1), np.float32)
+    gp = (ctypes.c_void_p * W)(*[_ptr(g) for g in grads])
+    ep = (ctypes.c_void_p * W)(*[_ptr(x) for x in e])
+    rc = _load().oracle_step_variant(t, P, W, dtype, ctypes.addressof(gp), ctypes.addressof(ep),
+                                     _ptr(w), _ptr(m), _ptr(bits), _ptr(idx), k,
+                                     hp.beta1, hp.beta2, hp.lr, hp.eps, hp.weight_decay,
+                                     int(variant), _ptr(pack), _ptr(gbar))
+    if rc != 0:
+        raise ValueError("oracle_step_variant failed")
+    return pack[:, :k], gbar[:k]
+
+
+def dense_adams_step(t: int, grads, w, m, hp: Hyper):
+    """Dense AdamS on the plain mean of the workers' gradients (no error feedback)."""
+    W = len(grads)
+    dtype = BF16 if grads[0].dtype == np.uint16 else F32
+    gp = (ctypes.c_void_p * W)(*[_ptr(g) for g in grads])
+    rc = _load().oracle_dense_adams_step(t, w.size, W, dtype, ctypes.addressof(gp), _ptr(w),
+                                         _ptr(m), hp.beta1, hp.beta2, hp.lr, hp.eps,
+                                         hp.weight_decay)
+    if rc != 0:
+        raise ValueError("oracle_dense_adams_step failed")
+
+
+def adamw_step(t: int, grads, w, m, v, hp: Hyper):
+    """Dense AdamW (EMA second moment) on the plain mean of the gradients."""
+    W = len(grads)
+    dtype = BF16 if grads[0].dtype == np.uint16 else F32
+    gp = (ctypes.c_void_p * W)(*[_ptr(g) for g in grads])
+    rc = _load().oracle_adamw_step(t, w.size, W, dtype, ctypes.addressof(gp), _ptr(w), _ptr(m),
+                                   _ptr(v), hp.beta1, hp.beta2, hp.lr, hp.eps, hp.weight_decay)
+    if rc != 0:
+        raise ValueError("oracle_adamw_step failed")
+
+
 def dense_mask(P: int):
     """The all-ones mask of step 1 and its index list."""
     bits = np.full((P + 31) // 32, 0xFFFFFFFF, np.uint32)
@@ -169,14 +223,17 @@ def new_state(w0: np.ndarray, W: int, sparsity: float, hp: Hyper,
                  shard_start=shard_start, shard_k=shard_k, hp=hp)
 
 
-def advance(st: State, grads, keep=None) -> dict:
+def advance(st: State, grads, keep=None, variant: int = 0) -> dict:
     """Step t+1 with the lagged mask, then refresh the mask from the new m."""
     t = st.t + 1
     if st.bits is None:
         used_bits, used_idx = dense_mask(st.w.size)
     else:
         used_bits, used_idx = st.bits, st.idx
-    pack, gbar = step(t, grads, st.e, st.w, st.m, used_bits, used_idx, st.hp)
+    if variant:
+        pack, gbar = step_variant(t, grads, st.e, st.w, st.m, used_bits, used_idx, st.hp, variant)
+    else:
+        pack, gbar = step(t, grads, st.e, st.w, st.m, used_bits, used_idx, st.hp)
     st.t = t
     st.bits, st.idx = topk_mask(st.m, st.shard_start, st.shard_k)
     rec = {"t": t, "used_bits": used_bits, "used_idx": used_idx, "pack": pack,

@@ -223,3 +223,144 @@ int oracle_step(int64_t t, int64_t P, int W, int grad_dtype, const void *const *
     }
     return ORACLE_OK;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Variant readings of the pages, selected by flags (one step, given mask).  */
+/*                                                                            */
+/* ORACLE_VARIANT_DENSE_OFFMASK: the other reading of what happens off the    */
+/*   mask -- every unselected coordinate also takes the AdamS update of       */
+/*   [P1] Sec. II-C with a zero synchronised gradient (m decays, v = b2 m^2). */
+/* ORACLE_VARIANT_MOMENT_SYNC: the single synchronised buffer holds the       */
+/*   first moment ([P2] Sec. 2, "deriving the global mean gradient ... from   */
+/*   the synchronised first-moment buffer"): each worker sends                */
+/*   b = b1 m_{t-1} + (1 - b1) a at its selected coordinates, the buffer is   */
+/*   the mean of the b, m_t is that mean, and the gradient the second moment  */
+/*   needs is recovered as g = (b_mean - b1 m_{t-1}) / (1 - b1).              */
+/* The residual is the unsent part of g + e in both ([P1] Sec. II-B).        */
+/* ------------------------------------------------------------------------- */
+#define ORACLE_VARIANT_DENSE_OFFMASK 1
+#define ORACLE_VARIANT_MOMENT_SYNC 2
+
+static void adams_one(float g, float *wi, float *mi, float beta1, float beta2, float bc1,
+                      float bc2, float lr, float eps, float wd)
+{
+    float m_prev = *mi, w_prev = *wi;
+    float m_new = beta1 * m_prev + (1.0f - beta1) * g;
+    float v = beta2 * (m_prev * m_prev) + (1.0f - beta2) * (g * g);
+    float m_hat = m_new / bc1;
+    float v_hat = v / bc2;
+    *wi = w_prev - lr * (m_hat / (sqrtf(v_hat) + eps) + wd * w_prev);
+    *mi = m_new;
+}
+
+int oracle_step_variant(int64_t t, int64_t P, int W, int grad_dtype, const void *const *grads,
+                        float *const *e, float *w, float *m, const uint32_t *bits,
+                        const uint32_t *idx, int64_t k, float beta1, float beta2, float lr,
+                        float eps, float wd, int variant, float *pack, float *gbar)
+{
+    if (t < 1 || P < 0 || W < 1 || k < 0 || k > P)
+        return ORACLE_EINVAL;
+    if (grad_dtype != ORACLE_F32 && grad_dtype != ORACLE_BF16)
+        return ORACLE_EINVAL;
+    int msync = (variant & ORACLE_VARIANT_MOMENT_SYNC) != 0;
+    float one_minus_b1 = 1.0f - beta1;
+    float one_minus_b2 = 1.0f - beta2;
+    float bc1 = (float)(1.0 - pow((double)beta1, (double)t));
+    float bc2 = (float)(1.0 - pow((double)beta2, (double)t));
+
+    for (int wk = 0; wk < W; ++wk) {
+        int64_t r = 0;
+        for (int64_t i = 0; i < P; ++i) {
+            float a = widen_grad(grads[wk], grad_dtype, i) + e[wk][i];
+            int selected = (bits[i / 32] >> (i % 32)) & 1u;
+            float sent = selected ? a : 0.0f;
+            if (selected) {
+                if (r >= k)
+                    return ORACLE_EINVAL;
+                pack[(int64_t)wk * k + r] = msync ? beta1 * m[i] + one_minus_b1 * a : a;
+                r = r + 1;
+            }
+            e[wk][i] = a - sent;
+        }
+        if (r != k)
+            return ORACLE_EINVAL;
+    }
+    for (int64_t j = 0; j < k; ++j) {
+        float sum = pack[j];
+        for (int wk = 1; wk < W; ++wk)
+            sum = sum + pack[(int64_t)wk * k + j];
+        gbar[j] = sum / (float)W;
+    }
+    for (int64_t j = 0; j < k; ++j) {
+        int64_t i = idx[j];
+        if (!msync) {
+            adams_one(gbar[j], &w[i], &m[i], beta1, beta2, bc1, bc2, lr, eps, wd);
+        } else {
+            float m_prev = m[i], w_prev = w[i];
+            float m_new = gbar[j];
+            float g = (m_new - beta1 * m_prev) / one_minus_b1;
+            float v = beta2 * (m_prev * m_prev) + one_minus_b2 * (g * g);
+            float m_hat = m_new / bc1;
+            float v_hat = v / bc2;
+            w[i] = w_prev - lr * (m_hat / (sqrtf(v_hat) + eps) + wd * w_prev);
+            m[i] = m_new;
+        }
+    }
+    if (variant & ORACLE_VARIANT_DENSE_OFFMASK) {
+        for (int64_t i = 0; i < P; ++i)
+            if (!((bits[i / 32] >> (i % 32)) & 1u))
+                adams_one(0.0f, &w[i], &m[i], beta1, beta2, bc1, bc2, lr, eps, wd);
+    }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Dense baselines the pages compare SCAPE against (abstract, Sec. I): dense */
+/* AdamS ([P1] Sec. II-C, Eq. 2) and dense AdamW, both on the plain mean of   */
+/* the W workers' gradients (no error feedback, no mask).  AdamW keeps the   */
+/* second moment as an EMA of g^2: v_t = b2 v_{t-1} + (1 - b2) g^2, with the */
+/* same bias corrections and decoupled weight decay.                         */
+/* ------------------------------------------------------------------------- */
+static float mean_grad(const void *const *grads, int W, int grad_dtype, int64_t i)
+{
+    float sum = widen_grad(grads[0], grad_dtype, i);
+    for (int wk = 1; wk < W; ++wk)
+        sum = sum + widen_grad(grads[wk], grad_dtype, i);
+    return sum / (float)W;
+}
+
+int oracle_dense_adams_step(int64_t t, int64_t P, int W, int grad_dtype,
+                            const void *const *grads, float *w, float *m, float beta1,
+                            float beta2, float lr, float eps, float wd)
+{
+    if (t < 1 || P < 0 || W < 1 || (grad_dtype != ORACLE_F32 && grad_dtype != ORACLE_BF16))
+        return ORACLE_EINVAL;
+    float bc1 = (float)(1.0 - pow((double)beta1, (double)t));
+    float bc2 = (float)(1.0 - pow((double)beta2, (double)t));
+    for (int64_t i = 0; i < P; ++i)
+        adams_one(mean_grad(grads, W, grad_dtype, i), &w[i], &m[i], beta1, beta2, bc1, bc2, lr,
+                  eps, wd);
+    return ORACLE_OK;
+}
+
+int oracle_adamw_step(int64_t t, int64_t P, int W, int grad_dtype, const void *const *grads,
+                      float *w, float *m, float *v, float beta1, float beta2, float lr,
+                      float eps, float wd)
+{
+    if (t < 1 || P < 0 || W < 1 || (grad_dtype != ORACLE_F32 && grad_dtype != ORACLE_BF16))
+        return ORACLE_EINVAL;
+    float bc1 = (float)(1.0 - pow((double)beta1, (double)t));
+    float bc2 = (float)(1.0 - pow((double)beta2, (double)t));
+    for (int64_t i = 0; i < P; ++i) {
+        float g = mean_grad(grads, W, grad_dtype, i);
+        float w_prev = w[i];
+        float m_new = beta1 * m[i] + (1.0f - beta1) * g;
+        float v_new = beta2 * v[i] + (1.0f - beta2) * (g * g);
+        float m_hat = m_new / bc1;
+        float v_hat = v_new / bc2;
+        w[i] = w_prev - lr * (m_hat / (sqrtf(v_hat) + eps) + wd * w_prev);
+        m[i] = m_new;
+        v[i] = v_new;
+    }
+    return ORACLE_OK;
+}
