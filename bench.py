@@ -247,7 +247,7 @@ def bench_gpu(args, wl):
     seed = 1000 * rank
     params = synth.init_params(P, seed=seed, device=dev)
     opt = pkg.Scape(params, W, wl.sparsity, layer_numel=[n for _, n in wl.layers],
-                    grad_dtype=gdt)
+                    grad_dtype=gdt, residuals=args.residuals)
     gen = synth.GradientStream(wl, seed=seed, device=dev)
     grads = gen.alloc()
 
@@ -308,6 +308,11 @@ def bench_gpu(args, wl):
     step_kernels = ("dense_step", "ef_compact", "reduce", "adams_sparse")
     refresh_ms = sum(ms for name, (ms, _) in prof.items() if name not in step_kernels) / args.steps
 
+    # dense baselines on the same workload and buffers (after the SCAPE timing)
+    baselines = None
+    if args.baselines:
+        baselines = bench_baselines(opt, wl, grads, dev)
+
     # end to end through the C ABI from pinned host memory
     e2e = None
     if args.e2e_steps > 0:
@@ -328,7 +333,8 @@ def bench_gpu(args, wl):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": wl.name, "P": P, "W": W, "sparsity": wl.sparsity,
                        "k": opt.k, "grad_dtype": wl.grad_dtype, "state_dtype": "f32",
-                       "l2": "inputs larger than L2 (gradients + residuals resident in HBM)",
+                       "residuals": args.residuals,
+                       "l2": "inputs larger than L2 (gradients + residuals far beyond 129 MB)",
                        "parallelism": f"{ws} independent problems (weak)"},
             "hbm_gbs": alg["total"] / (t_max / 1000.0) / 1e9,
             "hbm_frac": alg["total"] / (t_max / 1000.0) / 1e9 / peak,
@@ -343,6 +349,7 @@ def bench_gpu(args, wl):
             "gpu_launches": launches,
             "clocks": clocks,
             "e2e": e2e,
+            "baselines": baselines,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -351,6 +358,35 @@ def bench_gpu(args, wl):
         dist.destroy_process_group()
     opt.close()
     return 0
+
+
+def bench_baselines(opt, wl, grads, dev, warmup=2, steps=5):
+    """Per-step time of the dense AdamS and AdamW baselines (plain mean of the
+    W gradients, every coordinate updated) on the same device buffers."""
+    import torch
+
+    P, W, G = wl.P, wl.W, _grad_bytes(wl)
+    out = {}
+    v = torch.zeros(P, dtype=torch.float32, device=dev)
+    st = torch.cuda.current_stream()
+    for name, fn, state_bytes in (("dense_adams", lambda: opt.dense_adams_step(grads), 16),
+                                  ("adamw", lambda: opt.adamw_step(grads, v), 24)):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(st)
+        for _ in range(steps):
+            fn()
+        ev1.record(st)
+        torch.cuda.synchronize()
+        ms = ev0.elapsed_time(ev1) / steps
+        alg = W * P * G + state_bytes * P
+        out[name] = {"ms_per_step": ms, "params_per_s": P / (ms / 1000.0),
+                     "hbm_gbs": alg / (ms / 1000.0) / 1e9}
+    del v
+    torch.cuda.empty_cache()
+    return out
 
 
 def bench_e2e(opt, wl, dev_grads, steps, dev):
@@ -397,6 +433,10 @@ def main(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-steps", type=int, default=2)
+    ap.add_argument("--residuals", default="device", choices=["device", "host"],
+                    help="error-feedback buffers in HBM or in pinned host memory")
+    ap.add_argument("--baselines", type=int, default=1,
+                    help="also time the dense AdamS and AdamW baselines (0 to skip)")
     ap.add_argument("--P", type=int, default=None,
                     help="with --workload custom: flat parameter count")
     ap.add_argument("--workers", type=int, default=8, help="with --workload custom: W")

@@ -107,9 +107,13 @@ int scape_workspace_bytes(const scape_t *h, size_t *bytes);
  *   params       float32 w[P], updated in place
  *   m            float32 first moment m[P], updated in place (caller zeroes it
  *                before the first step)
- *   host_e_ptrs  host array of W device pointers, each float32 e^w[P]: the
- *                per-worker error-feedback residual ("SCAPE" Sec. II-B; FP32,
- *                same size as the gradient), updated in place (caller zeroes)
+ *   host_e_ptrs  host array of W device-accessible pointers, each float32
+ *                e^w[P]: the per-worker error-feedback residual ("SCAPE"
+ *                Sec. II-B; FP32, same size as the gradient), updated in place
+ *                (caller zeroes).  They may point to pinned host memory: the
+ *                kernels then read and write the residuals over the host link
+ *                in place, keeping W*P*4 bytes out of HBM (the pages offload
+ *                these buffers to the CPU side, "SCAPE" Sec. I)
  *   workspace    >= scape_workspace_bytes(), 256-byte aligned
  * params, m and every e^w must be 16-byte aligned and must not overlap.
  */
@@ -154,6 +158,39 @@ int scape_step(scape_t *h, const void *const *host_grad_ptrs, void *stream);
  * Errors: SCAPE_ESTATE before the first step.
  */
 int scape_refresh_mask(scape_t *h, void *stream);
+
+/*
+ * Variant readings (flags, combinable; default SCAPE_VARIANT_PAPER).  They
+ * change what later steps compute:
+ *   SCAPE_VARIANT_DENSE_OFFMASK  unselected coordinates also take the AdamS
+ *       update with a zero synchronised gradient (m decays by b1, v = b2 m^2),
+ *       the other reading of "SCAPE" Sec. II-C under a sparse buffer;
+ *   SCAPE_VARIANT_MOMENT_SYNC    the synchronised buffer holds first moments
+ *       ("Sintesi Tecnica: SCAPE" Sec. 2): each worker packs
+ *       b = b1 m_{t-1} + (1 - b1) a, m_t is the mean of the b, and the gradient
+ *       of the second moment is recovered as (m_t - b1 m_{t-1}) / (1 - b1).
+ * Errors: SCAPE_EINVAL for an unknown flag.
+ */
+enum scape_variant {
+    SCAPE_VARIANT_PAPER = 0,
+    SCAPE_VARIANT_DENSE_OFFMASK = 1,
+    SCAPE_VARIANT_MOMENT_SYNC = 2
+};
+int scape_set_variant(scape_t *h, int flags);
+
+/*
+ * Dense baselines the pages compare SCAPE against ("SCAPE" abstract, Sec. I),
+ * on the handle's bound w and m: the gradient is the plain ordered mean of
+ * the W workers' gradients (no error feedback, no mask; residuals untouched)
+ * and every coordinate is updated:
+ *   scape_dense_adams_step  AdamS of "SCAPE" Sec. II-C, Eq. 2;
+ *   scape_adamw_step        AdamW, v_t = b2 v_{t-1} + (1 - b2) g^2 in the
+ *                           caller's float32 v[P] (zero it before step 1).
+ * Both use and advance the handle's step count t for the bias corrections.
+ * Errors as scape_step().
+ */
+int scape_dense_adams_step(scape_t *h, const void *const *host_grad_ptrs, void *stream);
+int scape_adamw_step(scape_t *h, const void *const *host_grad_ptrs, float *v, void *stream);
 
 /* Learning rate for subsequent steps (schedules).  lr must be finite. */
 int scape_set_lr(scape_t *h, float lr);
@@ -206,7 +243,7 @@ int scape_step_host(scape_t *h, const void *const *host_grads_src,
  * scape_profile_read() copies the totals (milliseconds and launch counts,
  * SCAPE_NUM_KERNELS entries each) and scape_kernel_name() names entry i.
  */
-#define SCAPE_NUM_KERNELS 13
+#define SCAPE_NUM_KERNELS 16
 int scape_profile_enable(scape_t *h, int on);
 int scape_profile_collect(scape_t *h);
 int scape_profile_read(const scape_t *h, double *host_ms, int64_t *host_launches);

@@ -19,7 +19,7 @@ SCAPE_ESTATE = -4
 SCAPE_F32 = 0
 SCAPE_BF16 = 1
 SCAPE_MAX_WORKERS = 256
-SCAPE_NUM_KERNELS = 13
+SCAPE_NUM_KERNELS = 16
 
 LIB_PATH = _build.LIB
 
@@ -45,6 +45,9 @@ _PROTOS = {
     "scape_step": (_i32, [_vp, _vp, _vp]),
     "scape_refresh_mask": (_i32, [_vp, _vp]),
     "scape_set_lr": (_i32, [_vp, _f32]),
+    "scape_set_variant": (_i32, [_vp, _i32]),
+    "scape_dense_adams_step": (_i32, [_vp, _vp, _vp]),
+    "scape_adamw_step": (_i32, [_vp, _vp, _vp, _vp]),
     "scape_get_state": (_i32, [_vp, _vp, _vp, _vp, _vp]),
     "scape_get_buffers": (_i32, [_vp, _vp, _vp, _vp]),
     "scape_set_state": (_i32, [_vp, _i64, _vp, _vp]),
@@ -141,6 +144,25 @@ def scape_step(h, grad_ptrs, stream=0):
 
 def scape_refresh_mask(h, stream=0):
     _check(h, load().scape_refresh_mask(h, stream))
+
+
+SCAPE_VARIANT_PAPER = 0
+SCAPE_VARIANT_DENSE_OFFMASK = 1
+SCAPE_VARIANT_MOMENT_SYNC = 2
+
+
+def scape_set_variant(h, flags):
+    _check(h, load().scape_set_variant(h, int(flags)))
+
+
+def scape_dense_adams_step(h, grad_ptrs, stream=0):
+    arr = _ptr_array(grad_ptrs)
+    _check(h, load().scape_dense_adams_step(h, ctypes.addressof(arr), stream))
+
+
+def scape_adamw_step(h, grad_ptrs, v_ptr, stream=0):
+    arr = _ptr_array(grad_ptrs)
+    _check(h, load().scape_adamw_step(h, ctypes.addressof(arr), v_ptr, stream))
 
 
 def scape_set_lr(h, lr):

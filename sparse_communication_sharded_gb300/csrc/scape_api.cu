@@ -25,7 +25,7 @@ thread_local std::string g_create_error;
 const char* const kKernelNames[kNumKernels] = {
     "dense_step",  "ef_compact", "reduce", "adams_sparse", "cand_hist0", "cand_select",
     "cand_collect", "cand_hist",  "mark",   "scan",         "index",      "shard_count",
-    "tile_count"};
+    "tile_count",  "offmask",    "dense_adams", "adamw"};
 
 struct ProfRec {
   int kid;
@@ -47,6 +47,7 @@ struct scape {
   int64_t ntiles = 0, nwords = 0, kstride = 0;
   int cand_blocks = 1;  // blocks per shard of the candidate histogram passes
   bool all_dense = false;  // every shard keeps all of its coordinates
+  int variant = SCAPE_VARIANT_PAPER;
   // workspace offsets (bytes)
   size_t off_bits = 0, off_idx = 0, off_tbase = 0, off_tcnt = 0, off_pack = 0, off_gbar = 0,
          off_hist = 0, off_sel = 0, off_cand = 0, off_ccnt = 0, off_scan = 0, off_sstart = 0,
@@ -155,6 +156,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // Compaction of workers [w0, w1) into rows w0.. of the packed buffers.
 int enqueue_compact(scape_t* h, const WorkerPtrs& all, int w0, int w1, bool vec, cudaStream_t st) {
+  const MomentPack mp{h->m, h->beta1, 1.0f - h->beta1};
+  const MomentPack* mpp = (h->variant & SCAPE_VARIANT_MOMENT_SYNC) ? &mp : nullptr;
   WorkerPtrs p;
   std::memset(&p, 0, sizeof p);
   for (int w = w0; w < w1; ++w) {
@@ -163,19 +166,24 @@ int enqueue_compact(scape_t* h, const WorkerPtrs& all, int w0, int w1, bool vec,
   }
   return run_kernel(h, kKEfCompact, st, [&] {
     return launch_ef_compact(p, w1 - w0, h->P, h->dtype, vec, h->bits(), h->tile_base(),
-                             h->pack() + (int64_t)w0 * h->kstride, h->kstride, st);
+                             h->pack() + (int64_t)w0 * h->kstride, h->kstride, mpp, st);
   });
 }
 
-// The ordered sum of the packed buffers and the sparse AdamS update.
+// The ordered sum of the packed buffers and the sparse AdamS update (plus,
+// under the dense off-mask reading, the zero-gradient update elsewhere).
 int enqueue_update(scape_t* h, const AdamsConst& c, cudaStream_t st) {
   int rc = run_kernel(h, kKReduce, st, [&] {
     return launch_reduce(h->pack(), h->kstride, h->W, h->k, h->gbar(), st);
   });
   if (rc) return rc;
-  return run_kernel(h, kKAdamsSparse, st, [&] {
-    return launch_adams_sparse(h->idx(), h->gbar(), h->k, h->w, h->m, c, st);
+  const bool msync = (h->variant & SCAPE_VARIANT_MOMENT_SYNC) != 0;
+  rc = run_kernel(h, kKAdamsSparse, st, [&] {
+    return launch_adams_sparse(h->idx(), h->gbar(), h->k, h->w, h->m, c, msync, st);
   });
+  if (rc || !(h->variant & SCAPE_VARIANT_DENSE_OFFMASK)) return rc;
+  return run_kernel(h, kKOffmask, st,
+                    [&] { return launch_offmask(h->bits(), h->P, h->w, h->m, c, st); });
 }
 
 // Rank table and index list from the bitmap already in the workspace.
@@ -381,7 +389,8 @@ int scape_step(scape_t* h, const void* const* host_grad_ptrs, void* stream) {
   int rc;
   if (t == 1) {
     rc = run_kernel(h, kKDenseStep, st, [&] {
-      return launch_dense_step(p, h->W, h->P, h->dtype, vec, h->w, h->m, c, st);
+      return launch_dense_step(p, h->W, h->P, h->dtype, vec, h->w, h->m, c,
+                               (h->variant & SCAPE_VARIANT_MOMENT_SYNC) != 0, st);
     });
     if (rc) return rc;
     h->buffers_valid = false;
@@ -445,6 +454,49 @@ int scape_refresh_mask(scape_t* h, void* stream) {
   if (rc) return rc;
   h->mask_ready = true;
   return SCAPE_OK;
+}
+
+int scape_set_variant(scape_t* h, int flags) {
+  if (!h) return SCAPE_EINVAL;
+  if (flags & ~(SCAPE_VARIANT_DENSE_OFFMASK | SCAPE_VARIANT_MOMENT_SYNC))
+    return fail(h, SCAPE_EINVAL, "scape_set_variant: unknown flag");
+  h->variant = flags;
+  return SCAPE_OK;
+}
+
+// Dense baselines: plain mean of the workers' gradients, AdamS or AdamW on
+// every coordinate; no error feedback, no mask.
+static int dense_baseline(scape_t* h, const void* const* grads, float* v, bool adamw,
+                          void* stream) {
+  if (!h) return SCAPE_EINVAL;
+  if (!h->bound) return fail(h, SCAPE_ESTATE, "dense baseline: call scape_bind first");
+  if (!grads || (adamw && !v)) return fail(h, SCAPE_EINVAL, "dense baseline: NULL pointer");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  WorkerPtrs p;
+  std::memset(&p, 0, sizeof p);
+  bool vec = true;
+  for (int w = 0; w < h->W; ++w) {
+    if (!grads[w]) return fail(h, SCAPE_EINVAL, "dense baseline: NULL gradient pointer");
+    p.g[w] = grads[w];
+    p.e[w] = h->e[w];
+    vec = vec && aligned16(grads[w]);
+  }
+  const int64_t t = h->t + 1;
+  const AdamsConst c = make_const(h, t);
+  const int rc = run_kernel(h, adamw ? kKAdamW : kKDenseAdams, st, [&] {
+    return launch_dense_baseline(adamw, p, h->W, h->P, h->dtype, vec, h->w, h->m, v, c, st);
+  });
+  if (rc) return rc;
+  h->t = t;
+  return SCAPE_OK;
+}
+
+int scape_dense_adams_step(scape_t* h, const void* const* host_grad_ptrs, void* stream) {
+  return dense_baseline(h, host_grad_ptrs, nullptr, false, stream);
+}
+
+int scape_adamw_step(scape_t* h, const void* const* host_grad_ptrs, float* v, void* stream) {
+  return dense_baseline(h, host_grad_ptrs, v, true, stream);
 }
 
 int scape_set_lr(scape_t* h, float lr) {

@@ -75,6 +75,9 @@ enum KernelId {
   kKIndex,
   kKShardCount,
   kKTileCount,
+  kKOffmask,
+  kKDenseAdams,
+  kKAdamW,
   kNumKernels
 };
 static_assert(kNumKernels == SCAPE_NUM_KERNELS, "kernel table size");
@@ -131,17 +134,62 @@ __device__ __forceinline__ void adams_update(float g, float& w, float& m, const 
   m = m_new;
 }
 
+// AdamW update of one coordinate (dense baseline): v is an EMA of g^2.
+__device__ __forceinline__ void adamw_update(float g, float& w, float& m, float& v,
+                                             const AdamsConst& c) {
+  const float w_prev = w;
+  const float m_new = __fadd_rn(__fmul_rn(c.beta1, m), __fmul_rn(c.one_minus_b1, g));
+  const float v_new = __fadd_rn(__fmul_rn(c.beta2, v), __fmul_rn(c.one_minus_b2, __fmul_rn(g, g)));
+  const float m_hat = __fdiv_rn(m_new, c.bc1);
+  const float v_hat = __fdiv_rn(v_new, c.bc2);
+  const float denom = __fadd_rn(__fsqrt_rn(v_hat), c.eps);
+  const float upd = __fadd_rn(__fdiv_rn(m_hat, denom), __fmul_rn(c.wd, w_prev));
+  w = __fsub_rn(w_prev, __fmul_rn(c.lr, upd));
+  m = m_new;
+  v = v_new;
+}
+
+// AdamS update when the synchronised buffer holds the first moment b
+// (m_t = b) and the gradient is recovered as g = (b - b1 m_{t-1}) / (1 - b1).
+__device__ __forceinline__ void adams_update_from_moment(float b, float& w, float& m,
+                                                         const AdamsConst& c) {
+  const float m_prev = m, w_prev = w;
+  const float g = __fdiv_rn(__fsub_rn(b, __fmul_rn(c.beta1, m_prev)), c.one_minus_b1);
+  const float v = __fadd_rn(__fmul_rn(c.beta2, __fmul_rn(m_prev, m_prev)),
+                            __fmul_rn(c.one_minus_b2, __fmul_rn(g, g)));
+  const float m_hat = __fdiv_rn(b, c.bc1);
+  const float v_hat = __fdiv_rn(v, c.bc2);
+  const float denom = __fadd_rn(__fsqrt_rn(v_hat), c.eps);
+  const float upd = __fadd_rn(__fdiv_rn(m_hat, denom), __fmul_rn(c.wd, w_prev));
+  w = __fsub_rn(w_prev, __fmul_rn(c.lr, upd));
+  m = b;
+}
+
+// First-moment packing of the compaction (variant reading): m_{t-1} and b1.
+struct MomentPack {
+  const float* m;
+  float beta1, c1;
+};
+
 // ---------------------------------------------------------------- launchers
 // Each returns cudaGetLastError() after enqueueing on `st`.
+// moment: step 1 under the first-moment buffer reading.
 cudaError_t launch_dense_step(const WorkerPtrs& p, int W, int64_t P, int dtype, bool vec,
-                              float* w, float* m, const AdamsConst& c, cudaStream_t st);
+                              float* w, float* m, const AdamsConst& c, bool moment,
+                              cudaStream_t st);
+// mp == nullptr: the selected a^w are packed; else b = b1 m + (1 - b1) a^w.
 cudaError_t launch_ef_compact(const WorkerPtrs& p, int W, int64_t P, int dtype, bool vec,
                               const uint32_t* bits, const uint32_t* tile_base, float* pack,
-                              int64_t pack_stride, cudaStream_t st);
+                              int64_t pack_stride, const MomentPack* mp, cudaStream_t st);
+cudaError_t launch_dense_baseline(bool adamw, const WorkerPtrs& p, int W, int64_t P, int dtype,
+                                  bool vec, float* w, float* m, float* v, const AdamsConst& c,
+                                  cudaStream_t st);
+cudaError_t launch_offmask(const uint32_t* bits, int64_t P, float* w, float* m, const AdamsConst& c,
+                           cudaStream_t st);
 cudaError_t launch_reduce(const float* pack, int64_t pack_stride, int W, int64_t k, float* gbar,
                           cudaStream_t st);
 cudaError_t launch_adams_sparse(const uint32_t* idx, const float* gbar, int64_t k, float* w,
-                                float* m, const AdamsConst& c, cudaStream_t st);
+                                float* m, const AdamsConst& c, bool msync, cudaStream_t st);
 
 cudaError_t launch_hist(int pass, const float* m, int64_t P, int W, const int64_t* shard_start,
                         const ShardSel* sel, uint32_t* hist, cudaStream_t st);

@@ -71,25 +71,31 @@ __device__ __forceinline__ void store8_f32(float* p, const float (&x)[8]) {
 // block-exclusive popcount prefix, computed once and reused for all W workers.
 constexpr int kWorkerUnroll = 2;
 
+// With MSYNC (first-moment buffer reading) a selected parameter is sent as
+// b = b1 m_{t-1} + (1 - b1) a instead of a; the residual is the same.
+template <bool MSYNC>
 __device__ __forceinline__ void ef_select8(const float (&g)[8], const float (&e)[8], uint32_t byte,
-                                           float* __restrict__ prow, float (&out)[8]) {
+                                           float* __restrict__ prow, float (&out)[8],
+                                           const MomentPack& mp, int64_t i0) {
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const float a = __fadd_rn(g[j], e[j]);  // error-feedback add
     float sent = 0.f;
     if ((byte >> j) & 1u) {
       sent = a;
-      prow[__popc(byte & ((1u << j) - 1u))] = a;
+      float val = a;
+      if (MSYNC) val = __fadd_rn(__fmul_rn(mp.beta1, __ldg(mp.m + i0 + j)), __fmul_rn(mp.c1, a));
+      prow[__popc(byte & ((1u << j) - 1u))] = val;
     }
     out[j] = __fsub_rn(a, sent);  // residual: g + e - sent
   }
 }
 
-template <typename GT, bool VEC>
+template <typename GT, bool VEC, bool MSYNC>
 __global__ void __launch_bounds__(kTileThreads, 3)
 ef_compact_kernel(const __grid_constant__ WorkerPtrs ptrs, int W, int64_t P,
                   const uint32_t* __restrict__ bits, const uint32_t* __restrict__ tile_base,
-                  float* __restrict__ pack, int64_t pack_stride) {
+                  float* __restrict__ pack, int64_t pack_stride, MomentPack mp) {
   __shared__ uint32_t warp_tot[kTileThreads / 32];
   const int64_t tile = blockIdx.x;
   const int64_t i0 = tile * kTile + (int64_t)threadIdx.x * 8;
@@ -115,7 +121,7 @@ ef_compact_kernel(const __grid_constant__ WorkerPtrs ptrs, int W, int64_t P,
       for (int u = 0; u < kWorkerUnroll; ++u) {
         if (w0 + u < W) {
           float out[8];
-          ef_select8(g[u], e[u], byte, pbase + (int64_t)(w0 + u) * pack_stride, out);
+          ef_select8<MSYNC>(g[u], e[u], byte, pbase + (int64_t)(w0 + u) * pack_stride, out, mp, i0);
           store8_f32(ptrs.e[w0 + u] + i0, out);
         }
       }
@@ -130,7 +136,7 @@ ef_compact_kernel(const __grid_constant__ WorkerPtrs ptrs, int W, int64_t P,
         g[j] = in ? GradIO<GT>::load1(ptrs.g[wk], i0 + j) : 0.f;
         e[j] = in ? __ldcs(ptrs.e[wk] + i0 + j) : 0.f;
       }
-      ef_select8(g, e, byte, pbase + (int64_t)wk * pack_stride, out);
+      ef_select8<MSYNC>(g, e, byte, pbase + (int64_t)wk * pack_stride, out, mp, i0);
 #pragma unroll
       for (int j = 0; j < 8; ++j)
         if (i0 + j < P) __stcs(ptrs.e[wk] + i0 + j, out[j]);
@@ -139,45 +145,89 @@ ef_compact_kernel(const __grid_constant__ WorkerPtrs ptrs, int W, int64_t P,
 }
 
 // ------------------------------------------------------------------ dense_step
-// Step 1: every coordinate is selected, so the synchronised buffer is the
-// ordered mean of all a^w = g^w + e^w and the residuals become a - a.
-template <typename GT, bool VEC>
+// KIND == kDenseScape: SCAPE step 1.  Every coordinate is selected, so the
+// synchronised buffer is the ordered mean of all a^w = g^w + e^w and the
+// residuals become a - a.
+// KIND == kDenseAdams / kDenseAdamW: the dense baselines the pages compare
+// against, on the ordered mean of the g^w alone (no error feedback): AdamS
+// ("SCAPE" Sec. II-C, Eq. 2) and AdamW (v an EMA of g^2, kept in `var`).
+// KIND == kDenseScapeMoment: step 1 under the first-moment buffer reading (the
+// workers send b = b1 m + (1 - b1) a; m_t is their mean).
+constexpr int kDenseScape = 0, kDenseAdams = 1, kDenseAdamW = 2, kDenseScapeMoment = 3;
+
+template <typename GT, bool VEC, int KIND>
 __global__ void __launch_bounds__(256)
 dense_step_kernel(const __grid_constant__ WorkerPtrs ptrs, int W, int64_t P,
-                  float* __restrict__ wts, float* __restrict__ mom, AdamsConst c) {
+                  float* __restrict__ wts, float* __restrict__ mom, float* __restrict__ var,
+                  AdamsConst c) {
+  constexpr bool EF = KIND == kDenseScape || KIND == kDenseScapeMoment;
+  constexpr bool MOM = KIND == kDenseScapeMoment;
   const int64_t i0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
   if (i0 >= P) return;
   const bool full = VEC && (i0 + 8 <= P);
   const int n = full ? 8 : (int)(P - i0 < 8 ? P - i0 : 8);
-  float sum[8];
+  float sum[8], m0[8];
+  if (MOM)
+    for (int j = 0; j < 8; ++j) m0[j] = j < n ? mom[i0 + j] : 0.f;
   for (int wk = 0; wk < W; ++wk) {
     float g[8], e[8], z[8];
     if (full) {
       GradIO<GT>::load8(ptrs.g[wk], i0, g);
-      load8_f32(ptrs.e[wk] + i0, e);
+      if (EF) load8_f32(ptrs.e[wk] + i0, e);
     } else {
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         g[j] = j < n ? GradIO<GT>::load1(ptrs.g[wk], i0 + j) : 0.f;
-        e[j] = j < n ? ptrs.e[wk][i0 + j] : 0.f;
+        e[j] = (EF && j < n) ? ptrs.e[wk][i0 + j] : 0.f;
       }
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const float a = __fadd_rn(g[j], e[j]);
-      sum[j] = (wk == 0) ? a : __fadd_rn(sum[j], a);
+      const float a = EF ? __fadd_rn(g[j], e[j]) : g[j];
+      const float b = MOM ? __fadd_rn(__fmul_rn(c.beta1, m0[j]), __fmul_rn(c.one_minus_b1, a)) : a;
+      sum[j] = (wk == 0) ? b : __fadd_rn(sum[j], b);
       z[j] = __fsub_rn(a, a);
     }
-    if (full) {
-      store8_f32(ptrs.e[wk] + i0, z);
-    } else {
-      for (int j = 0; j < n; ++j) ptrs.e[wk][i0 + j] = z[j];
+    if (EF) {
+      if (full) {
+        store8_f32(ptrs.e[wk] + i0, z);
+      } else {
+        for (int j = 0; j < n; ++j) ptrs.e[wk][i0 + j] = z[j];
+      }
     }
   }
   const float fw = (float)W;
   for (int j = 0; j < n; ++j) {
+    const float gm = __fdiv_rn(sum[j], fw);
     float wv = wts[i0 + j], mv = mom[i0 + j];
-    adams_update(__fdiv_rn(sum[j], fw), wv, mv, c);
+    if (KIND == kDenseAdamW) {
+      float vv = var[i0 + j];
+      adamw_update(gm, wv, mv, vv, c);
+      var[i0 + j] = vv;
+    } else if (MOM) {
+      adams_update_from_moment(gm, wv, mv, c);
+    } else {
+      adams_update(gm, wv, mv, c);
+    }
+    wts[i0 + j] = wv;
+    mom[i0 + j] = mv;
+  }
+}
+
+// ------------------------------------------------------------------ offmask
+// Dense off-mask reading: every unselected coordinate takes the AdamS update
+// with a zero synchronised gradient.  4 parameters per thread.
+__global__ void __launch_bounds__(256)
+offmask_kernel(const uint32_t* __restrict__ bits, int64_t P, float* __restrict__ wts,
+               float* __restrict__ mom, AdamsConst c) {
+  const int64_t i0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (i0 >= P) return;
+  const uint32_t nib = (__ldg(bits + (i0 >> 5)) >> (uint32_t)(i0 & 31)) & 0xFu;
+  if (nib == 0xFu) return;  // all four selected: already updated
+  for (int j = 0; j < 4 && i0 + j < P; ++j) {
+    if ((nib >> j) & 1u) continue;
+    float wv = wts[i0 + j], mv = mom[i0 + j];
+    adams_update(0.0f, wv, mv, c);
     wts[i0 + j] = wv;
     mom[i0 + j] = mv;
   }
@@ -213,7 +263,16 @@ reduce_kernel(const float* __restrict__ pack, int64_t stride, int W, int64_t k,
 }
 
 // ------------------------------------------------------------------ adams_sparse
-// For the k selected coordinates i = idx[j]: AdamS with g = g_bar[j].
+// For the k selected coordinates i = idx[j]: AdamS with g = g_bar[j]; with
+// MSYNC the buffer holds the synchronised first moment instead (m_t = b_bar,
+// g recovered from it for the second moment).
+template <bool MSYNC>
+__device__ __forceinline__ void sparse_update(float b, float& w, float& m, const AdamsConst& c) {
+  if (MSYNC) adams_update_from_moment(b, w, m, c);
+  else adams_update(b, w, m, c);
+}
+
+template <bool MSYNC>
 __global__ void __launch_bounds__(256)
 adams_sparse_kernel(const uint32_t* __restrict__ idx, const float* __restrict__ gbar, int64_t k,
                     float* __restrict__ wts, float* __restrict__ mom, AdamsConst c) {
@@ -232,7 +291,7 @@ adams_sparse_kernel(const uint32_t* __restrict__ idx, const float* __restrict__ 
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      adams_update(gg[q], wv[q], mv[q], c);
+      sparse_update<MSYNC>(gg[q], wv[q], mv[q], c);
       wts[ii[q]] = wv[q];
       mom[ii[q]] = mv[q];
     }
@@ -240,48 +299,74 @@ adams_sparse_kernel(const uint32_t* __restrict__ idx, const float* __restrict__ 
     for (int64_t j = j0; j < k; ++j) {
       const uint32_t i = idx[j];
       float wv = wts[i], mv = mom[i];
-      adams_update(gbar[j], wv, mv, c);
+      sparse_update<MSYNC>(gbar[j], wv, mv, c);
       wts[i] = wv;
       mom[i] = mv;
     }
   }
 }
 
+template <typename GT, int KIND>
+void dense_kind(const WorkerPtrs& p, int W, int64_t P, bool vec, float* w, float* m, float* v,
+                const AdamsConst& c, cudaStream_t st) {
+  const int64_t threads = (P + 7) / 8;
+  const unsigned grid = (unsigned)((threads + 255) / 256);
+  if (vec) dense_step_kernel<GT, true, KIND><<<grid, 256, 0, st>>>(p, W, P, w, m, v, c);
+  else dense_step_kernel<GT, false, KIND><<<grid, 256, 0, st>>>(p, W, P, w, m, v, c);
+}
+
+template <typename GT, bool MSYNC>
+void compact_kind(const WorkerPtrs& p, int W, int64_t P, bool vec, const uint32_t* bits,
+                  const uint32_t* tile_base, float* pack, int64_t pack_stride,
+                  const MomentPack& mp, cudaStream_t st) {
+  const unsigned grid = (unsigned)((P + kTile - 1) / kTile);
+  if (vec)
+    ef_compact_kernel<GT, true, MSYNC>
+        <<<grid, kTileThreads, 0, st>>>(p, W, P, bits, tile_base, pack, pack_stride, mp);
+  else
+    ef_compact_kernel<GT, false, MSYNC>
+        <<<grid, kTileThreads, 0, st>>>(p, W, P, bits, tile_base, pack, pack_stride, mp);
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ launchers
 cudaError_t launch_dense_step(const WorkerPtrs& p, int W, int64_t P, int dtype, bool vec,
-                              float* w, float* m, const AdamsConst& c, cudaStream_t st) {
-  const int64_t threads = (P + 7) / 8;
-  const unsigned grid = (unsigned)((threads + 255) / 256);
+                              float* w, float* m, const AdamsConst& c, bool moment,
+                              cudaStream_t st) {
   if (dtype == SCAPE_BF16) {
-    if (vec) dense_step_kernel<__nv_bfloat16, true><<<grid, 256, 0, st>>>(p, W, P, w, m, c);
-    else dense_step_kernel<__nv_bfloat16, false><<<grid, 256, 0, st>>>(p, W, P, w, m, c);
+    if (moment) dense_kind<__nv_bfloat16, kDenseScapeMoment>(p, W, P, vec, w, m, nullptr, c, st);
+    else dense_kind<__nv_bfloat16, kDenseScape>(p, W, P, vec, w, m, nullptr, c, st);
   } else {
-    if (vec) dense_step_kernel<float, true><<<grid, 256, 0, st>>>(p, W, P, w, m, c);
-    else dense_step_kernel<float, false><<<grid, 256, 0, st>>>(p, W, P, w, m, c);
+    if (moment) dense_kind<float, kDenseScapeMoment>(p, W, P, vec, w, m, nullptr, c, st);
+    else dense_kind<float, kDenseScape>(p, W, P, vec, w, m, nullptr, c, st);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dense_baseline(bool adamw, const WorkerPtrs& p, int W, int64_t P, int dtype,
+                                  bool vec, float* w, float* m, float* v, const AdamsConst& c,
+                                  cudaStream_t st) {
+  if (dtype == SCAPE_BF16) {
+    if (adamw) dense_kind<__nv_bfloat16, kDenseAdamW>(p, W, P, vec, w, m, v, c, st);
+    else dense_kind<__nv_bfloat16, kDenseAdams>(p, W, P, vec, w, m, v, c, st);
+  } else {
+    if (adamw) dense_kind<float, kDenseAdamW>(p, W, P, vec, w, m, v, c, st);
+    else dense_kind<float, kDenseAdams>(p, W, P, vec, w, m, v, c, st);
   }
   return cudaGetLastError();
 }
 
 cudaError_t launch_ef_compact(const WorkerPtrs& p, int W, int64_t P, int dtype, bool vec,
                               const uint32_t* bits, const uint32_t* tile_base, float* pack,
-                              int64_t pack_stride, cudaStream_t st) {
-  const unsigned grid = (unsigned)((P + kTile - 1) / kTile);
+                              int64_t pack_stride, const MomentPack* mp, cudaStream_t st) {
+  const MomentPack none{nullptr, 0.f, 0.f};
   if (dtype == SCAPE_BF16) {
-    if (vec)
-      ef_compact_kernel<__nv_bfloat16, true>
-          <<<grid, kTileThreads, 0, st>>>(p, W, P, bits, tile_base, pack, pack_stride);
-    else
-      ef_compact_kernel<__nv_bfloat16, false>
-          <<<grid, kTileThreads, 0, st>>>(p, W, P, bits, tile_base, pack, pack_stride);
+    if (mp) compact_kind<__nv_bfloat16, true>(p, W, P, vec, bits, tile_base, pack, pack_stride, *mp, st);
+    else compact_kind<__nv_bfloat16, false>(p, W, P, vec, bits, tile_base, pack, pack_stride, none, st);
   } else {
-    if (vec)
-      ef_compact_kernel<float, true>
-          <<<grid, kTileThreads, 0, st>>>(p, W, P, bits, tile_base, pack, pack_stride);
-    else
-      ef_compact_kernel<float, false>
-          <<<grid, kTileThreads, 0, st>>>(p, W, P, bits, tile_base, pack, pack_stride);
+    if (mp) compact_kind<float, true>(p, W, P, vec, bits, tile_base, pack, pack_stride, *mp, st);
+    else compact_kind<float, false>(p, W, P, vec, bits, tile_base, pack, pack_stride, none, st);
   }
   return cudaGetLastError();
 }
@@ -295,10 +380,18 @@ cudaError_t launch_reduce(const float* pack, int64_t pack_stride, int W, int64_t
 }
 
 cudaError_t launch_adams_sparse(const uint32_t* idx, const float* gbar, int64_t k, float* w,
-                                float* m, const AdamsConst& c, cudaStream_t st) {
+                                float* m, const AdamsConst& c, bool msync, cudaStream_t st) {
   if (k <= 0) return cudaSuccess;
-  const int64_t threads = (k + 3) / 4;
-  adams_sparse_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(idx, gbar, k, w, m, c);
+  const unsigned grid = (unsigned)(((k + 3) / 4 + 255) / 256);
+  if (msync) adams_sparse_kernel<true><<<grid, 256, 0, st>>>(idx, gbar, k, w, m, c);
+  else adams_sparse_kernel<false><<<grid, 256, 0, st>>>(idx, gbar, k, w, m, c);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_offmask(const uint32_t* bits, int64_t P, float* w, float* m, const AdamsConst& c,
+                           cudaStream_t st) {
+  const int64_t threads = (P + 3) / 4;
+  offmask_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(bits, P, w, m, c);
   return cudaGetLastError();
 }
 

@@ -17,7 +17,10 @@ class Scape:
 
     def __init__(self, params: torch.Tensor, W: int, sparsity: float, *, layer_numel=None,
                  lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1,
-                 grad_dtype=torch.bfloat16):
+                 grad_dtype=torch.bfloat16, residuals: str = "device"):
+        """residuals: "device" (HBM) or "host": the W error-feedback buffers
+        live in pinned host memory, which the kernels read and write in place
+        over the host link (keeps W*P*4 bytes out of HBM)."""
         if not params.is_cuda or params.dtype != torch.float32 or not params.is_contiguous():
             raise ValueError("params must be a contiguous float32 CUDA tensor")
         P = params.numel()
@@ -35,7 +38,12 @@ class Scape:
         dev = params.device
         self.params = params
         self.m = torch.zeros(P, dtype=torch.float32, device=dev)
-        self.e = [torch.zeros(P, dtype=torch.float32, device=dev) for _ in range(W)]
+        if residuals == "device":
+            self.e = [torch.zeros(P, dtype=torch.float32, device=dev) for _ in range(W)]
+        elif residuals == "host":
+            self.e = [torch.zeros(P, dtype=torch.float32).pin_memory() for _ in range(W)]
+        else:
+            raise ValueError('residuals must be "device" or "host"')
         self.ws_bytes = C.scape_workspace_bytes(self.h)
         self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
         C.scape_bind(self.h, params.data_ptr(), self.m.data_ptr(), [x.data_ptr() for x in self.e],
@@ -61,6 +69,19 @@ class Scape:
         C.scape_step_host(self.h, [g.data_ptr() for g in host_grads],
                           [g.data_ptr() for g in dev_grads], host_params_out.data_ptr(),
                           self._stream())
+
+    def set_variant(self, flags):
+        C.scape_set_variant(self.h, flags)
+
+    def dense_adams_step(self, grads):
+        """Dense AdamS baseline on the mean gradient (no error feedback, no mask)."""
+        C.scape_dense_adams_step(self.h, [g.data_ptr() for g in grads], self._stream())
+
+    def adamw_step(self, grads, v: torch.Tensor):
+        """Dense AdamW baseline; v is the caller's float32 second moment."""
+        if v.dtype != torch.float32 or v.numel() != self.P or not v.is_cuda:
+            raise ValueError("v must be a float32 CUDA tensor of P elements")
+        C.scape_adamw_step(self.h, [g.data_ptr() for g in grads], v.data_ptr(), self._stream())
 
     def set_lr(self, lr):
         C.scape_set_lr(self.h, lr)

@@ -49,7 +49,7 @@ class Report:
 
 
 def run_full_trajectory(wl: synth.Workload, device, steps: int, seed: int = 0,
-                        grad_offset_elems: int = 0):
+                        grad_offset_elems: int = 0, variant: int = 0):
     """Whole problem on both sides (small sizes): compare every step."""
     P, W, s = wl.P, wl.W, wl.sparsity
     gdt = torch.bfloat16 if wl.grad_dtype == "bf16" else torch.float32
@@ -57,6 +57,8 @@ def run_full_trajectory(wl: synth.Workload, device, steps: int, seed: int = 0,
     gen = synth.GradientStream(wl, seed=seed, device="cpu")
     params = w0.to(device)
     opt = make_opt(params, W, s, gdt)
+    if variant:
+        opt.set_variant(variant)
     st = O.new_state(w0.numpy(), W, s, HP)
     rep = Report()
     # optional misaligned gradient buffers (scalar path)
@@ -69,7 +71,7 @@ def run_full_trajectory(wl: synth.Workload, device, steps: int, seed: int = 0,
             view.copy_(g.to(device))
             dg.append(view)
         opt.step(dg)
-        rec = O.advance(st, [synth.to_numpy_grad(g) for g in grads])
+        rec = O.advance(st, [synth.to_numpy_grad(g) for g in grads], variant=variant)
         if t >= 2:
             torch.cuda.synchronize()
             pack = u32(opt.pack())

@@ -12,7 +12,7 @@ import pytest
 import torch
 
 from oracle import oracle as O
-from sparse_communication_sharded_gb300 import ScapeError, synth
+from sparse_communication_sharded_gb300 import Scape, ScapeError, synth
 from tests._harness import HP, bits_to_bool, make_opt, run_full_trajectory, run_sampled_shards, u32
 
 pytestmark = pytest.mark.gpu
@@ -246,3 +246,31 @@ def test_flat_sweep_largest_point_sampled(cuda_device):
     rep = run_sampled_shards(wl, cuda_device, 3, (0, 7))
     assert rep.exact
     torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------ residuals in host memory
+@pytest.mark.parametrize("P,W,s,dtype", [(70001, 4, 0.99, "bf16"), (4096, 2, 0.9, "f32")])
+def test_host_resident_residuals_match_oracle(cuda_device, P, W, s, dtype):
+    """Error-feedback buffers in pinned host memory, read and written in place
+    by the kernels: same trajectory as the oracle, bit for bit."""
+    gdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    wl = _wl(P, W, s, dtype)
+    gen = synth.GradientStream(wl, seed=8, device="cpu")
+    w0 = synth.init_params(P, seed=8)
+    params = w0.to(cuda_device)
+    opt = Scape(params, W, s, lr=HP.lr, beta1=HP.beta1, beta2=HP.beta2, eps=HP.eps,
+                weight_decay=HP.weight_decay, grad_dtype=gdt, residuals="host")
+    assert not opt.e[0].is_cuda
+    st = O.new_state(w0.numpy(), W, s, HP)
+    for _ in range(6):
+        grads = gen.next()
+        opt.step([g.to(cuda_device) for g in grads])
+        opt.refresh_mask()
+        O.advance(st, [synth.to_numpy_grad(g) for g in grads])
+    torch.cuda.synchronize()
+    assert np.array_equal(u32(params), st.w.view(np.uint32))
+    assert np.array_equal(u32(opt.m), st.m.view(np.uint32))
+    for w in range(W):
+        assert np.array_equal(opt.e[w].numpy().view(np.uint32), st.e[w].view(np.uint32))
+    assert np.array_equal(u32(opt.bits()), st.bits)
+    opt.close()
