@@ -68,8 +68,11 @@ def _load():
                                                 f32, f32, f32, f32, f32]
         lib.oracle_adamw_step.argtypes = [i64, i64, i32, i32, vp, vp, vp, vp,
                                           f32, f32, f32, f32, f32]
+        lib.oracle_union_topk_step.argtypes = [i64, i64, i32, i32, vp, vp, vp, vp, i64,
+                                               f32, f32, f32, f32, f32, vp, vp, vp, vp, vp]
         for fn in (lib.oracle_layout, lib.oracle_topk_mask, lib.oracle_step,
-                   lib.oracle_step_variant, lib.oracle_dense_adams_step, lib.oracle_adamw_step):
+                   lib.oracle_step_variant, lib.oracle_dense_adams_step, lib.oracle_adamw_step,
+                   lib.oracle_union_topk_step):
             fn.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -188,6 +191,36 @@ def adamw_step(t: int, grads, w, m, v, hp: Hyper):
                                    _ptr(v), hp.beta1, hp.beta2, hp.lr, hp.eps, hp.weight_decay)
     if rc != 0:
         raise ValueError("oracle_adamw_step failed")
+
+
+def union_k_worker(P: int, sparsity: float) -> int:
+    """Coordinates each worker selects over the whole vector (same rounding as
+    the shards' k)."""
+    ppm = sparsity_ppm(sparsity)
+    return (P * (1000000 - ppm) + 999999) // 1000000
+
+
+def union_topk_step(t: int, grads, e, w, m, k_worker: int, hp: Hyper):
+    """Gradient top-k with error feedback and a union mask.  Updates e, w, m
+    in place; returns (union bits, idx, pack [W, k_union], gbar)."""
+    W = len(grads)
+    P = w.size
+    dtype = BF16 if grads[0].dtype == np.uint16 else F32
+    bits = np.zeros((P + 31) // 32, np.uint32)
+    idx = np.zeros(P, np.uint32)
+    ku = np.zeros(1, np.int64)
+    pack = np.zeros(W * P, np.float32)
+    gbar = np.zeros(P, np.float32)
+    gp = (ctypes.c_void_p * W)(*[_ptr(g) for g in grads])
+    ep = (ctypes.c_void_p * W)(*[_ptr(x) for x in e])
+    rc = _load().oracle_union_topk_step(t, P, W, dtype, ctypes.addressof(gp), ctypes.addressof(ep),
+                                        _ptr(w), _ptr(m), int(k_worker), hp.beta1, hp.beta2,
+                                        hp.lr, hp.eps, hp.weight_decay, _ptr(bits), _ptr(idx),
+                                        _ptr(ku), _ptr(pack), _ptr(gbar))
+    if rc != 0:
+        raise ValueError("oracle_union_topk_step failed")
+    k = int(ku[0])
+    return bits, idx[:k].copy(), pack[:W * k].reshape(W, k).copy(), gbar[:k].copy()
 
 
 def dense_mask(P: int):

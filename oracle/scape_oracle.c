@@ -364,3 +364,67 @@ int oracle_adamw_step(int64_t t, int64_t P, int W, int grad_dtype, const void *c
     }
     return ORACLE_OK;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Gradient top-k with error feedback and a union mask: the second           */
+/* synchronisation scheme of [P1] Sec. II-B, the baseline SCAPE's partitioned */
+/* mask is designed against.  Each worker selects the k_worker largest |a^w|, */
+/* a^w = g^w + e^w, over the whole vector (larger magnitude first, lower      */
+/* index on ties); the masks are gathered into their union; every worker     */
+/* sends its a^w at every union position (the all-reduce over the global     */
+/* mask), so its residual becomes a - a there and stays a elsewhere; the     */
+/* mean over the workers drives AdamS ([P1] Sec. II-C) at the union          */
+/* positions, the others are left unchanged.  As W grows the union fills in. */
+/* ------------------------------------------------------------------------- */
+int oracle_union_topk_step(int64_t t, int64_t P, int W, int grad_dtype,
+                           const void *const *grads, float *const *e, float *w, float *m,
+                           int64_t k_worker, float beta1, float beta2, float lr, float eps,
+                           float wd, uint32_t *union_bits, uint32_t *idx, int64_t *k_union,
+                           float *pack, float *gbar)
+{
+    if (t < 1 || P < 1 || W < 1 || k_worker < 0 || k_worker > P)
+        return ORACLE_EINVAL;
+    if (grad_dtype != ORACLE_F32 && grad_dtype != ORACLE_BF16)
+        return ORACLE_EINVAL;
+    int64_t nwords = (P + 31) / 32;
+    memset(union_bits, 0, (size_t)nwords * sizeof(uint32_t));
+    oracle_entry *ent = (oracle_entry *)malloc((size_t)P * sizeof(oracle_entry));
+    if (!ent)
+        return ORACLE_EINVAL;
+    for (int wk = 0; wk < W; ++wk) {
+        for (int64_t i = 0; i < P; ++i) {
+            e[wk][i] = widen_grad(grads[wk], grad_dtype, i) + e[wk][i]; /* a^w */
+            ent[i].key = magnitude_key(e[wk][i]);
+            ent[i].index = i;
+        }
+        qsort(ent, (size_t)P, sizeof(oracle_entry), entry_order);
+        for (int64_t r = 0; r < k_worker; ++r) {
+            int64_t i = ent[r].index;
+            union_bits[i / 32] |= 1u << (i % 32);
+        }
+    }
+    free(ent);
+    int64_t k = 0;
+    for (int64_t i = 0; i < P; ++i)
+        if ((union_bits[i / 32] >> (i % 32)) & 1u)
+            idx[k++] = (uint32_t)i;
+    *k_union = k;
+    for (int wk = 0; wk < W; ++wk) {
+        for (int64_t j = 0; j < k; ++j) {
+            int64_t i = idx[j];
+            float a = e[wk][i];
+            pack[(int64_t)wk * k + j] = a;
+            e[wk][i] = a - a;
+        }
+    }
+    float bc1 = (float)(1.0 - pow((double)beta1, (double)t));
+    float bc2 = (float)(1.0 - pow((double)beta2, (double)t));
+    for (int64_t j = 0; j < k; ++j) {
+        float sum = pack[j];
+        for (int wk = 1; wk < W; ++wk)
+            sum = sum + pack[(int64_t)wk * k + j];
+        gbar[j] = sum / (float)W;
+        adams_one(gbar[j], &w[idx[j]], &m[idx[j]], beta1, beta2, bc1, bc2, lr, eps, wd);
+    }
+    return ORACLE_OK;
+}
