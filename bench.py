@@ -385,6 +385,26 @@ def bench_baselines(opt, wl, grads, dev, warmup=2, steps=5):
         out[name] = {"ms_per_step": ms, "params_per_s": P / (ms / 1000.0),
                      "hbm_gbs": alg / (ms / 1000.0) / 1e9}
     del v
+    # union-mask gradient top-k (each worker's own top-k, OR-ed into one mask):
+    # step time and how much the union fills in relative to one worker's k
+    kw = (P * (1000000 - round(wl.sparsity * 1e6)) + 999999) // 1000000
+    sizes, ms_list = [], []
+    for it in range(warmup + 3):
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(st)
+        ku = opt.union_step(grads)
+        ev1.record(st)
+        torch.cuda.synchronize()
+        if it >= warmup:
+            sizes.append(ku)
+            ms_list.append(ev0.elapsed_time(ev1))
+    out["union_topk"] = {"ms_per_step": sum(ms_list) / len(ms_list), "k_worker": kw,
+                         "k_union": sizes, "fill_in": sum(sizes) / len(sizes) / kw,
+                         "union_density": sum(sizes) / len(sizes) / P,
+                         "scape_k": opt.k}
+    opt._union_ws = None
+    opt._union_cap = None
     torch.cuda.empty_cache()
     return out
 

@@ -192,6 +192,29 @@ int scape_set_variant(scape_t *h, int flags);
 int scape_dense_adams_step(scape_t *h, const void *const *host_grad_ptrs, void *stream);
 int scape_adamw_step(scape_t *h, const void *const *host_grad_ptrs, float *v, void *stream);
 
+/*
+ * Union-mask gradient top-k baseline: the second synchronisation scheme of
+ * "SCAPE" Sec. II-B, which the partitioned mask is designed against.  Each
+ * worker selects the k_w = ceil(P (1 - sparsity)) largest |g^w + e^w| over the
+ * whole vector (ties to the lower index); the W masks are OR-ed into their
+ * union (the mask all-gather); every worker sends its error-fed gradient at
+ * every union position (the all-reduce over the global mask), so its residual
+ * becomes a - a there and g + e elsewhere; AdamS ("SCAPE" Sec. II-C) runs on
+ * the ordered mean at the union positions, others unchanged.  The union grows
+ * with W (fill-in); its size is returned in *host_k_union.
+ *   workspace  caller device memory of scape_union_workspace_bytes(capacity)
+ *              bytes, 256-byte aligned; it keeps per-worker selection state
+ *              between calls (a new pointer starts it afresh)
+ *   capacity   the largest union the packed buffers hold, 1..P (P never
+ *              overflows).  A larger union returns SCAPE_EINVAL after the
+ *              selection, with the residuals holding g + e: do not retry.
+ * Synchronises `stream` once (to read the union size).  Uses and advances the
+ * handle's step count; the SCAPE mask state is not touched.
+ */
+int scape_union_workspace_bytes(const scape_t *h, int64_t capacity, size_t *bytes);
+int scape_union_step(scape_t *h, const void *const *host_grad_ptrs, void *workspace,
+                     size_t ws_bytes, int64_t capacity, int64_t *host_k_union, void *stream);
+
 /* Learning rate for subsequent steps (schedules).  lr must be finite. */
 int scape_set_lr(scape_t *h, float lr);
 
@@ -243,7 +266,7 @@ int scape_step_host(scape_t *h, const void *const *host_grads_src,
  * scape_profile_read() copies the totals (milliseconds and launch counts,
  * SCAPE_NUM_KERNELS entries each) and scape_kernel_name() names entry i.
  */
-#define SCAPE_NUM_KERNELS 16
+#define SCAPE_NUM_KERNELS 18
 int scape_profile_enable(scape_t *h, int on);
 int scape_profile_collect(scape_t *h);
 int scape_profile_read(const scape_t *h, double *host_ms, int64_t *host_launches);

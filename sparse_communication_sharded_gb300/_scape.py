@@ -19,7 +19,7 @@ SCAPE_ESTATE = -4
 SCAPE_F32 = 0
 SCAPE_BF16 = 1
 SCAPE_MAX_WORKERS = 256
-SCAPE_NUM_KERNELS = 16
+SCAPE_NUM_KERNELS = 18
 
 LIB_PATH = _build.LIB
 
@@ -47,6 +47,8 @@ _PROTOS = {
     "scape_set_lr": (_i32, [_vp, _f32]),
     "scape_set_variant": (_i32, [_vp, _i32]),
     "scape_dense_adams_step": (_i32, [_vp, _vp, _vp]),
+    "scape_union_workspace_bytes": (_i32, [_vp, _i64, _vp]),
+    "scape_union_step": (_i32, [_vp, _vp, _vp, ctypes.c_size_t, _i64, _vp, _vp]),
     "scape_adamw_step": (_i32, [_vp, _vp, _vp, _vp]),
     "scape_get_state": (_i32, [_vp, _vp, _vp, _vp, _vp]),
     "scape_get_buffers": (_i32, [_vp, _vp, _vp, _vp]),
@@ -163,6 +165,20 @@ def scape_dense_adams_step(h, grad_ptrs, stream=0):
 def scape_adamw_step(h, grad_ptrs, v_ptr, stream=0):
     arr = _ptr_array(grad_ptrs)
     _check(h, load().scape_adamw_step(h, ctypes.addressof(arr), v_ptr, stream))
+
+
+def scape_union_workspace_bytes(h, capacity):
+    n = ctypes.c_size_t()
+    _check(h, load().scape_union_workspace_bytes(h, int(capacity), ctypes.byref(n)))
+    return n.value
+
+
+def scape_union_step(h, grad_ptrs, ws_ptr, ws_bytes, capacity, stream=0):
+    arr = _ptr_array(grad_ptrs)
+    ku = ctypes.c_int64()
+    _check(h, load().scape_union_step(h, ctypes.addressof(arr), ws_ptr, ws_bytes, int(capacity),
+                                      ctypes.byref(ku), stream))
+    return ku.value
 
 
 def scape_set_lr(h, lr):

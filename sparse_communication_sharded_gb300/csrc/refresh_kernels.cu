@@ -13,8 +13,9 @@
 // tie_select find the index istar of the need-th equal key in index order.
 // The mark kernel then writes the bitmap elementwise
 //   bit_i = key_i > kstar  ||  (key_i == kstar && i <= istar)
-// with per-tile popcounts; scan turns those into the per-tile rank table, and
-// index writes the ascending packed index list.
+// with per-tile popcounts (or, in accumulate mode, ORs it into an existing
+// bitmap); scan turns per-tile counts into the rank table, and index writes
+// the ascending packed index list.
 #include "scape_internal.cuh"
 
 namespace scapek {
@@ -261,7 +262,7 @@ tie_select_kernel(const float* __restrict__ m, const int64_t* __restrict__ shard
 __global__ void __launch_bounds__(128)
 mark_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __restrict__ shard_start,
             const ShardSel* __restrict__ sel, uint32_t* __restrict__ bits,
-            uint32_t* __restrict__ tile_cnt) {
+            uint32_t* __restrict__ tile_cnt, bool accumulate) {
   __shared__ uint32_t warp_cnt[4];
   const int64_t tile = blockIdx.x;
   const int64_t t0 = tile * kTile;
@@ -320,7 +321,7 @@ mark_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __rest
     word |= __shfl_xor_sync(0xffffffffu, word, 4);
     const int64_t widx = (wb + 128 * r) / 32 + (lane >> 3);
     if ((lane & 7) == 0) {
-      if (widx < nwords) bits[widx] = word;
+      if (widx < nwords) bits[widx] = accumulate ? (bits[widx] | word) : word;
       cnt += __popc(word);
     }
   }
@@ -473,9 +474,9 @@ cudaError_t launch_tie_select(const float* m, int W, const int64_t* shard_start,
 
 cudaError_t launch_mark(const float* m, int64_t P, int W, const int64_t* shard_start,
                         const ShardSel* sel, uint32_t* bits, uint32_t* tile_cnt,
-                        cudaStream_t st) {
+                        cudaStream_t st, bool accumulate) {
   const unsigned grid = (unsigned)((P + kTile - 1) / kTile);
-  mark_kernel<<<grid, 128, 0, st>>>(m, P, W, shard_start, sel, bits, tile_cnt);
+  mark_kernel<<<grid, 128, 0, st>>>(m, P, W, shard_start, sel, bits, tile_cnt, accumulate);
   return cudaGetLastError();
 }
 

@@ -25,7 +25,7 @@ thread_local std::string g_create_error;
 const char* const kKernelNames[kNumKernels] = {
     "dense_step",  "ef_compact", "reduce", "adams_sparse", "cand_hist0", "cand_select",
     "cand_collect", "cand_hist",  "mark",   "scan",         "index",      "shard_count",
-    "tile_count",  "offmask",    "dense_adams", "adamw"};
+    "tile_count",  "offmask",    "dense_adams", "adamw", "ef_add", "union_move"};
 
 struct ProfRec {
   int kid;
@@ -64,6 +64,8 @@ struct scape {
   bool mask_ready = false;
   bool buffers_valid = false;
   int64_t launches = 0;
+  // union-mask baseline: workspace whose per-worker selection state is live
+  const void* union_ws = nullptr;
   // end-to-end pipelining (created on the first scape_step_host call)
   static constexpr int kMaxGroups = 8;
   bool aux_ready = false;
@@ -497,6 +499,169 @@ int scape_dense_adams_step(scape_t* h, const void* const* host_grad_ptrs, void* 
 
 int scape_adamw_step(scape_t* h, const void* const* host_grad_ptrs, float* v, void* stream) {
   return dense_baseline(h, host_grad_ptrs, v, true, stream);
+}
+
+// ------------------------------------------------------------------ union-mask baseline
+namespace {
+struct UnionLayout {
+  size_t start, kk, sel, hist, cand, ccnt, bits, tcnt, tbase, scan, idx, pack, gbar, total;
+  int64_t cstride;
+};
+
+UnionLayout union_layout(const scape_t* h, int64_t cap) {
+  UnionLayout L;
+  size_t off = 0;
+  auto carve = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, kAlign);
+    return o;
+  };
+  L.cstride = (int64_t)align_up((size_t)cap, 64);
+  L.start = carve(2 * 8);
+  L.kk = carve(8);
+  L.sel = carve(sizeof(ShardSel) * h->W);
+  L.hist = carve((size_t)kCandBins0 * 4);
+  L.cand = carve((size_t)h->P * sizeof(uint2));
+  L.ccnt = carve(4);
+  L.bits = carve(align_up((size_t)h->nwords, 64) * 4);
+  L.tcnt = carve((size_t)h->ntiles * 4);
+  L.tbase = carve((size_t)(h->ntiles + 1) * 4);
+  L.scan = carve((size_t)scan_scratch_words(h->ntiles) * 4);
+  L.idx = carve((size_t)h->P * 4);
+  L.pack = carve((size_t)h->W * L.cstride * 4);
+  L.gbar = carve((size_t)L.cstride * 4);
+  L.total = off;
+  return L;
+}
+
+int64_t union_k_worker(const scape_t* h) { return (h->P * (1000000 - h->ppm) + 999999) / 1000000; }
+}  // namespace
+
+int scape_union_workspace_bytes(const scape_t* h, int64_t capacity, size_t* bytes) {
+  if (!h || !bytes || capacity < 1 || capacity > h->P) return SCAPE_EINVAL;
+  *bytes = union_layout(h, capacity).total;
+  return SCAPE_OK;
+}
+
+int scape_union_step(scape_t* h, const void* const* host_grad_ptrs, void* workspace,
+                     size_t ws_bytes, int64_t capacity, int64_t* host_k_union, void* stream) {
+  if (!h) return SCAPE_EINVAL;
+  if (!h->bound) return fail(h, SCAPE_ESTATE, "scape_union_step: call scape_bind first");
+  if (!host_grad_ptrs || !workspace || !host_k_union)
+    return fail(h, SCAPE_EINVAL, "scape_union_step: NULL pointer");
+  if (capacity < 1 || capacity > h->P)
+    return fail(h, SCAPE_EINVAL, "scape_union_step: capacity out of [1, P]");
+  const UnionLayout L = union_layout(h, capacity);
+  if (ws_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0)
+    return fail(h, SCAPE_EINVAL, "scape_union_step: workspace too small or not 256-byte aligned");
+  char* ws = static_cast<char*>(workspace);
+  int64_t* ustart = reinterpret_cast<int64_t*>(ws + L.start);
+  int64_t* uk = reinterpret_cast<int64_t*>(ws + L.kk);
+  ShardSel* usel = reinterpret_cast<ShardSel*>(ws + L.sel);
+  uint32_t* uhist = reinterpret_cast<uint32_t*>(ws + L.hist);
+  uint2* ucand = reinterpret_cast<uint2*>(ws + L.cand);
+  uint32_t* ucnt = reinterpret_cast<uint32_t*>(ws + L.ccnt);
+  uint32_t* ubits = reinterpret_cast<uint32_t*>(ws + L.bits);
+  uint32_t* utcnt = reinterpret_cast<uint32_t*>(ws + L.tcnt);
+  uint32_t* utbase = reinterpret_cast<uint32_t*>(ws + L.tbase);
+  uint32_t* uscan = reinterpret_cast<uint32_t*>(ws + L.scan);
+  uint32_t* uidx = reinterpret_cast<uint32_t*>(ws + L.idx);
+  float* upack = reinterpret_cast<float*>(ws + L.pack);
+  float* ugbar = reinterpret_cast<float*>(ws + L.gbar);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t kw = union_k_worker(h);
+  cudaError_t e = cudaSuccess;
+  if (h->union_ws != workspace) {
+    // new workspace: one-shard table over the whole vector, no bucket guesses
+    const int64_t tab[3] = {0, h->P, kw};
+    e = cudaMemcpy(ustart, tab, 16, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(uk, tab + 2, 8, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemset(usel, 0xFF, sizeof(ShardSel) * h->W);
+    if (e != cudaSuccess) return cuda_fail(h, e, "scape_union_step: workspace setup");
+    h->union_ws = workspace;
+  }
+  WorkerPtrs p;
+  std::memset(&p, 0, sizeof p);
+  bool vec = true;
+  for (int w = 0; w < h->W; ++w) {
+    if (!host_grad_ptrs[w]) return fail(h, SCAPE_EINVAL, "scape_union_step: NULL gradient pointer");
+    p.g[w] = host_grad_ptrs[w];
+    p.e[w] = h->e[w];
+    vec = vec && aligned16(host_grad_ptrs[w]);
+  }
+  const int64_t t = h->t + 1;
+  const AdamsConst c = make_const(h, t);
+  // 1. a^w = g^w + e^w, kept in the residual buffers
+  int rc = run_kernel(h, kKEfAdd, st, [&] { return launch_ef_add(p, h->W, h->P, h->dtype, vec, st); });
+  if (rc) return rc;
+  e = cudaMemsetAsync(ubits, 0, (size_t)h->nwords * 4, st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "scape_union_step: bitmap clear");
+  // 2. each worker's top-k over the whole vector, OR-ed into the union
+  for (int w = 0; w < h->W; ++w) {
+    const float* a = h->e[w];
+    ShardSel* sw = usel + w;
+    if (kw < h->P) {
+      e = cudaMemsetAsync(uhist, 0, (size_t)kCandBins0 * 4, st);
+      if (e == cudaSuccess) e = cudaMemsetAsync(ucnt, 0, 4, st);
+      if (e != cudaSuccess) return cuda_fail(h, e, "scape_union_step: histogram clear");
+      rc = run_kernel(h, kKCandHist0, st, [&] {
+        return launch_chist0(a, h->P, 1, ustart, sw, uhist, ucand, ucnt, st);
+      });
+      if (rc) return rc;
+    }
+    rc = run_kernel(h, kKCandSelect, st,
+                    [&] { return launch_cselect(0, 1, ustart, uk, sw, uhist, ucnt, st); });
+    if (rc) return rc;
+    if (kw < h->P) {
+      rc = run_kernel(h, kKCandCollect, st, [&] {
+        return launch_collect(a, h->P, 1, ustart, sw, ucand, ucnt, st);
+      });
+      if (rc) return rc;
+      for (int pass = 1; pass <= 5; ++pass) {
+        rc = run_kernel(h, kKCandHist, st, [&] {
+          return launch_chist(pass, 1, 1200, ustart, sw, ucand, ucnt, uhist, st);
+        });
+        if (rc) return rc;
+        rc = run_kernel(h, kKCandSelect, st,
+                        [&] { return launch_cselect(pass, 1, ustart, uk, sw, uhist, ucnt, st); });
+        if (rc) return rc;
+      }
+    }
+    rc = run_kernel(h, kKMark, st, [&] {
+      return launch_mark(a, h->P, 1, ustart, sw, ubits, utcnt, st, /*accumulate=*/true);
+    });
+    if (rc) return rc;
+  }
+  // 3. rank table and index list of the union; its size to the host
+  rc = run_kernel(h, kKTileCount, st, [&] { return launch_tile_count(ubits, h->P, utcnt, st); });
+  if (rc) return rc;
+  rc = run_kernel(
+      h, kKScan, st, [&] { return launch_scan(utcnt, h->ntiles, utbase, uscan, st); },
+      kScanLaunches);
+  if (rc) return rc;
+  rc = run_kernel(h, kKIndex, st, [&] { return launch_index(ubits, h->P, utbase, uidx, st); });
+  if (rc) return rc;
+  uint32_t ku = 0;
+  e = cudaMemcpyAsync(&ku, utbase + h->ntiles, 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "scape_union_step: union size readback");
+  *host_k_union = ku;
+  if ((int64_t)ku > capacity)
+    return fail(h, SCAPE_EINVAL,
+                "scape_union_step: union larger than capacity (residuals now hold g + e)");
+  // 4. every worker sends its values at every union position; mean; AdamS
+  rc = run_kernel(h, kKUnionMove, st,
+                  [&] { return launch_union_move(p, h->W, uidx, ku, upack, L.cstride, st); });
+  if (rc) return rc;
+  rc = run_kernel(h, kKReduce, st,
+                  [&] { return launch_reduce(upack, L.cstride, h->W, ku, ugbar, st); });
+  if (rc) return rc;
+  rc = run_kernel(h, kKAdamsSparse, st, [&] {
+    return launch_adams_sparse(uidx, ugbar, ku, h->w, h->m, c, false, st);
+  });
+  if (rc) return rc;
+  h->t = t;
+  return SCAPE_OK;
 }
 
 int scape_set_lr(scape_t* h, float lr) {

@@ -78,6 +78,8 @@ enum KernelId {
   kKOffmask,
   kKDenseAdams,
   kKAdamW,
+  kKEfAdd,
+  kKUnionMove,
   kNumKernels
 };
 static_assert(kNumKernels == SCAPE_NUM_KERNELS, "kernel table size");
@@ -200,9 +202,15 @@ cudaError_t launch_tie_count(const float* m, int W, const int64_t* shard_start,
                              cudaStream_t st);
 cudaError_t launch_tie_select(const float* m, int W, const int64_t* shard_start, ShardSel* sel,
                               const uint32_t* eqcnt, int64_t nchunk, cudaStream_t st);
+// accumulate: OR the new bits into `bits` instead of overwriting them.
 cudaError_t launch_mark(const float* m, int64_t P, int W, const int64_t* shard_start,
                         const ShardSel* sel, uint32_t* bits, uint32_t* tile_cnt,
-                        cudaStream_t st);
+                        cudaStream_t st, bool accumulate = false);
+// union-mask baseline (union_kernels.cu)
+cudaError_t launch_ef_add(const WorkerPtrs& p, int W, int64_t P, int dtype, bool vec,
+                          cudaStream_t st);
+cudaError_t launch_union_move(const WorkerPtrs& p, int W, const uint32_t* idx, int64_t k,
+                              float* pack, int64_t stride, cudaStream_t st);
 cudaError_t launch_tile_count(const uint32_t* bits, int64_t P, uint32_t* tile_cnt,
                               cudaStream_t st);
 // Three launches; `scratch` holds scan_scratch_words(ntiles) words.

@@ -83,6 +83,19 @@ class Scape:
             raise ValueError("v must be a float32 CUDA tensor of P elements")
         C.scape_adamw_step(self.h, [g.data_ptr() for g in grads], v.data_ptr(), self._stream())
 
+    def union_step(self, grads, capacity=None):
+        """Union-mask gradient top-k baseline step; returns the union size.
+        The workspace (packed buffers for `capacity` union positions, default
+        P) is allocated on first use and kept."""
+        cap = self.P if capacity is None else int(capacity)
+        if getattr(self, "_union_cap", None) != cap:
+            nbytes = C.scape_union_workspace_bytes(self.h, cap)
+            self._union_ws = torch.empty(nbytes, dtype=torch.uint8, device=self.params.device)
+            self._union_cap = cap
+        return C.scape_union_step(self.h, [g.data_ptr() for g in grads],
+                                  self._union_ws.data_ptr(), self._union_ws.numel(), cap,
+                                  self._stream())
+
     def set_lr(self, lr):
         C.scape_set_lr(self.h, lr)
 

@@ -71,3 +71,43 @@ def test_dense_baselines_match_oracle(cuda_device, adamw, P, W, dtype):
     for e in opt.e:                                  # residuals untouched
         assert not e.any()
     opt.close()
+
+
+# ------------------------------------------------------------ union-mask baseline
+@pytest.mark.parametrize("P,W,s,dtype,quant", [(4096, 4, 0.9, "f32", False),
+                                               (70001, 8, 0.99, "bf16", False),
+                                               (30000, 3, 0.9, "f32", True),
+                                               (5000, 2, 0.0, "f32", False)])
+def test_union_baseline_matches_oracle(cuda_device, P, W, s, dtype, quant):
+    gdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    wl = synth.Workload(f"p{P}", (("flat", P),), W=W, sparsity=s, steps=5, grad_dtype=dtype,
+                        quantum=2.0 ** -15 if quant else None)
+    gen = synth.GradientStream(wl, seed=6, device="cpu")
+    w0 = synth.init_params(P, seed=6)
+    params = w0.to(cuda_device)
+    opt = make_opt(params, W, s, gdt)
+    w, m = w0.numpy().copy(), np.zeros(P, np.float32)
+    e = [np.zeros(P, np.float32) for _ in range(W)]
+    kw = O.union_k_worker(P, s)
+    for t in range(1, 6):
+        grads = gen.next()
+        ku = opt.union_step([g.to(cuda_device) for g in grads])
+        bits, idx, pack, gbar = O.union_topk_step(t, [synth.to_numpy_grad(g) for g in grads],
+                                                  e, w, m, kw, HP)
+        assert ku == idx.size
+    torch.cuda.synchronize()
+    assert_close_f32(params.cpu().numpy(), w, "w")
+    assert np.array_equal(u32(params), w.view(np.uint32))
+    assert np.array_equal(u32(opt.m), m.view(np.uint32))
+    for wk in range(W):
+        assert np.array_equal(u32(opt.e[wk]), e[wk].view(np.uint32))
+    opt.close()
+
+
+def test_union_capacity_overflow_is_reported(cuda_device):
+    P, W = 8192, 8
+    opt = make_opt(torch.zeros(P, device=cuda_device), W, 0.9, torch.float32)
+    g = [torch.randn(P, device=cuda_device) for _ in range(W)]
+    with pytest.raises(C.ScapeError):
+        opt.union_step(g, capacity=O.union_k_worker(P, 0.9))   # independent noise fills in
+    opt.close()
