@@ -229,7 +229,7 @@ def bench_gpu(args, wl):
     import torch.distributed as dist
 
     import sparse_communication_sharded_gb300 as pkg
-    from sparse_communication_sharded_gb300 import synth
+    from sparse_communication_sharded_gb300 import multirank, synth
 
     ws, rank, local = _dist()
     if ws > 1:
@@ -310,13 +310,20 @@ def bench_gpu(args, wl):
 
     # dense baselines on the same workload and buffers (after the SCAPE timing)
     baselines = None
-    if args.baselines:
+    if args.baselines and ws == 1:
         baselines = bench_baselines(opt, wl, grads, dev)
 
     # end to end through the C ABI from pinned host memory
     e2e = None
     if args.e2e_steps > 0:
-        e2e = bench_e2e(opt, wl, grads, args.e2e_steps, dev)
+        e2e = bench_e2e(opt, wl, grads, args.e2e_steps, dev, shared_source=ws > 1)
+        if ws > 1:
+            # whole job: every rank stepped P parameters; the slowest rank sets the time
+            t_e2e = multirank.max_over_ranks(e2e["ms_per_step"], device=dev)
+            e2e["ms_per_step"] = t_e2e
+            e2e["value"] = ws * P / (t_e2e / 1000.0)
+            e2e["h2d_bytes_per_step"] *= ws
+            e2e["d2h_bytes_per_step"] *= ws
 
     cpu = None
     if rank == 0 and ws == 1 and args.cpu_steps > 0:
@@ -409,7 +416,7 @@ def bench_baselines(opt, wl, grads, dev, warmup=2, steps=5):
     return out
 
 
-def bench_e2e(opt, wl, dev_grads, steps, dev):
+def bench_e2e(opt, wl, dev_grads, steps, dev, shared_source=False):
     """Same step through scape_step_host: per step the W gradients are copied
     from pinned host memory, the step and refresh run, and w[P] is copied back."""
     import torch
@@ -418,7 +425,7 @@ def bench_e2e(opt, wl, dev_grads, steps, dev):
     gdt = dev_grads[0].dtype
     esz = dev_grads[0].element_size()
     need = W * P * esz + 4 * P
-    if _mem_available() > 3 * need:
+    if not shared_source and _mem_available() > 3 * need:
         host = [torch.empty(P, dtype=gdt).pin_memory() for _ in range(W)]
         shared = False
     else:

@@ -289,6 +289,10 @@ mark_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __rest
     }
   }
   const int64_t nwords = (P + 31) / 32;
+  // Whole-tile fast path: "key > kstar, or key == kstar and i <= istar" is
+  // "key >= kstar + (i > istar)", with i taken relative to the tile in 32 bits.
+  const int64_t rel64 = istar_s - t0;
+  const int lim = rel64 < 0 ? -1 : (rel64 >= kTile ? kTile : (int)rel64);
   uint32_t cnt = 0;
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
@@ -296,11 +300,10 @@ mark_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __rest
     const float x[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
     uint32_t nib = 0;
     if (uniform && full) {
+      const int li = warp * 512 + 128 * r + 4 * lane;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t key = magnitude_key(x[q]);
-        nib |= (uint32_t)(key > kstar_s || (key == kstar_s && i0 + q <= istar_s)) << q;
-      }
+      for (int q = 0; q < 4; ++q)
+        nib |= (uint32_t)(magnitude_key(x[q]) >= kstar_s + (uint32_t)(li + q > lim)) << q;
     } else {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
