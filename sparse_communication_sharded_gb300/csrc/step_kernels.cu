@@ -69,7 +69,10 @@ __device__ __forceinline__ void store8_f32(float* p, const float (&x)[8]) {
 // (one byte of the mask bitmap).  The rank of every selected parameter in the
 // packed buffers is the tile's base (from the refresh's rank table) plus the
 // block-exclusive popcount prefix, computed once and reused for all W workers.
+// Workers whose loads are issued together, and resident blocks per SM (64
+// registers): measured best of {1,2,4} x {2,3,4} on GB300 (6.70 TB/s).
 constexpr int kWorkerUnroll = 2;
+constexpr int kEfMinBlocks = 4;
 
 // With MSYNC (first-moment buffer reading) a selected parameter is sent as
 // b = b1 m_{t-1} + (1 - b1) a instead of a; the residual is the same.
@@ -92,7 +95,7 @@ __device__ __forceinline__ void ef_select8(const float (&g)[8], const float (&e)
 }
 
 template <typename GT, bool VEC, bool MSYNC>
-__global__ void __launch_bounds__(kTileThreads, 3)
+__global__ void __launch_bounds__(kTileThreads, kEfMinBlocks)
 ef_compact_kernel(const __grid_constant__ WorkerPtrs ptrs, int W, int64_t P,
                   const uint32_t* __restrict__ bits, const uint32_t* __restrict__ tile_base,
                   float* __restrict__ pack, int64_t pack_stride, MomentPack mp) {

@@ -36,6 +36,8 @@ TRAJ = [
     (33333, 7, 0.99, "f32", True),      # ties + shard boundaries mid-word
     (5, 8, 0.5, "f32", False),          # P < W: empty shards
     (2048 * 3, 2, 0.75, "bf16", False),  # exact multiple of the tile
+    (1 << 16, 256, 0.99, "bf16", False),  # the largest W the ABI accepts
+    (3000, 256, 0.9, "f32", False),       # W = 256 with shards of 11-12 parameters
 ]
 
 
