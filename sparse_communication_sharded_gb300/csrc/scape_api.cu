@@ -202,7 +202,7 @@ int rebuild_from_bits(scape_t* h, cudaStream_t st, bool counts_ready) {
       kScanLaunches);
   if (rc) return rc;
   return run_kernel(h, kKIndex, st,
-                    [&] { return launch_index(h->bits(), h->P, h->tile_base(), h->idx(), st); });
+                    [&] { return launch_index(h->bits(), h->P, h->tile_base(), h->idx(), h->k, st); });
 }
 
 }  // namespace
@@ -639,7 +639,7 @@ int scape_union_step(scape_t* h, const void* const* host_grad_ptrs, void* worksp
       h, kKScan, st, [&] { return launch_scan(utcnt, h->ntiles, utbase, uscan, st); },
       kScanLaunches);
   if (rc) return rc;
-  rc = run_kernel(h, kKIndex, st, [&] { return launch_index(ubits, h->P, utbase, uidx, st); });
+  rc = run_kernel(h, kKIndex, st, [&] { return launch_index(ubits, h->P, utbase, uidx, -1, st); });
   if (rc) return rc;
   uint32_t ku = 0;
   e = cudaMemcpyAsync(&ku, utbase + h->ntiles, 4, cudaMemcpyDeviceToHost, st);

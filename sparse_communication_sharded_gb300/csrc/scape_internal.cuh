@@ -218,8 +218,9 @@ int64_t scan_scratch_words(int64_t ntiles);
 cudaError_t launch_scan(const uint32_t* tile_cnt, int64_t ntiles, uint32_t* tile_base,
                         uint32_t* scratch, cudaStream_t st);
 constexpr int kScanLaunches = 3;
+// k: number of set bits if known (picks the kernel for the density), else -1.
 cudaError_t launch_index(const uint32_t* bits, int64_t P, const uint32_t* tile_base,
-                         uint32_t* idx, cudaStream_t st);
+                         uint32_t* idx, int64_t k, cudaStream_t st);
 // candidate-based exact top-k threshold (topk_kernels.cu)
 constexpr int kCandBins0 = 4096;
 cudaError_t launch_chist0(const float* m, int64_t P, int W, const int64_t* shard_start,

@@ -105,12 +105,13 @@ extern "C" int scape_topk_mask_static(const float* m, int64_t P, int W, double s
   if ((reinterpret_cast<uintptr_t>(m) & 15u) != 0) return SCAPE_EINVAL;
 
   // host copy of the shard sizes: chunk-table stride and the all-kept case
-  int64_t nmax = 0;
+  int64_t nmax = 0, ktot = 0;
   bool all_dense = true;
   for (int s = 0; s < W; ++s) {
     const int64_t n = ((int64_t)(s + 1) * P) / W - ((int64_t)s * P) / W;
     const int64_t k = (n * (1000000 - ppm) + 999999) / 1000000;
     nmax = n > nmax ? n : nmax;
+    ktot += k;
     if (k != n) all_dense = false;
   }
   const int64_t nchunk = nmax > 0 ? (nmax + kTieChunk - 1) / kTieChunk : 1;
@@ -150,6 +151,6 @@ extern "C" int scape_topk_mask_static(const float* m, int64_t P, int W, double s
   if ((e = launch_mark(m, P, W, start, sel, bits, tile_cnt, st)) != cudaSuccess) return SCAPE_ECUDA;
   if ((e = launch_scan(tile_cnt, ntiles, tile_base, scan_scratch, st)) != cudaSuccess)
     return SCAPE_ECUDA;
-  if ((e = launch_index(bits, P, tile_base, idx, st)) != cudaSuccess) return SCAPE_ECUDA;
+  if ((e = launch_index(bits, P, tile_base, idx, ktot, st)) != cudaSuccess) return SCAPE_ECUDA;
   return SCAPE_OK;
 }
