@@ -46,16 +46,30 @@ def _grad_bytes(wl):
     return 2 if wl.grad_dtype == "bf16" else 4
 
 
-def algorithmic_bytes(wl, k):
-    """Bytes the method must move per step, by kernel (see the design notes)."""
+FUSION = {"none": 0, "sum": 1, "update": 2}  # scape_set_fusion levels
+
+
+def algorithmic_bytes(wl, k, fusion="sum"):
+    """Bytes the method must move per step, by kernel (see the design notes).
+    fusion "sum": the compaction also writes g_bar, so the packed buffers are
+    written but never re-read; "update": it also updates w and m at the k
+    selected coordinates (no index list or g_bar to read back)."""
     P, W, G = wl.P, wl.W, _grad_bytes(wl)
     ntiles = (P + 2047) // 2048
     ef = W * P * (G + 8) + P / 8 + 4 * ntiles + 4 * k * W
-    red = 4 * k * W + 4 * k
-    upd = 24 * k
     refresh = 4 * P + P / 8 + P / 8 + 4 * k
-    return {"ef_compact": ef, "reduce": red, "adams_sparse": upd, "refresh": refresh,
-            "total": ef + red + upd + refresh}
+    out = {"refresh": refresh}
+    if fusion == "update":
+        out["ef_compact"] = ef + 4 * k + 16 * k
+    elif fusion == "sum":
+        out["ef_compact"] = ef + 4 * k
+        out["adams_sparse"] = 24 * k
+    else:
+        out["ef_compact"] = ef
+        out["reduce"] = 4 * k * W + 4 * k
+        out["adams_sparse"] = 24 * k
+    out["total"] = sum(out.values())
+    return out
 
 
 def _kernel_source_hash():
@@ -248,6 +262,7 @@ def bench_gpu(args, wl):
     params = synth.init_params(P, seed=seed, device=dev)
     opt = pkg.Scape(params, W, wl.sparsity, layer_numel=[n for _, n in wl.layers],
                     grad_dtype=gdt, residuals=args.residuals)
+    opt.set_fusion(FUSION[args.fusion])
     gen = synth.GradientStream(wl, seed=seed, device=dev)
     grads = gen.alloc()
 
@@ -293,7 +308,7 @@ def bench_gpu(args, wl):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         t_max = float(tt.item())
     value = ws * P / (t_max / 1000.0)
-    alg = algorithmic_bytes(wl, opt.k)
+    alg = algorithmic_bytes(wl, opt.k, fusion=args.fusion)
     peak, peak_kind = _peaks()
 
     ef_ms, ef_n = prof["ef_compact"]
@@ -340,7 +355,7 @@ def bench_gpu(args, wl):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": wl.name, "P": P, "W": W, "sparsity": wl.sparsity,
                        "k": opt.k, "grad_dtype": wl.grad_dtype, "state_dtype": "f32",
-                       "residuals": args.residuals,
+                       "residuals": args.residuals, "fusion": args.fusion,
                        "l2": "inputs larger than L2 (gradients + residuals far beyond 129 MB)",
                        "parallelism": f"{ws} independent problems (weak)"},
             "hbm_gbs": alg["total"] / (t_max / 1000.0) / 1e9,
@@ -437,6 +452,11 @@ def bench_e2e(opt, wl, dev_grads, steps, dev, shared_source=False):
         h_.copy_(d)
     out = torch.empty(P, dtype=torch.float32).pin_memory()
     st = torch.cuda.current_stream()
+    # untimed: the first transfers from freshly pinned pages, and the library's
+    # copy stream and events, are one-time costs
+    for _ in range(2):
+        opt.step_host(host, dev_grads, out)
+    st.synchronize()
     times = []
     for _ in range(steps):
         torch.cuda.synchronize()
@@ -448,6 +468,7 @@ def bench_e2e(opt, wl, dev_grads, steps, dev, shared_source=False):
     del host
     return {"value": P / secs, "unit": UNIT, "h2d_bytes_per_step": W * P * esz,
             "d2h_bytes_per_step": 4 * P, "ms_per_step": 1000 * secs,
+            "ms_each": [1000 * x for x in times],
             "shared_host_source": shared}
 
 
@@ -462,6 +483,9 @@ def main(argv=None):
     ap.add_argument("--cpu-steps", type=int, default=2)
     ap.add_argument("--residuals", default="device", choices=["device", "host"],
                     help="error-feedback buffers in HBM or in pinned host memory")
+    ap.add_argument("--fusion", default="sum", choices=sorted(FUSION),
+                    help="what the compaction pass also does: none (separate reduce and "
+                         "adams_sparse), sum (writes g_bar), update (also AdamS)")
     ap.add_argument("--baselines", type=int, default=1,
                     help="also time the dense AdamS and AdamW baselines (0 to skip)")
     ap.add_argument("--P", type=int, default=None,

@@ -179,6 +179,24 @@ enum scape_variant {
 int scape_set_variant(scape_t *h, int flags);
 
 /*
+ * How much of the step the compaction pass does (results are bit-identical
+ * at every level).  The compaction sees every worker of a tile, so it can
+ * form the synchronised buffer while the residuals stream through:
+ *   SCAPE_FUSE_NONE    the ordered sum of the W packed buffers and the
+ *       unpack + AdamS run as two separate launches after it, the layout of
+ *       "Sintesi Tecnica: SCAPE" Sec. 2;
+ *   SCAPE_FUSE_SUM     (default) the compaction also writes g_bar
+ *       (worker-ordered sum / W); the unpack + AdamS runs as its own launch;
+ *   SCAPE_FUSE_UPDATE  the compaction also applies AdamS at the selected
+ *       coordinates (no further launch; its scattered w and m accesses then
+ *       interleave with the residual stream, which measured slower).
+ * The packed buffers and g_bar are written at every level.
+ * Errors: SCAPE_EINVAL for an unknown level.
+ */
+enum scape_fusion { SCAPE_FUSE_NONE = 0, SCAPE_FUSE_SUM = 1, SCAPE_FUSE_UPDATE = 2 };
+int scape_set_fusion(scape_t *h, int level);
+
+/*
  * Dense baselines the pages compare SCAPE against ("SCAPE" abstract, Sec. I),
  * on the handle's bound w and m: the gradient is the plain ordered mean of
  * the W workers' gradients (no error feedback, no mask; residuals untouched)
@@ -250,11 +268,17 @@ int scape_set_state(scape_t *h, int64_t t, const uint32_t *bits, void *stream);
  * memory (pinned for asynchronous copies) into the caller's device gradient
  * buffers, run scape_step() and scape_refresh_mask(), then copy w[P] back to
  * host_params_out.  From step 2 on, the uploads run on an internal copy stream
- * in up to 8 worker groups and each group's compaction starts on `stream` as
- * soon as its gradients have landed; the parameter download overlaps the mask
- * refresh.  All of the call's work is ordered before later work on `stream`:
- * synchronise `stream` before reading host_params_out or reusing the host
- * gradient buffers.  The first call creates the copy stream and its events.
+ * in up to 16 worker groups and each group's compaction starts on `stream` as
+ * soon as its gradients have landed.  When host_params_out is page-locked and
+ * only the selected coordinates change (the default reading), w is downloaded
+ * on a second internal stream while the gradients upload (the previous
+ * parameters) and a kernel then writes the k updated values into
+ * host_params_out through its device address; otherwise w is downloaded after
+ * the update, overlapping the mask refresh.  Either way host_params_out ends
+ * holding all P parameters after the step.  All of the call's work is ordered
+ * before later work on `stream`: synchronise `stream` before reading
+ * host_params_out or reusing the host gradient buffers.  The first call
+ * creates the internal streams and their events.
  */
 int scape_step_host(scape_t *h, const void *const *host_grads_src,
                     void *const *host_dev_grad_ptrs, float *host_params_out, void *stream);
@@ -266,7 +290,7 @@ int scape_step_host(scape_t *h, const void *const *host_grads_src,
  * scape_profile_read() copies the totals (milliseconds and launch counts,
  * SCAPE_NUM_KERNELS entries each) and scape_kernel_name() names entry i.
  */
-#define SCAPE_NUM_KERNELS 18
+#define SCAPE_NUM_KERNELS 22
 int scape_profile_enable(scape_t *h, int on);
 int scape_profile_collect(scape_t *h);
 int scape_profile_read(const scape_t *h, double *host_ms, int64_t *host_launches);

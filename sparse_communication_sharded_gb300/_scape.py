@@ -19,7 +19,7 @@ SCAPE_ESTATE = -4
 SCAPE_F32 = 0
 SCAPE_BF16 = 1
 SCAPE_MAX_WORKERS = 256
-SCAPE_NUM_KERNELS = 18
+SCAPE_NUM_KERNELS = 22
 
 LIB_PATH = _build.LIB
 
@@ -46,6 +46,7 @@ _PROTOS = {
     "scape_refresh_mask": (_i32, [_vp, _vp]),
     "scape_set_lr": (_i32, [_vp, _f32]),
     "scape_set_variant": (_i32, [_vp, _i32]),
+    "scape_set_fusion": (_i32, [_vp, _i32]),
     "scape_dense_adams_step": (_i32, [_vp, _vp, _vp]),
     "scape_union_workspace_bytes": (_i32, [_vp, _i64, _vp]),
     "scape_union_step": (_i32, [_vp, _vp, _vp, ctypes.c_size_t, _i64, _vp, _vp]),
@@ -155,6 +156,13 @@ SCAPE_VARIANT_MOMENT_SYNC = 2
 
 def scape_set_variant(h, flags):
     _check(h, load().scape_set_variant(h, int(flags)))
+
+
+FUSE_NONE, FUSE_SUM, FUSE_UPDATE = 0, 1, 2
+
+
+def scape_set_fusion(h, level):
+    _check(h, load().scape_set_fusion(h, int(level)))
 
 
 def scape_dense_adams_step(h, grad_ptrs, stream=0):

@@ -259,15 +259,14 @@ tie_select_kernel(const float* __restrict__ m, const int64_t* __restrict__ shard
 // [512q, 512q + 512) of the tile in four rounds of 128: lane l decides the four
 // parameters of one 16-byte load, the 4-bit pieces of 8 neighbouring lanes are
 // OR-ed into one 32-bit word by shuffles, and lane 8g writes word g of the round.
-__global__ void __launch_bounds__(128)
-mark_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __restrict__ shard_start,
-            const ShardSel* __restrict__ sel, uint32_t* __restrict__ bits,
-            uint32_t* __restrict__ tile_cnt, bool accumulate) {
+__device__ __forceinline__ void mark_tile(int64_t tile, const float* __restrict__ m, int64_t P,
+                                          int W, const int64_t* __restrict__ shard_start,
+                                          const ShardSel* __restrict__ sel,
+                                          uint32_t* __restrict__ bits,
+                                          uint32_t* __restrict__ tile_cnt, bool accumulate) {
   __shared__ uint32_t warp_cnt[4];
   __shared__ int sh_s, sh_uniform, sh_lim;
   __shared__ uint32_t sh_kstar;
-  __shared__ int64_t sh_istar;
-  const int64_t tile = blockIdx.x;
   const int64_t t0 = tile * kTile;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t wb = t0 + warp * 512;
@@ -295,14 +294,12 @@ mark_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __rest
     sh_s = s0;
     sh_uniform = __ldg(shard_start + s0 + 1) >= t1;
     sh_kstar = sel[s0].kstar;
-    sh_istar = ist;
     sh_lim = rel64 < 0 ? -1 : (rel64 >= kTile ? kTile : (int)rel64);
   }
   __syncthreads();
   const int s = sh_s;
   const bool uniform = sh_uniform != 0;
   const uint32_t kstar_s = sh_kstar;
-  const int64_t istar_s = sh_istar;
 
   const int64_t nwords = (P + 31) / 32;
   // Whole-tile fast path: "key > kstar, or key == kstar and i <= istar" is
@@ -348,6 +345,34 @@ mark_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __rest
   if (lane == 0) warp_cnt[warp] = cnt;
   __syncthreads();
   if (threadIdx.x == 0) tile_cnt[tile] = warp_cnt[0] + warp_cnt[1] + warp_cnt[2] + warp_cnt[3];
+}
+
+__global__ void __launch_bounds__(128)
+mark_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __restrict__ shard_start,
+            const ShardSel* __restrict__ sel, uint32_t* __restrict__ bits,
+            uint32_t* __restrict__ tile_cnt, bool accumulate) {
+  mark_tile(blockIdx.x, m, P, W, shard_start, sel, bits, tile_cnt, accumulate);
+}
+
+// Warm refresh, grid (G, W): the tiles starting in shard s that the
+// speculative bitmap does not cover -- all of them when the shard is flagged
+// kSelRemark, else only its last one when it crosses the shard's end (or the
+// end of the vector).  Each tile is owned by the shard it starts in.
+__global__ void __launch_bounds__(128)
+remark_kernel(const float* __restrict__ m, int64_t P, int W,
+              const int64_t* __restrict__ shard_start, const ShardSel* __restrict__ sel,
+              uint32_t* __restrict__ bits, uint32_t* __restrict__ tile_cnt) {
+  const int s = blockIdx.y;
+  const int64_t s_lo = shard_start[s], s_hi = shard_start[s + 1];
+  if (s_lo >= s_hi) return;
+  int64_t t_begin = (s_lo + kTile - 1) / kTile;
+  const int64_t t_end = (s_hi + kTile - 1) / kTile;
+  if (!(sel[s].flags & kSelRemark)) {
+    if (t_end <= t_begin || t_end * kTile == s_hi) return;
+    t_begin = t_end - 1;
+  }
+  for (int64_t t = t_begin + blockIdx.x; t < t_end; t += gridDim.x)
+    mark_tile(t, m, P, W, shard_start, sel, bits, tile_cnt, false);
 }
 
 // Per-tile popcount of an existing bitmap (checkpoint resume).
@@ -536,6 +561,30 @@ cudaError_t launch_mark(const float* m, int64_t P, int W, const int64_t* shard_s
                         cudaStream_t st, bool accumulate) {
   const unsigned grid = (unsigned)((P + kTile - 1) / kTile);
   mark_kernel<<<grid, 128, 0, st>>>(m, P, W, shard_start, sel, bits, tile_cnt, accumulate);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_remark(const float* m, int64_t P, int W, const int64_t* shard_start,
+                          const ShardSel* sel, uint32_t* bits, uint32_t* tile_cnt,
+                          cudaStream_t st) {
+  // enough 128-thread blocks to fill the GPU when every shard is re-marked;
+  // in the common case all but one block per shard return at once
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+      sms = n;
+    else
+      sms = 148;
+  }
+  const int64_t ntiles = (P + kTile - 1) / kTile;
+  const int64_t per_shard = (ntiles + W - 1) / W + 1;
+  int64_t gx = ((int64_t)sms * 16 + W - 1) / W;
+  if (gx > per_shard) gx = per_shard;
+  if (gx < 1) gx = 1;
+  remark_kernel<<<dim3((unsigned)gx, (unsigned)W), 128, 0, st>>>(m, P, W, shard_start, sel, bits,
+                                                                 tile_cnt);
   return cudaGetLastError();
 }
 

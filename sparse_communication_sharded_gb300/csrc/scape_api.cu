@@ -25,7 +25,8 @@ thread_local std::string g_create_error;
 const char* const kKernelNames[kNumKernels] = {
     "dense_step",  "ef_compact", "reduce", "adams_sparse", "cand_hist0", "cand_select",
     "cand_collect", "cand_hist",  "mark",   "scan",         "index",      "shard_count",
-    "tile_count",  "offmask",    "dense_adams", "adamw", "ef_add", "union_move"};
+    "tile_count",  "offmask",    "dense_adams", "adamw", "ef_add", "union_move", "spec_mark",
+    "fixup", "remark", "param_patch"};
 
 struct ProfRec {
   int kid;
@@ -48,6 +49,7 @@ struct scape {
   int cand_blocks = 1;  // blocks per shard of the candidate histogram passes
   bool all_dense = false;  // every shard keeps all of its coordinates
   int variant = SCAPE_VARIANT_PAPER;
+  int fusion = SCAPE_FUSE_SUM;  // what the compaction pass also does
   // workspace offsets (bytes)
   size_t off_bits = 0, off_idx = 0, off_tbase = 0, off_tcnt = 0, off_pack = 0, off_gbar = 0,
          off_hist = 0, off_sel = 0, off_cand = 0, off_ccnt = 0, off_scan = 0, off_sstart = 0,
@@ -62,15 +64,16 @@ struct scape {
   // state
   int64_t t = 0;
   bool mask_ready = false;
+  bool warm = false;  // the select state holds a finished threshold per shard
   bool buffers_valid = false;
   int64_t launches = 0;
   // union-mask baseline: workspace whose per-worker selection state is live
   const void* union_ws = nullptr;
   // end-to-end pipelining (created on the first scape_step_host call)
-  static constexpr int kMaxGroups = 8;
+  static constexpr int kMaxGroups = 16;
   bool aux_ready = false;
-  cudaStream_t copy_stream = nullptr;
-  cudaEvent_t ev_start = nullptr, ev_updated = nullptr, ev_done = nullptr;
+  cudaStream_t copy_stream = nullptr, down_stream = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_updated = nullptr, ev_done = nullptr, ev_down = nullptr;
   cudaEvent_t ev_group[kMaxGroups] = {};
   // profiling
   bool prof = false;
@@ -92,6 +95,7 @@ struct scape {
   ShardSel* sel() const { return at<ShardSel>(off_sel); }
   uint2* cand() const { return at<uint2>(off_cand); }
   uint32_t* cand_cnt() const { return at<uint32_t>(off_ccnt); }
+  uint32_t* above_cnt() const { return at<uint32_t>(off_ccnt) + W; }
   uint32_t* scan_scratch() const { return at<uint32_t>(off_scan); }
   int64_t* d_shard_start() const { return at<int64_t>(off_sstart); }
   int64_t* d_shard_k() const { return at<int64_t>(off_sk); }
@@ -156,8 +160,11 @@ AdamsConst make_const(const scape_t* h, int64_t t) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Compaction of workers [w0, w1) into rows w0.. of the packed buffers.
-int enqueue_compact(scape_t* h, const WorkerPtrs& all, int w0, int w1, bool vec, cudaStream_t st) {
+// Compaction of workers [w0, w1) into rows w0.. of the packed buffers; with
+// the fused update, the ordered sum continues across the groups in g_bar and
+// the group that ends at W applies AdamS.
+int enqueue_compact(scape_t* h, const WorkerPtrs& all, int w0, int w1, bool vec,
+                    const AdamsConst& c, cudaStream_t st) {
   const MomentPack mp{h->m, h->beta1, 1.0f - h->beta1};
   const MomentPack* mpp = (h->variant & SCAPE_VARIANT_MOMENT_SYNC) ? &mp : nullptr;
   WorkerPtrs p;
@@ -166,23 +173,36 @@ int enqueue_compact(scape_t* h, const WorkerPtrs& all, int w0, int w1, bool vec,
     p.g[w - w0] = all.g[w];
     p.e[w - w0] = all.e[w];
   }
+  EfFuse fz{h->gbar(), h->w, h->m, c, h->W, 0};
+  if (h->fusion != SCAPE_FUSE_NONE) {
+    fz.flags = kEfAccum;
+    if (w0 > 0) fz.flags |= kEfResume;
+    if (w1 == h->W) fz.flags |= kEfFinish;
+    if (w1 == h->W && h->fusion == SCAPE_FUSE_UPDATE) fz.flags |= kEfUpdate;
+  }
   return run_kernel(h, kKEfCompact, st, [&] {
     return launch_ef_compact(p, w1 - w0, h->P, h->dtype, vec, h->bits(), h->tile_base(),
-                             h->pack() + (int64_t)w0 * h->kstride, h->kstride, mpp, st);
+                             h->pack() + (int64_t)w0 * h->kstride, h->kstride, mpp, fz, st);
   });
 }
 
-// The ordered sum of the packed buffers and the sparse AdamS update (plus,
-// under the dense off-mask reading, the zero-gradient update elsewhere).
+// The ordered sum of the packed buffers and the sparse AdamS update, unless
+// the compaction already applied them (plus, under the dense off-mask
+// reading, the zero-gradient update elsewhere).
 int enqueue_update(scape_t* h, const AdamsConst& c, cudaStream_t st) {
-  int rc = run_kernel(h, kKReduce, st, [&] {
-    return launch_reduce(h->pack(), h->kstride, h->W, h->k, h->gbar(), st);
-  });
-  if (rc) return rc;
-  const bool msync = (h->variant & SCAPE_VARIANT_MOMENT_SYNC) != 0;
-  rc = run_kernel(h, kKAdamsSparse, st, [&] {
-    return launch_adams_sparse(h->idx(), h->gbar(), h->k, h->w, h->m, c, msync, st);
-  });
+  int rc = SCAPE_OK;
+  if (h->fusion == SCAPE_FUSE_NONE) {
+    rc = run_kernel(h, kKReduce, st, [&] {
+      return launch_reduce(h->pack(), h->kstride, h->W, h->k, h->gbar(), st);
+    });
+    if (rc) return rc;
+  }
+  if (h->fusion != SCAPE_FUSE_UPDATE) {
+    const bool msync = (h->variant & SCAPE_VARIANT_MOMENT_SYNC) != 0;
+    rc = run_kernel(h, kKAdamsSparse, st, [&] {
+      return launch_adams_sparse(h->idx(), h->gbar(), h->k, h->w, h->m, c, msync, st);
+    });
+  }
   if (rc || !(h->variant & SCAPE_VARIANT_DENSE_OFFMASK)) return rc;
   return run_kernel(h, kKOffmask, st,
                     [&] { return launch_offmask(h->bits(), h->P, h->w, h->m, c, st); });
@@ -285,7 +305,7 @@ int scape_create(scape_t** out, int n_layers, const int64_t* host_layer_numel, i
   h->off_sel = carve((size_t)W * sizeof(ShardSel));
   // candidates of shard s live in [shard_start[s], shard_start[s+1]): capacity = shard size
   h->off_cand = carve((size_t)P * sizeof(uint2));
-  h->off_ccnt = carve((size_t)W * 4);
+  h->off_ccnt = carve((size_t)W * 2 * 4);  // candidate counts, then counts above the window
   h->off_scan = carve((size_t)scan_scratch_words(h->ntiles) * 4);
   h->off_sstart = carve((size_t)(W + 1) * 8);
   h->off_sk = carve((size_t)W * 8);
@@ -307,7 +327,9 @@ void scape_destroy(scape_t* h) {
     cudaEventDestroy(h->ev_start);
     cudaEventDestroy(h->ev_updated);
     cudaEventDestroy(h->ev_done);
+    cudaEventDestroy(h->ev_down);
     cudaStreamDestroy(h->copy_stream);
+    cudaStreamDestroy(h->down_stream);
   }
   delete h;
 }
@@ -366,6 +388,7 @@ int scape_bind(scape_t* h, float* params, float* m, float* const* host_e_ptrs, v
   h->bound = true;
   h->t = 0;
   h->mask_ready = false;
+  h->warm = false;
   h->buffers_valid = false;
   return SCAPE_OK;
 }
@@ -397,7 +420,7 @@ int scape_step(scape_t* h, const void* const* host_grad_ptrs, void* stream) {
     if (rc) return rc;
     h->buffers_valid = false;
   } else {
-    rc = enqueue_compact(h, p, 0, h->W, vec, st);
+    rc = enqueue_compact(h, p, 0, h->W, vec, c, st);
     if (rc) return rc;
     rc = enqueue_update(h, c, st);
     if (rc) return rc;
@@ -407,25 +430,42 @@ int scape_step(scape_t* h, const void* const* host_grad_ptrs, void* stream) {
   return SCAPE_OK;
 }
 
-int scape_refresh_mask(scape_t* h, void* stream) {
-  if (!h) return SCAPE_EINVAL;
-  if (!h->bound) return fail(h, SCAPE_ESTATE, "scape_refresh_mask: call scape_bind first");
-  if (h->t < 1) return fail(h, SCAPE_ESTATE, "scape_refresh_mask: no step taken yet");
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+namespace {
+
+// Radix passes 1..5 over the staged candidates.
+int enqueue_radix(scape_t* h, cudaStream_t st) {
+  for (int pass = 1; pass <= 5; ++pass) {
+    int rc = run_kernel(h, kKCandHist, st, [&] {
+      return launch_chist(pass, h->W, h->cand_blocks, h->d_shard_start(), h->sel(), h->cand(),
+                          h->cand_cnt(), h->hist(), st);
+    });
+    if (rc) return rc;
+    rc = run_kernel(h, kKCandSelect, st, [&] {
+      return launch_cselect(pass, h->W, h->d_shard_start(), h->d_shard_k(), h->sel(), h->hist(),
+                            h->cand_cnt(), kSelFormCold, st);
+    });
+    if (rc) return rc;
+  }
+  return SCAPE_OK;
+}
+
+// First refresh after bind (and every refresh of a mask of all ones): full
+// histogram, bucket, collect on a miss, radix passes, then the mark pass.
+int refresh_cold(scape_t* h, cudaStream_t st) {
   int rc;
   if (!h->all_dense) {
     cudaError_t e = cudaMemsetAsync(h->hist(), 0, (size_t)h->W * kCandBins0 * 4, st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(h->cand_cnt(), 0, (size_t)h->W * 4, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->cand_cnt(), 0, (size_t)h->W * 2 * 4, st);
     if (e != cudaSuccess) return cuda_fail(h, e, "scape_refresh_mask: histogram clear");
     rc = run_kernel(h, kKCandHist0, st, [&] {
       return launch_chist0(h->m, h->P, h->W, h->d_shard_start(), h->sel(), h->hist(), h->cand(),
-                           h->cand_cnt(), st);
+                           h->cand_cnt(), false, st);
     });
     if (rc) return rc;
   }
   rc = run_kernel(h, kKCandSelect, st, [&] {
     return launch_cselect(0, h->W, h->d_shard_start(), h->d_shard_k(), h->sel(), h->hist(),
-                          h->cand_cnt(), st);
+                          h->cand_cnt(), kSelFormCold, st);
   });
   if (rc) return rc;
   if (!h->all_dense) {
@@ -434,27 +474,92 @@ int scape_refresh_mask(scape_t* h, void* stream) {
                             h->cand_cnt(), st);
     });
     if (rc) return rc;
-    for (int pass = 1; pass <= 5; ++pass) {
-      rc = run_kernel(h, kKCandHist, st, [&] {
-        return launch_chist(pass, h->W, h->cand_blocks, h->d_shard_start(), h->sel(), h->cand(),
-                            h->cand_cnt(), h->hist(), st);
-      });
-      if (rc) return rc;
-      rc = run_kernel(h, kKCandSelect, st, [&] {
-        return launch_cselect(pass, h->W, h->d_shard_start(), h->d_shard_k(), h->sel(), h->hist(),
-                              h->cand_cnt(), st);
-      });
-      if (rc) return rc;
-    }
+    rc = enqueue_radix(h, st);
+    if (rc) return rc;
   }
-  rc = run_kernel(h, kKMark, st, [&] {
+  return run_kernel(h, kKMark, st, [&] {
     return launch_mark(h->m, h->P, h->W, h->d_shard_start(), h->sel(), h->bits(), h->tile_cnt(),
                        st);
   });
+}
+
+// Every later refresh: the bitmap is written speculatively from the previous
+// thresholds in the same read of m that stages the candidates; the new
+// thresholds only correct it.  Every launch is enqueued whatever the data
+// holds; the kernels for the rare cases (a shard whose threshold left its
+// bucket window) return at once when no shard needs them.
+int refresh_warm(scape_t* h, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(h->hist(), 0, (size_t)h->W * kCandBins0 * 4, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(h->cand_cnt(), 0, (size_t)h->W * 2 * 4, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(h->tile_cnt(), 0, (size_t)h->ntiles * 4, st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "scape_refresh_mask: count clear");
+  int rc = run_kernel(h, kKSpecMark, st, [&] {
+    return launch_spec(h->m, h->P, h->W, h->d_shard_start(), h->sel(), h->cand(), h->cand_cnt(),
+                       h->above_cnt(), h->bits(), h->tile_cnt(), st);
+  });
   if (rc) return rc;
+  rc = run_kernel(h, kKCandHist, st, [&] {
+    return launch_whist(h->W, h->cand_blocks, h->d_shard_start(), h->sel(), h->cand(),
+                        h->cand_cnt(), h->above_cnt(), h->hist(), st);
+  });
+  if (rc) return rc;
+  rc = run_kernel(h, kKCandSelect, st, [&] {
+    return launch_cselect(0, h->W, h->d_shard_start(), h->d_shard_k(), h->sel(), h->hist(),
+                          h->cand_cnt(), kSelFormWarm, st);
+  });
+  if (rc) return rc;
+  rc = run_kernel(h, kKCandHist0, st, [&] {
+    return launch_chist0(h->m, h->P, h->W, h->d_shard_start(), h->sel(), h->hist(), h->cand(),
+                         h->cand_cnt(), true, st);
+  });
+  if (rc) return rc;
+  rc = run_kernel(h, kKCandSelect, st, [&] {
+    return launch_cselect(0, h->W, h->d_shard_start(), h->d_shard_k(), h->sel(), h->hist(),
+                          h->cand_cnt(), kSelFormRerun, st);
+  });
+  if (rc) return rc;
+  rc = run_kernel(h, kKCandCollect, st, [&] {
+    return launch_collect(h->m, h->P, h->W, h->d_shard_start(), h->sel(), h->cand(),
+                          h->cand_cnt(), st);
+  });
+  if (rc) return rc;
+  rc = enqueue_radix(h, st);
+  if (rc) return rc;
+  rc = run_kernel(h, kKFixup, st, [&] {
+    return launch_fixup(h->d_shard_start(), h->sel(), h->cand(), h->cand_cnt(), h->W,
+                        h->cand_blocks, h->bits(), h->tile_cnt(), st);
+  });
+  if (rc) return rc;
+  return run_kernel(h, kKRemark, st, [&] {
+    return launch_remark(h->m, h->P, h->W, h->d_shard_start(), h->sel(), h->bits(),
+                         h->tile_cnt(), st);
+  });
+}
+
+}  // namespace
+
+int scape_refresh_mask(scape_t* h, void* stream) {
+  if (!h) return SCAPE_EINVAL;
+  if (!h->bound) return fail(h, SCAPE_ESTATE, "scape_refresh_mask: call scape_bind first");
+  if (h->t < 1) return fail(h, SCAPE_ESTATE, "scape_refresh_mask: no step taken yet");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int rc = (h->warm && !h->all_dense) ? refresh_warm(h, st) : refresh_cold(h, st);
+  if (rc) {
+    h->warm = false;
+    return rc;
+  }
   rc = rebuild_from_bits(h, st, true);
   if (rc) return rc;
+  h->warm = true;
   h->mask_ready = true;
+  return SCAPE_OK;
+}
+
+int scape_set_fusion(scape_t* h, int level) {
+  if (!h) return SCAPE_EINVAL;
+  if (level != SCAPE_FUSE_NONE && level != SCAPE_FUSE_SUM && level != SCAPE_FUSE_UPDATE)
+    return fail(h, SCAPE_EINVAL, "scape_set_fusion: unknown level");
+  h->fusion = level;
   return SCAPE_OK;
 }
 
@@ -605,12 +710,12 @@ int scape_union_step(scape_t* h, const void* const* host_grad_ptrs, void* worksp
       if (e == cudaSuccess) e = cudaMemsetAsync(ucnt, 0, 4, st);
       if (e != cudaSuccess) return cuda_fail(h, e, "scape_union_step: histogram clear");
       rc = run_kernel(h, kKCandHist0, st, [&] {
-        return launch_chist0(a, h->P, 1, ustart, sw, uhist, ucand, ucnt, st);
+        return launch_chist0(a, h->P, 1, ustart, sw, uhist, ucand, ucnt, false, st);
       });
       if (rc) return rc;
     }
     rc = run_kernel(h, kKCandSelect, st,
-                    [&] { return launch_cselect(0, 1, ustart, uk, sw, uhist, ucnt, st); });
+                    [&] { return launch_cselect(0, 1, ustart, uk, sw, uhist, ucnt, kSelFormCold, st); });
     if (rc) return rc;
     if (kw < h->P) {
       rc = run_kernel(h, kKCandCollect, st, [&] {
@@ -623,7 +728,7 @@ int scape_union_step(scape_t* h, const void* const* host_grad_ptrs, void* worksp
         });
         if (rc) return rc;
         rc = run_kernel(h, kKCandSelect, st,
-                        [&] { return launch_cselect(pass, 1, ustart, uk, sw, uhist, ucnt, st); });
+                        [&] { return launch_cselect(pass, 1, ustart, uk, sw, uhist, ucnt, kSelFormCold, st); });
         if (rc) return rc;
       }
     }
@@ -761,19 +866,38 @@ int scape_step_host(scape_t* h, const void* const* host_grads_src, void* const* 
   }
   if (!h->aux_ready) {
     e = cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking);
-    for (auto* ev : {&h->ev_start, &h->ev_updated, &h->ev_done})
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->down_stream, cudaStreamNonBlocking);
+    for (auto* ev : {&h->ev_start, &h->ev_updated, &h->ev_done, &h->ev_down})
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
     for (int g = 0; g < scape_t::kMaxGroups && e == cudaSuccess; ++g)
       e = cudaEventCreateWithFlags(&h->ev_group[g], cudaEventDisableTiming);
     if (e != cudaSuccess) return cuda_fail(h, e, "scape_step_host: stream/event setup");
     h->aux_ready = true;
   }
+  // Parameters: under the paper's reading a step changes w only at its k
+  // selected coordinates, so the dense download of w runs first (the previous
+  // parameters, on the second copy direction, while the gradients upload) and
+  // the k new values are written into the host copy afterwards by a kernel,
+  // through the page-locked buffer's device address.  Otherwise (pageable
+  // output, or every coordinate updated) w is downloaded after the update.
+  float* host_out_dev = nullptr;
+  const bool patch = !(h->variant & SCAPE_VARIANT_DENSE_OFFMASK) &&
+                     cudaHostGetDevicePointer(reinterpret_cast<void**>(&host_out_dev),
+                                              host_params_out, 0) == cudaSuccess;
+  if (!patch) (void)cudaGetLastError();  // not page-locked: clear the lookup's error
   // Worker groups: group g's uploads run on the copy stream while the
   // compaction of the groups before it runs on `stream`.
   const int G = h->W < scape_t::kMaxGroups ? h->W : scape_t::kMaxGroups;
-  cudaStream_t cp = h->copy_stream;
-  e = cudaEventRecord(h->ev_start, st);  // earlier users of the gradient buffers
+  cudaStream_t cp = h->copy_stream, dn = h->down_stream;
+  e = cudaEventRecord(h->ev_start, st);  // earlier users of the gradient and output buffers
   if (e == cudaSuccess) e = cudaStreamWaitEvent(cp, h->ev_start, 0);
+  if (e == cudaSuccess && patch) {
+    e = cudaStreamWaitEvent(dn, h->ev_start, 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(host_params_out, h->w, (size_t)h->P * 4, cudaMemcpyDeviceToHost, dn);
+    if (e == cudaSuccess) e = cudaEventRecord(h->ev_down, dn);
+  }
+  if (e != cudaSuccess) return cuda_fail(h, e, "scape_step_host: parameter download");
   for (int g = 0; g < G && e == cudaSuccess; ++g) {
     for (int w = g * h->W / G; w < (g + 1) * h->W / G && e == cudaSuccess; ++w)
       e = cudaMemcpyAsync(host_dev_grad_ptrs[w], host_grads_src[w], gbytes, cudaMemcpyHostToDevice,
@@ -793,20 +917,29 @@ int scape_step_host(scape_t* h, const void* const* host_grads_src, void* const* 
   const AdamsConst c = make_const(h, t);
   for (int g = 0; g < G; ++g) {
     e = cudaStreamWaitEvent(st, h->ev_group[g], 0);
+    // w changes from the last group on: the dense download must have read it
+    if (e == cudaSuccess && patch && g == G - 1) e = cudaStreamWaitEvent(st, h->ev_down, 0);
     if (e != cudaSuccess) return cuda_fail(h, e, "scape_step_host: stream wait");
-    const int rc = enqueue_compact(h, p, g * h->W / G, (g + 1) * h->W / G, vec, st);
+    const int rc = enqueue_compact(h, p, g * h->W / G, (g + 1) * h->W / G, vec, c, st);
     if (rc) return rc;
   }
   int rc = enqueue_update(h, c, st);
   if (rc) return rc;
   h->t = t;
   h->buffers_valid = true;
+  if (patch) {
+    rc = run_kernel(h, kKParamPatch, st, [&] {
+      return launch_param_patch(h->idx(), h->k, h->w, host_out_dev, st);
+    });
+    if (rc) return rc;
+    return scape_refresh_mask(h, stream);
+  }
   // the parameter download overlaps the mask refresh
   e = cudaEventRecord(h->ev_updated, st);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(cp, h->ev_updated, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(dn, h->ev_updated, 0);
   if (e == cudaSuccess)
-    e = cudaMemcpyAsync(host_params_out, h->w, (size_t)h->P * 4, cudaMemcpyDeviceToHost, cp);
-  if (e == cudaSuccess) e = cudaEventRecord(h->ev_done, cp);
+    e = cudaMemcpyAsync(host_params_out, h->w, (size_t)h->P * 4, cudaMemcpyDeviceToHost, dn);
+  if (e == cudaSuccess) e = cudaEventRecord(h->ev_done, dn);
   if (e != cudaSuccess) return cuda_fail(h, e, "scape_step_host: parameter download");
   rc = scape_refresh_mask(h, stream);
   if (rc) return rc;

@@ -50,10 +50,15 @@ struct ShardSel {
   int64_t istar;      // keys == kstar with index <= istar are selected
   uint64_t cprefix;   // composite-key bits fixed so far (candidate select)
   uint32_t guess;     // first-digit bucket of the previous refresh (0xFFFFFFFF: none)
-  uint32_t flags;     // kSelNeedCollect: candidates must be gathered by a second pass
+  uint32_t flags;     // kSelNeedCollect, kSelRemark, kSelNeedHist
+  uint32_t kstar_prev;  // the threshold the speculative bitmap was written with
+  uint32_t pad;
+  int64_t istar_prev;
 };
 constexpr uint32_t kNoGuess = 0xFFFFFFFFu;
-constexpr uint32_t kSelNeedCollect = 1u;
+constexpr uint32_t kSelNeedCollect = 1u;  // the threshold bucket moved: collect again
+constexpr uint32_t kSelRemark = 2u;       // the speculative bitmap of this shard is unusable
+constexpr uint32_t kSelNeedHist = 4u;     // warm refresh missed: count the shard fully
 
 // AdamS constants of one step; all computed on the host in float.
 struct AdamsConst {
@@ -80,6 +85,10 @@ enum KernelId {
   kKAdamW,
   kKEfAdd,
   kKUnionMove,
+  kKSpecMark,
+  kKFixup,
+  kKRemark,
+  kKParamPatch,
   kNumKernels
 };
 static_assert(kNumKernels == SCAPE_NUM_KERNELS, "kernel table size");
@@ -173,6 +182,23 @@ struct MomentPack {
   float beta1, c1;
 };
 
+// Reduction and update carried by a compaction launch.  A launch covers a
+// group of consecutive workers; with kEfAccum it keeps, per selected slot, the
+// worker-ordered sum of the packed values (started from the group's first
+// worker, or with kEfResume from the partial sum left in gbar by the previous
+// group) and stores it back to gbar; with kEfFinish it stores g_bar = sum / W
+// instead (no reduce launch needed), and with kEfUpdate also applies AdamS at
+// the selected coordinates (no adams_sparse launch needed).
+constexpr int kEfAccum = 1, kEfResume = 2, kEfFinish = 4, kEfUpdate = 8;
+struct EfFuse {
+  float* gbar;
+  float* w;
+  float* m;
+  AdamsConst c;
+  int W_total;
+  int flags;
+};
+
 // ---------------------------------------------------------------- launchers
 // Each returns cudaGetLastError() after enqueueing on `st`.
 // moment: step 1 under the first-moment buffer reading.
@@ -182,12 +208,16 @@ cudaError_t launch_dense_step(const WorkerPtrs& p, int W, int64_t P, int dtype, 
 // mp == nullptr: the selected a^w are packed; else b = b1 m + (1 - b1) a^w.
 cudaError_t launch_ef_compact(const WorkerPtrs& p, int W, int64_t P, int dtype, bool vec,
                               const uint32_t* bits, const uint32_t* tile_base, float* pack,
-                              int64_t pack_stride, const MomentPack* mp, cudaStream_t st);
+                              int64_t pack_stride, const MomentPack* mp, const EfFuse& fz,
+                              cudaStream_t st);
 cudaError_t launch_dense_baseline(bool adamw, const WorkerPtrs& p, int W, int64_t P, int dtype,
                                   bool vec, float* w, float* m, float* v, const AdamsConst& c,
                                   cudaStream_t st);
 cudaError_t launch_offmask(const uint32_t* bits, int64_t P, float* w, float* m, const AdamsConst& c,
                            cudaStream_t st);
+// dst[idx[j]] = w[idx[j]], j < k (dst: device address of mapped host memory)
+cudaError_t launch_param_patch(const uint32_t* idx, int64_t k, const float* w, float* dst,
+                               cudaStream_t st);
 cudaError_t launch_reduce(const float* pack, int64_t pack_stride, int W, int64_t k, float* gbar,
                           cudaStream_t st);
 cudaError_t launch_adams_sparse(const uint32_t* idx, const float* gbar, int64_t k, float* w,
@@ -223,11 +253,38 @@ cudaError_t launch_index(const uint32_t* bits, int64_t P, const uint32_t* tile_b
                          uint32_t* idx, int64_t k, cudaStream_t st);
 // candidate-based exact top-k threshold (topk_kernels.cu)
 constexpr int kCandBins0 = 4096;
+// selective: only shards flagged kSelNeedHist, and nothing staged.
 cudaError_t launch_chist0(const float* m, int64_t P, int W, const int64_t* shard_start,
                           const ShardSel* sel, uint32_t* hist, uint2* cand, uint32_t* cand_cnt,
+                          bool selective, cudaStream_t st);
+// Warm refresh: one read of m that writes the bitmap words and popcounts of
+// every whole single-shard tile from the shard's previous threshold (tile_cnt
+// zeroed first), stages the candidates of the previous bucket window and counts
+// the parameters above it (above_cnt zeroed first).
+cudaError_t launch_spec(const float* m, int64_t P, int W, const int64_t* shard_start,
+                        const ShardSel* sel, uint2* cand, uint32_t* cand_cnt, uint32_t* above_cnt,
+                        uint32_t* bits, uint32_t* tile_cnt, cudaStream_t st);
+// Window histogram of the staged candidates with the outside counts lumped.
+cudaError_t launch_whist(int W, int blocks_per_shard, const int64_t* shard_start,
+                         const ShardSel* sel, const uint2* cand, const uint32_t* cand_cnt,
+                         const uint32_t* above_cnt, uint32_t* hist, cudaStream_t st);
+// Flip the candidates whose selection differs between the previous and the new
+// threshold (shards without kSelRemark).
+cudaError_t launch_fixup(const int64_t* shard_start, const ShardSel* sel, const uint2* cand,
+                         const uint32_t* cand_cnt, int W, int blocks_per_shard, uint32_t* bits,
+                         uint32_t* tile_cnt, cudaStream_t st);
+// Mark the tiles the speculative bitmap does not cover: every tile starting in
+// a kSelRemark shard, and each shard's last tile when it crosses the shard end
+// or the end of the vector.
+cudaError_t launch_remark(const float* m, int64_t P, int W, const int64_t* shard_start,
+                          const ShardSel* sel, uint32_t* bits, uint32_t* tile_cnt,
                           cudaStream_t st);
+// form (pass 0): kSelFormCold on a full histogram, kSelFormWarm on the window
+// histogram, kSelFormRerun for the kSelNeedHist shards after their full count.
+constexpr int kSelFormCold = 0, kSelFormWarm = 1, kSelFormRerun = 2;
 cudaError_t launch_cselect(int pass, int W, const int64_t* shard_start, const int64_t* shard_k,
-                           ShardSel* sel, uint32_t* hist, uint32_t* cand_cnt, cudaStream_t st);
+                           ShardSel* sel, uint32_t* hist, uint32_t* cand_cnt, int form,
+                           cudaStream_t st);
 cudaError_t launch_collect(const float* m, int64_t P, int W, const int64_t* shard_start,
                            const ShardSel* sel, uint2* cand, uint32_t* cand_cnt, cudaStream_t st);
 cudaError_t launch_chist(int pass, int W, int blocks_per_shard, const int64_t* shard_start,

@@ -5,8 +5,12 @@
 //   ef_compact   error-feedback add + lagged-mask compaction + residual
 //                ("SCAPE" Sec. II-B: sent = TopK(g + e) through the mask,
 //                e <- g + e - sent), one pass over every worker's g and e.
+//                It can also form the ordered sum of the packed values
+//                (g_bar; the default) and apply AdamS at the selected
+//                coordinates (EfFuse flags).
 //   reduce       ordered sum of the W packed buffers / W: the single
-//                synchronised sparse buffer ("Sintesi Tecnica: SCAPE" Sec. 2).
+//                synchronised sparse buffer ("Sintesi Tecnica: SCAPE" Sec. 2)
+//                (separate-launch form, and the union-mask baseline).
 //   adams_sparse unpack + AdamS ("SCAPE" Sec. II-C, Eq. 2) at the k selected
 //                coordinates, m and v both from that one buffer.
 #include "scape_internal.cuh"
@@ -19,6 +23,19 @@ struct GradIO;
 
 template <>
 struct GradIO<float> {
+  // 8 consecutive gradients as loaded (kept packed until used)
+  struct Raw {
+    float4 a, b;
+  };
+  static __device__ __forceinline__ Raw load_raw(const void* base, int64_t i0) {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + i0);
+    return Raw{__ldcs(p), __ldcs(p + 1)};
+  }
+  static __device__ __forceinline__ float at(const Raw& r, int j) {
+    const float4& v = j < 4 ? r.a : r.b;
+    const int q = j & 3;
+    return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
+  }
   // 8 consecutive gradients starting at a 32-byte multiple of the base.
   static __device__ __forceinline__ void load8(const void* base, int64_t i0, float (&g)[8]) {
     const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + i0);
@@ -33,6 +50,16 @@ struct GradIO<float> {
 
 template <>
 struct GradIO<__nv_bfloat16> {
+  // 8 bfloat16 gradients in four 32-bit words, widened only when used
+  using Raw = uint4;
+  static __device__ __forceinline__ Raw load_raw(const void* base, int64_t i0) {
+    return __ldcs(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + i0));
+  }
+  static __device__ __forceinline__ float at(const Raw& r, int j) {
+    const uint32_t u = (j >> 1) == 0 ? r.x : (j >> 1) == 1 ? r.y : (j >> 1) == 2 ? r.z : r.w;
+    // bfloat16 is the high half of a binary32: widening is exact.
+    return __uint_as_float((j & 1) ? (u & 0xFFFF0000u) : (u << 16));
+  }
   static __device__ __forceinline__ void load8(const void* base, int64_t i0, float (&g)[8]) {
     const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + i0);
     uint4 v = __ldcs(p);
@@ -71,60 +98,117 @@ __device__ __forceinline__ void store8_f32(float* p, const float (&x)[8]) {
 // block-exclusive popcount prefix, computed once and reused for all W workers.
 // Workers whose loads are issued together, and resident blocks per SM (64
 // registers): measured best of {1,2,4} x {2,3,4} on GB300 (6.70 TB/s).
+//
+// Because one block sees every worker of its tile, the synchronised buffer's
+// sum can be formed here, in worker order, while the workers stream through:
+// each selected slot's running sum sits in shared memory (owned by the thread
+// of that slot), and after the last worker the same thread divides by W and
+// writes g_bar, and can apply AdamS to its selected coordinates (EfFuse
+// flags; w and m at those coordinates are fetched into shared memory by
+// cp.async at the block's start).  The packed buffers are still written: they
+// are what each worker sends.
 constexpr int kWorkerUnroll = 2;
 constexpr int kEfMinBlocks = 4;
 
 // With MSYNC (first-moment buffer reading) a selected parameter is sent as
 // b = b1 m_{t-1} + (1 - b1) a instead of a; the residual is the same.
-template <bool MSYNC>
-__device__ __forceinline__ void ef_select8(const float (&g)[8], const float (&e)[8], uint32_t byte,
+// Every selected value is also added to its slot's running sum (started at
+// -0.0, the identity of IEEE addition, so the sum equals the worker-ordered
+// sum that begins with worker 0's value).
+template <bool MSYNC, class G>
+__device__ __forceinline__ void ef_select8(G&& g, const float (&e)[8], uint32_t byte,
                                            float* __restrict__ prow, float (&out)[8],
-                                           const MomentPack& mp, int64_t i0) {
+                                           const MomentPack& mp, int64_t i0, float* ssum) {
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const float a = __fadd_rn(g[j], e[j]);  // error-feedback add
+    const float a = __fadd_rn(g(j), e[j]);  // error-feedback add
     float sent = 0.f;
     if ((byte >> j) & 1u) {
       sent = a;
       float val = a;
-      if (MSYNC) val = __fadd_rn(__fmul_rn(mp.beta1, __ldg(mp.m + i0 + j)), __fmul_rn(mp.c1, a));
-      prow[__popc(byte & ((1u << j) - 1u))] = val;
+      if (MSYNC) val = __fadd_rn(__fmul_rn(mp.beta1, mp.m[i0 + j]), __fmul_rn(mp.c1, a));
+      const int r = __popc(byte & ((1u << j) - 1u));
+      prow[r] = val;
+      ssum[r] = __fadd_rn(ssum[r], val);
     }
     out[j] = __fsub_rn(a, sent);  // residual: g + e - sent
   }
+}
+
+// 4-byte global -> shared copy that completes in the background (cp.async);
+// the issuing thread waits for its own copies with cp_async_wait<n>.
+__device__ __forceinline__ void cp_async4(float* smem, const float* gmem) {
+  const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
 template <typename GT, bool VEC, bool MSYNC>
 __global__ void __launch_bounds__(kTileThreads, kEfMinBlocks)
 ef_compact_kernel(const __grid_constant__ WorkerPtrs ptrs, int W, int64_t P,
                   const uint32_t* __restrict__ bits, const uint32_t* __restrict__ tile_base,
-                  float* __restrict__ pack, int64_t pack_stride, MomentPack mp) {
+                  float* __restrict__ pack, int64_t pack_stride, MomentPack mp, EfFuse fz) {
   __shared__ uint32_t warp_tot[kTileThreads / 32];
+  __shared__ float tile_sum[kTile];
+  __shared__ float tile_w[kTile], tile_m[kTile];  // w, m at the selected slots (finishing launch)
   const int64_t tile = blockIdx.x;
   const int64_t i0 = tile * kTile + (int64_t)threadIdx.x * 8;
   uint32_t byte = 0;
   if (i0 < P) byte = (__ldg(bits + (i0 >> 5)) >> (uint32_t)(i0 & 31)) & 0xFFu;
   uint32_t total;
   const uint32_t excl = block_exclusive_scan<kTileThreads>(__popc(byte), warp_tot, &total);
-  float* const pbase = pack + (int64_t)__ldg(tile_base + tile) + excl;
+  const int64_t slot0 = (int64_t)__ldg(tile_base + tile) + excl;
+  float* const pbase = pack + slot0;
+  // this thread's selected slots: tile_sum[excl .. excl + popc(byte))
+  float* const ssum = tile_sum + excl;
+  // Background copies, so that no load of the update waits at the block's end:
+  // group 0 the partial sums of the previous worker group, group 1 w and m at
+  // this thread's selected coordinates.
+  if ((fz.flags & (kEfAccum | kEfResume)) == (kEfAccum | kEfResume)) {
+    for (int r = 0; r < __popc(byte); ++r) cp_async4(ssum + r, fz.gbar + slot0 + r);
+  } else {
+    for (int r = 0; r < __popc(byte); ++r) ssum[r] = -0.0f;
+  }
+  cp_async_commit();
+  if ((fz.flags & (kEfAccum | kEfFinish | kEfUpdate)) == (kEfAccum | kEfFinish | kEfUpdate)) {
+    uint32_t rest = byte;
+    for (int r = 0; rest != 0u; ++r, rest &= rest - 1u) {
+      const int64_t i = i0 + (__ffs(rest) - 1);
+      cp_async4(tile_w + excl + r, fz.w + i);
+      cp_async4(tile_m + excl + r, fz.m + i);
+    }
+  }
+  cp_async_commit();
+  cp_async_wait<1>();  // the partial sums have landed
 
   if (VEC && (tile + 1) * kTile <= P) {
     // full tile: 16-byte loads and stores; the loads of a worker pair are
     // issued before either pair member is stored
-    for (int w0 = 0; w0 < W; w0 += kWorkerUnroll) {
-      float g[kWorkerUnroll][8], e[kWorkerUnroll][8];
+    // float32 gradients: one worker in flight (two would spill at 64 registers)
+    constexpr int U = sizeof(GT) == 2 ? kWorkerUnroll : 1;
+    for (int w0 = 0; w0 < W; w0 += U) {
+      typename GradIO<GT>::Raw g[U];
+      float e[U][8];
 #pragma unroll
-      for (int u = 0; u < kWorkerUnroll; ++u) {
+      for (int u = 0; u < U; ++u) {
         if (w0 + u < W) {
-          GradIO<GT>::load8(ptrs.g[w0 + u], i0, g[u]);
+          g[u] = GradIO<GT>::load_raw(ptrs.g[w0 + u], i0);
           load8_f32(ptrs.e[w0 + u] + i0, e[u]);
         }
       }
 #pragma unroll
-      for (int u = 0; u < kWorkerUnroll; ++u) {
+      for (int u = 0; u < U; ++u) {
         if (w0 + u < W) {
           float out[8];
-          ef_select8<MSYNC>(g[u], e[u], byte, pbase + (int64_t)(w0 + u) * pack_stride, out, mp, i0);
+          const auto& gu = g[u];
+          ef_select8<MSYNC>([&](int j) { return GradIO<GT>::at(gu, j); }, e[u], byte,
+                            pbase + (int64_t)(w0 + u) * pack_stride, out, mp, i0, ssum);
           store8_f32(ptrs.e[w0 + u] + i0, out);
         }
       }
@@ -139,11 +223,36 @@ ef_compact_kernel(const __grid_constant__ WorkerPtrs ptrs, int W, int64_t P,
         g[j] = in ? GradIO<GT>::load1(ptrs.g[wk], i0 + j) : 0.f;
         e[j] = in ? __ldcs(ptrs.e[wk] + i0 + j) : 0.f;
       }
-      ef_select8<MSYNC>(g, e, byte, pbase + (int64_t)wk * pack_stride, out, mp, i0);
+      ef_select8<MSYNC>([&](int j) { return g[j]; }, e, byte, pbase + (int64_t)wk * pack_stride,
+                        out, mp, i0, ssum);
 #pragma unroll
       for (int j = 0; j < 8; ++j)
         if (i0 + j < P) __stcs(ptrs.e[wk] + i0 + j, out[j]);
     }
+  }
+  if (!(fz.flags & kEfAccum)) return;
+  // g_bar = (((p_0 + p_1) + ...) + p_{W-1}) / W and AdamS at each selected
+  // coordinate ("SCAPE" Sec. II-C, Eq. 2); or the partial sum for the next group
+  if (!(fz.flags & kEfFinish)) {
+    for (int r = 0; r < __popc(byte); ++r) fz.gbar[slot0 + r] = ssum[r];
+    return;
+  }
+  const float fw = (float)fz.W_total;
+  if (!(fz.flags & kEfUpdate)) {
+    for (int r = 0; r < __popc(byte); ++r) fz.gbar[slot0 + r] = __fdiv_rn(ssum[r], fw);
+    return;
+  }
+  cp_async_wait<0>();
+  uint32_t rest = byte;
+  for (int r = 0; rest != 0u; ++r, rest &= rest - 1u) {
+    const float gm = __fdiv_rn(ssum[r], fw);
+    fz.gbar[slot0 + r] = gm;
+    float wv = tile_w[(ssum - tile_sum) + r], mv = tile_m[(ssum - tile_sum) + r];
+    if (MSYNC) adams_update_from_moment(gm, wv, mv, fz.c);
+    else adams_update(gm, wv, mv, fz.c);
+    const int64_t i = i0 + (__ffs(rest) - 1);
+    fz.w[i] = wv;
+    fz.m[i] = mv;
   }
 }
 
@@ -309,6 +418,19 @@ adams_sparse_kernel(const uint32_t* __restrict__ idx, const float* __restrict__ 
   }
 }
 
+// ------------------------------------------------------------------ param_patch
+// dst[idx[j]] = w[idx[j]] for the k coordinates a step changed; dst is the
+// device address of the caller's page-locked host copy of the parameters,
+// whose other coordinates already hold the (unchanged) previous values.
+__global__ void __launch_bounds__(256)
+param_patch_kernel(const uint32_t* __restrict__ idx, int64_t k, const float* __restrict__ w,
+                   float* __restrict__ dst) {
+  const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= k) return;
+  const uint32_t i = __ldg(idx + j);
+  dst[i] = __ldg(w + i);
+}
+
 template <typename GT, int KIND>
 void dense_kind(const WorkerPtrs& p, int W, int64_t P, bool vec, float* w, float* m, float* v,
                 const AdamsConst& c, cudaStream_t st) {
@@ -321,14 +443,14 @@ void dense_kind(const WorkerPtrs& p, int W, int64_t P, bool vec, float* w, float
 template <typename GT, bool MSYNC>
 void compact_kind(const WorkerPtrs& p, int W, int64_t P, bool vec, const uint32_t* bits,
                   const uint32_t* tile_base, float* pack, int64_t pack_stride,
-                  const MomentPack& mp, cudaStream_t st) {
+                  const MomentPack& mp, const EfFuse& fz, cudaStream_t st) {
   const unsigned grid = (unsigned)((P + kTile - 1) / kTile);
   if (vec)
     ef_compact_kernel<GT, true, MSYNC>
-        <<<grid, kTileThreads, 0, st>>>(p, W, P, bits, tile_base, pack, pack_stride, mp);
+        <<<grid, kTileThreads, 0, st>>>(p, W, P, bits, tile_base, pack, pack_stride, mp, fz);
   else
     ef_compact_kernel<GT, false, MSYNC>
-        <<<grid, kTileThreads, 0, st>>>(p, W, P, bits, tile_base, pack, pack_stride, mp);
+        <<<grid, kTileThreads, 0, st>>>(p, W, P, bits, tile_base, pack, pack_stride, mp, fz);
 }
 
 }  // namespace
@@ -362,14 +484,15 @@ cudaError_t launch_dense_baseline(bool adamw, const WorkerPtrs& p, int W, int64_
 
 cudaError_t launch_ef_compact(const WorkerPtrs& p, int W, int64_t P, int dtype, bool vec,
                               const uint32_t* bits, const uint32_t* tile_base, float* pack,
-                              int64_t pack_stride, const MomentPack* mp, cudaStream_t st) {
+                              int64_t pack_stride, const MomentPack* mp, const EfFuse& fz,
+                              cudaStream_t st) {
   const MomentPack none{nullptr, 0.f, 0.f};
   if (dtype == SCAPE_BF16) {
-    if (mp) compact_kind<__nv_bfloat16, true>(p, W, P, vec, bits, tile_base, pack, pack_stride, *mp, st);
-    else compact_kind<__nv_bfloat16, false>(p, W, P, vec, bits, tile_base, pack, pack_stride, none, st);
+    if (mp) compact_kind<__nv_bfloat16, true>(p, W, P, vec, bits, tile_base, pack, pack_stride, *mp, fz, st);
+    else compact_kind<__nv_bfloat16, false>(p, W, P, vec, bits, tile_base, pack, pack_stride, none, fz, st);
   } else {
-    if (mp) compact_kind<float, true>(p, W, P, vec, bits, tile_base, pack, pack_stride, *mp, st);
-    else compact_kind<float, false>(p, W, P, vec, bits, tile_base, pack, pack_stride, none, st);
+    if (mp) compact_kind<float, true>(p, W, P, vec, bits, tile_base, pack, pack_stride, *mp, fz, st);
+    else compact_kind<float, false>(p, W, P, vec, bits, tile_base, pack, pack_stride, none, fz, st);
   }
   return cudaGetLastError();
 }
@@ -388,6 +511,13 @@ cudaError_t launch_adams_sparse(const uint32_t* idx, const float* gbar, int64_t 
   const unsigned grid = (unsigned)(((k + 3) / 4 + 255) / 256);
   if (msync) adams_sparse_kernel<true><<<grid, 256, 0, st>>>(idx, gbar, k, w, m, c);
   else adams_sparse_kernel<false><<<grid, 256, 0, st>>>(idx, gbar, k, w, m, c);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_param_patch(const uint32_t* idx, int64_t k, const float* w, float* dst,
+                               cudaStream_t st) {
+  if (k <= 0) return cudaSuccess;
+  param_patch_kernel<<<(unsigned)((k + 255) / 256), 256, 0, st>>>(idx, k, w, dst);
   return cudaGetLastError();
 }
 

@@ -8,6 +8,7 @@
 // which is distinct for every parameter, so the k_s-th largest composite of a
 // shard fixes the selection exactly: i is selected iff comp(i) >= kstar64.
 //
+// Cold refresh (no usable previous threshold):
 //   chist0    one read of m: per-shard histogram of composite bits 62..51
 //             (the top 12 bits of |m|); stages candidates near last step's
 //             bucket
@@ -16,8 +17,16 @@
 //             index) of every parameter in that bucket
 //   chist/cselect 1..5   radix passes over the candidates only, digits
 //             50..40, 39..29, 28..18, 17..7, 6..0 of the composite key
-// The result is written as (kstar, istar) into the shard's ShardSel for the
-// mark kernel: bit_i = key_i > kstar || (key_i == kstar && i <= istar).
+//   then the mark kernel writes the bitmap from (kstar, istar):
+//             bit_i = key_i > kstar || (key_i == kstar && i <= istar).
+// Warm refresh (every later one): the one read of m (spec) writes the bitmap
+// from the previous threshold while staging the candidates of its bucket
+// window and counting the parameters above it; whist + cselect0 place the new
+// threshold's bucket; shards whose bucket left the window are counted fully
+// (chist0 selective, cselect0 rerun) and collected; the radix passes run as
+// above; fixup flips the candidates between the old and the new threshold,
+// and the remark kernel re-marks the tiles the speculative bitmap could not
+// cover (shard-boundary tiles, the ragged end, shards that missed).
 #include "scape_internal.cuh"
 
 namespace scapek {
@@ -30,27 +39,32 @@ __device__ __forceinline__ uint64_t composite(uint32_t key, uint32_t i) {
 }
 
 // ------------------------------------------------------------------ passes over m
-// One kernel for both reads of m.  Blocks are persistent: block b walks a
-// contiguous run of 2048-parameter segments, following the shard boundaries
-// incrementally, so it meets at most a few of them.  Per shard piece it
+// mpass: the histogram and collect reads of m.  Blocks are persistent: block b
+// walks a contiguous run of 2048-parameter segments (the mark tiles),
+// following the shard boundaries incrementally, so it meets at most a few of
+// them.  Per shard piece it
 //   HIST:    adds the 12-bit first digit of every key to a shared-memory
 //            histogram (flushed to the shard's row when the shard changes), and
 //            stages candidates whose digit lies within one bucket of the
-//            previous refresh's bucket (`guess`): the mask is stable from step
-//            to step, so that bucket usually still holds the threshold;
-//   COLLECT: (second pass, only for shards whose guess missed) stages every
+//            previous refresh's bucket (`guess`).  `selective`: only shards
+//            flagged kSelNeedHist, nothing staged;
+//   COLLECT: (only for shards whose threshold bucket moved) stages every
 //            parameter whose digit equals the bucket just selected.
 // Each warp stages its candidates in a private shared-memory buffer (ballot
 // append) and flushes it to the shard's range of `cand` with one global
 // atomic, so segments need no block-wide barrier.
 constexpr int kMSeg = 2048;       // parameters per segment (256 threads x 2 x float4)
 constexpr int kWarpStage = 384;   // staged candidates per warp
+constexpr int kMHist = 0, kMCollect = 1;
+static_assert(kMSeg == kTile, "a segment is one mark tile");
 
-template <bool HIST>
+template <int MODE>
 __global__ void __launch_bounds__(256)
 mpass_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __restrict__ shard_start,
              const ShardSel* __restrict__ sel, uint32_t* __restrict__ hist,
-             uint2* __restrict__ cand, uint32_t* __restrict__ cand_cnt, int64_t segs_per_block) {
+             uint2* __restrict__ cand, uint32_t* __restrict__ cand_cnt, int64_t segs_per_block,
+             int selective) {
+  constexpr bool HIST = MODE == kMHist;
   __shared__ uint32_t sh[HIST ? kCBins0 : 1];
   __shared__ uint2 wbuf[8][kWarpStage];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -60,11 +74,14 @@ mpass_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __res
   if (g0 >= g1) return;
   const int64_t r0 = g0 * kMSeg, r1 = min(g1 * kMSeg, P);
   int s = shard_of(r0, P, W);
-  if (!HIST) {
-    // nothing to do unless a shard of this block's range must be collected
+  // shards this mode works on
+  auto wanted = [&](const ShardSel& q) -> bool {
+    if (!HIST) return q.mode == kSelSearch && (q.flags & kSelNeedCollect);
+    return !selective || (q.flags & kSelNeedHist);
+  };
+  if (!HIST || selective) {
     bool any = false;
-    for (int q = s; q < W && __ldg(shard_start + q) < r1; ++q)
-      any |= sel[q].mode == kSelSearch && (sel[q].flags & kSelNeedCollect);
+    for (int q = s; q < W && __ldg(shard_start + q) < r1; ++q) any |= wanted(sel[q]);
     if (!any) return;
   }
   if (HIST) {
@@ -114,18 +131,14 @@ mpass_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __res
         }
         cur = s;
         const ShardSel ss = sel[s];
-        if (HIST) {
-          active = true;
-          wlo = 0xFFFFFFFFu;
-          wwid = 0;
-          if (ss.guess != kNoGuess) {
-            wlo = ss.guess > 0 ? ss.guess - 1 : 0;
-            wwid = ss.guess + 1 - wlo;
-          }
-        } else {
-          active = ss.mode == kSelSearch && (ss.flags & kSelNeedCollect);
+        active = wanted(ss);
+        wlo = 0xFFFFFFFFu;
+        wwid = 0;
+        if (!HIST) {
           wlo = (uint32_t)ss.cprefix;
-          wwid = 0;
+        } else if (ss.guess != kNoGuess && !selective) {
+          wlo = ss.guess > 0 ? ss.guess - 1 : 0;
+          wwid = ss.guess + 1 - wlo;
         }
       }
       const int64_t lo = max(seg0, __ldg(shard_start + s)), hi = min(seg1, s_hi);
@@ -188,14 +201,270 @@ mpass_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __res
   }
 }
 
+// ------------------------------------------------------------------ spec
+// Warm refresh: the one read of m, for shards that have a previous threshold
+// (kstar, istar) and bucket `guess`.  Blocks are persistent over a contiguous
+// run of 2048-parameter tiles; each shard piece of the run is split into its
+// whole tiles and at most two partial pieces.
+//  * Whole tiles get their bitmap words and popcount from the previous
+//    threshold.  Lane l of warp w holds parameters 1024h + 128w + 32q + l of
+//    the tile (h = 0..1, q = 0..3; coalesced 4-byte loads at fixed offsets
+//    from one pointer), so the ballot of "selected" for (h, q) is bitmap word
+//    32h + 4w + q and lane 0 stores a warp's four words with one 16-byte store.
+//    The next tile's values are loaded while the current one is processed.
+//  * Candidates whose bucket is within one of `guess` are staged as in mpass.
+//  * above_cnt[s] gets the popcount of those tiles plus the number of
+//    parameters above the window in the partial pieces.  Parameters above the
+//    window are all selected by the previous threshold, so whist recovers the
+//    count above the window by subtracting the staged candidates that the
+//    previous threshold selected in whole tiles.
+// Partial pieces (shard boundaries inside a tile, the ragged end) are only
+// staged and counted; the remark kernel writes their bits.
+constexpr int kSpecBlocksPerSm = 4;
+
+__global__ void __launch_bounds__(256, kSpecBlocksPerSm)
+spec_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __restrict__ shard_start,
+            const ShardSel* __restrict__ sel, uint2* __restrict__ cand,
+            uint32_t* __restrict__ cand_cnt, uint32_t* __restrict__ above_cnt,
+            uint32_t* __restrict__ bits, uint32_t* __restrict__ tile_cnt, int64_t segs_per_block) {
+  __shared__ uint2 wbuf[8][kWarpStage];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t nseg = (P + kMSeg - 1) / kMSeg;
+  const int64_t g0 = (int64_t)blockIdx.x * segs_per_block;
+  const int64_t g1 = min(g0 + segs_per_block, nseg);
+  if (g0 >= g1) return;
+  // P < 2^31: every index below fits 32 bits
+  const uint32_t r0 = (uint32_t)(g0 * kMSeg), r1 = (uint32_t)min(g1 * kMSeg, P);
+  int s = shard_of(r0, P, W);
+  {
+    bool any = false;
+    for (int q = s; q < W && (uint32_t)__ldg(shard_start + q) < r1; ++q)
+      any |= sel[q].guess != kNoGuess;
+    if (!any) return;
+  }
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  uint2* const mybuf = wbuf[warp];
+  uint32_t wn = 0;  // entries in this warp's buffer (same value in every lane)
+
+  auto flush_warp = [&](int shard) {
+    if (wn == 0) return;
+    __syncwarp();
+    uint32_t base = 0;
+    if (lane == 0) base = atomicAdd(cand_cnt + shard, wn);
+    base = __shfl_sync(0xffffffffu, base, 0);
+    uint2* out = cand + __ldg(shard_start + shard) + base;
+    for (uint32_t j = lane; j < wn; j += 32) out[j] = mybuf[j];
+    __syncwarp();
+    wn = 0;
+  };
+
+  uint32_t pos = r0;
+  while (pos < r1) {
+    while (s < W - 1 && (uint32_t)__ldg(shard_start + s + 1) <= pos) ++s;
+    const uint32_t end = min((uint32_t)__ldg(shard_start + s + 1), r1);
+    const ShardSel ss = sel[s];
+    if (ss.guess != kNoGuess) {
+      const uint32_t wlo = ss.guess > 0 ? ss.guess - 1 : 0;
+      const uint32_t wkey_lo = wlo << 19;                   // window: key - wkey_lo < wkey_n
+      const uint32_t wkey_n = (ss.guess + 2 - wlo) << 19;
+      const uint32_t top_key = (ss.guess + 2) << 19;        // keys >= top_key: above it
+      const uint32_t kstar = ss.kstar;
+      const uint32_t istar = (uint32_t)ss.istar;
+      uint32_t acount = 0;  // this thread's share of above_cnt[s]
+
+      // partial piece [a, b): stage and count, 256 parameters per round
+      auto piece = [&](uint32_t a, uint32_t b) {
+        for (uint32_t b0 = a; b0 < b; b0 += 256) {
+          const uint32_t i = b0 + threadIdx.x;
+          const bool in = i < b;
+          const uint32_t key = in ? magnitude_key(__ldcs(m + i)) : 0u;
+          acount += (in && key >= top_key) ? 1u : 0u;
+          const bool hit = in && key - wkey_lo < wkey_n;
+          const uint32_t ball = __ballot_sync(0xffffffffu, hit);
+          if (ball) {
+            if (hit) mybuf[wn + __popc(ball & lt_mask)] = make_uint2(key, i);
+            wn += __popc(ball);
+            if (wn > kWarpStage - 32) flush_warp(s);
+          }
+        }
+      };
+
+      const uint32_t ta = (pos + kMSeg - 1) / kMSeg, tb = end / kMSeg;  // whole tiles [ta, tb)
+      if (ta >= tb) {
+        piece(pos, end);
+      } else {
+        piece(pos, ta * kMSeg);
+        if (wn > kWarpStage - 256) flush_warp(s);  // a tile adds at most 256 per warp
+        const uint32_t t_is = istar / kMSeg;  // the tile holding istar
+        const int lim = (int)(istar - t_is * kMSeg);
+        const float* p = m + (size_t)ta * kMSeg + 128 * warp + lane;
+        uint32_t* bw = bits + (size_t)ta * (kMSeg / 32) + 4 * warp;
+        float xc[8], xn[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) xc[j] = __ldcs(p + 1024 * (j >> 2) + 32 * (j & 3));
+        for (uint32_t t = ta; t < tb; ++t) {
+          if (t + 1 < tb) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) xn[j] = __ldcs(p + kMSeg + 1024 * (j >> 2) + 32 * (j & 3));
+          }
+          // selected: key > kstar, or key == kstar and i <= istar
+          const uint32_t thr = kstar + (t > t_is ? 1u : 0u);
+          const bool mixed = t == t_is;
+          const uint32_t ibase = t * kMSeg + 128 * warp + lane;
+          uint32_t tc = 0;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t key[4], wd[4], hb[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) key[q] = magnitude_key(xc[4 * h + q]);
+            if (!mixed) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) wd[q] = __ballot_sync(0xffffffffu, key[q] >= thr);
+            } else {
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                wd[q] = __ballot_sync(
+                    0xffffffffu,
+                    key[q] >= kstar + (uint32_t)(1024 * h + 128 * warp + 32 * q + lane > lim));
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              hb[q] = __ballot_sync(0xffffffffu, key[q] - wkey_lo < wkey_n);
+            if ((hb[0] | hb[1] | hb[2] | hb[3]) != 0u) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                if ((hb[q] >> lane) & 1u)
+                  mybuf[wn + __popc(hb[q] & lt_mask)] =
+                      make_uint2(key[q], ibase + 1024 * h + 32 * q);
+                wn += __popc(hb[q]);
+              }
+            }
+            if (lane == 0) {
+              *reinterpret_cast<uint4*>(bw + 32 * h) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+              tc += __popc(wd[0]) + __popc(wd[1]) + __popc(wd[2]) + __popc(wd[3]);
+            }
+          }
+          if (lane == 0 && tc) {
+            atomicAdd(tile_cnt + t, tc);
+            acount += tc;
+          }
+          if (wn > kWarpStage - 256) flush_warp(s);
+          p += kMSeg;
+          bw += kMSeg / 32;
+          if (t + 1 < tb) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) xc[j] = xn[j];
+          }
+        }
+        piece(tb * kMSeg, end);
+      }
+      flush_warp(s);
+      const uint32_t a = __reduce_add_sync(0xffffffffu, acount);
+      if (lane == 0 && a) atomicAdd(above_cnt + s, a);
+    }
+    pos = end;
+  }
+}
+
+// ------------------------------------------------------------------ whist
+// Warm refresh, grid (G, W): the first-digit histogram of shard s from its
+// staged window candidates, with the parameters above and below the window
+// lumped into the two bins next to it.  cselect pass 0 then finds the
+// threshold bucket as on a full histogram; a lumped bin means a miss.
+//   above = above_cnt[s] - (staged candidates the previous threshold selected
+//           inside whole single-shard tiles)
+//   below = n - staged - above
+// Blocks add their parts with atomics; the sums are final when cselect runs.
+__global__ void __launch_bounds__(256)
+whist_kernel(const int64_t* __restrict__ shard_start, const ShardSel* __restrict__ sel,
+             const uint2* __restrict__ cand, const uint32_t* __restrict__ cand_cnt,
+             const uint32_t* __restrict__ above_cnt, uint32_t* __restrict__ hist) {
+  __shared__ uint32_t sh[4];  // three window bins, then the selected count
+  const int s = blockIdx.y;
+  const ShardSel ss = sel[s];
+  const uint32_t guess = ss.guess;
+  if (guess == kNoGuess) return;
+  const uint32_t wlo = guess > 0 ? guess - 1 : 0;
+  const uint64_t k_old = composite(ss.kstar, (uint32_t)ss.istar);
+  const int64_t s_lo = shard_start[s], s_hi = shard_start[s + 1];
+  if (threadIdx.x < 4) sh[threadIdx.x] = 0;
+  __syncthreads();
+  const uint32_t cnt = cand_cnt[s];
+  const uint2* c = cand + s_lo;
+  for (uint32_t j = blockIdx.x * blockDim.x + threadIdx.x; j < cnt; j += gridDim.x * blockDim.x) {
+    const uint2 v = __ldg(c + j);
+    const uint32_t b = (v.x >> 19) - wlo;  // in [0, 3) for staged candidates
+    if (b < 3u) atomicAdd(&sh[b], 1u);
+    const int64_t t0 = (int64_t)(v.y / kTile) * kTile;
+    if (composite(v.x, v.y) >= k_old && t0 >= s_lo && t0 + kTile <= s_hi) atomicAdd(&sh[3], 1u);
+  }
+  __syncthreads();
+  uint32_t* row = hist + (int64_t)s * kCBins0;
+  if (threadIdx.x < 3 && sh[threadIdx.x]) atomicAdd(row + wlo + threadIdx.x, sh[threadIdx.x]);
+  if (threadIdx.x == 0) {
+    // digits above guess + 1 exist only if guess + 2 <= 4095; below wlo only if guess >= 2
+    const uint32_t a = blockIdx.x == 0 ? above_cnt[s] : 0u;
+    const uint32_t n = (uint32_t)(s_hi - s_lo);
+    if (guess + 2 < (uint32_t)kCBins0) {
+      const uint32_t v = a - sh[3];
+      if (v) atomicAdd(row + guess + 2, v);
+    }
+    if (guess >= 2) {
+      const uint32_t v = (blockIdx.x == 0 ? n - cnt - a : 0u) + sh[3];
+      if (v) atomicAdd(row + guess - 2, v);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ fixup
+// Warm refresh, grid (G, W), shards that hit (no kSelRemark): the speculative
+// bitmap selected comp >= K_old, the answer is comp >= K_new; the parameters
+// whose bit differs have composites in [min, max) of the two, and their
+// digits lie between the two thresholds' buckets, inside the staged window.
+// Flip them (only in the whole single-shard tiles the speculative pass wrote)
+// and move the tile popcounts by one each.
+__global__ void __launch_bounds__(256)
+fixup_kernel(const int64_t* __restrict__ shard_start, const ShardSel* __restrict__ sel,
+             const uint2* __restrict__ cand, const uint32_t* __restrict__ cand_cnt,
+             uint32_t* __restrict__ bits, uint32_t* __restrict__ tile_cnt) {
+  const int s = blockIdx.y;
+  const ShardSel ss = sel[s];
+  if (ss.mode != kSelDone || (ss.flags & kSelRemark)) return;
+  const uint64_t k_old = composite(ss.kstar_prev, (uint32_t)ss.istar_prev);
+  const uint64_t k_new = composite(ss.kstar, (uint32_t)ss.istar);
+  if (k_old == k_new) return;
+  const uint64_t lo = k_old < k_new ? k_old : k_new, hi = k_old < k_new ? k_new : k_old;
+  const uint32_t gain = k_new < k_old ? 1u : 0xFFFFFFFFu;  // +1 or -1 per flipped bit
+  const int64_t s_lo = shard_start[s], s_hi = shard_start[s + 1];
+  const uint32_t cnt = cand_cnt[s];
+  const uint2* c = cand + s_lo;
+  for (uint32_t j = blockIdx.x * blockDim.x + threadIdx.x; j < cnt; j += gridDim.x * blockDim.x) {
+    const uint2 v = __ldg(c + j);
+    const uint64_t comp = composite(v.x, v.y);
+    if (comp < lo || comp >= hi) continue;
+    const int64_t t0 = (int64_t)(v.y / kTile) * kTile;
+    if (t0 < s_lo || t0 + kTile > s_hi) continue;  // re-marked whole instead
+    atomicXor(bits + (v.y >> 5), 1u << (v.y & 31));
+    atomicAdd(tile_cnt + v.y / kTile, gain);
+  }
+}
+
 // ------------------------------------------------------------------ cselect
 // One block per shard: find the digit of the pass holding the krem-th largest
 // composite among those matching the prefix, narrow the prefix, clear the row.
+// Pass 0 runs in one of three forms (`form`):
+//   kSelFormCold   on a full histogram; a bucket outside the staged window needs a
+//              collect pass;
+//   kSelFormWarm   on the window histogram (whist); no guess, or a lumped bin,
+//              needs a full histogram of the shard first (kSelNeedHist), and
+//              its speculative bitmap is unusable (kSelRemark);
+//   kSelFormRerun  only kSelNeedHist shards, on their full histogram.
+
 template <int PASS>
 __global__ void __launch_bounds__(256)
 cselect_kernel(const int64_t* __restrict__ shard_start, const int64_t* __restrict__ shard_k,
                ShardSel* __restrict__ sel, uint32_t* __restrict__ hist,
-               uint32_t* __restrict__ cand_cnt) {
+               uint32_t* __restrict__ cand_cnt, int form) {
   constexpr int WID = PASS == 0 ? 12 : (PASS == 5 ? 7 : 11);
   constexpr int NB = 1 << WID;
   constexpr int PER = NB >= 256 ? NB / 256 : 1;
@@ -204,9 +473,16 @@ cselect_kernel(const int64_t* __restrict__ shard_start, const int64_t* __restric
   const int s = blockIdx.x;
   uint32_t* row = hist + (int64_t)s * kCBins0;
   const int64_t s_lo = shard_start[s], s_hi = shard_start[s + 1];
-  ShardSel st;
+  ShardSel st = sel[s];
+  __syncthreads();  // every thread has read sel[s] before thread 0 rewrites it
   if (PASS == 0) {
+    if (form == kSelFormRerun && !(st.flags & kSelNeedHist)) return;
     const int64_t n = s_hi - s_lo, k = shard_k[s];
+    if (form != kSelFormRerun) {
+      // the threshold the speculative bitmap was written with
+      st.kstar_prev = st.kstar;
+      st.istar_prev = st.istar;
+    }
     st.prefix = 0;
     st.krem = (uint32_t)k;
     st.kstar = 0;
@@ -214,16 +490,26 @@ cselect_kernel(const int64_t* __restrict__ shard_start, const int64_t* __restric
     st.count_eq = 0;
     st.istar = s_hi - 1;
     st.cprefix = 0;
-    st.guess = sel[s].guess;
     st.flags = 0;
-    if (n <= 0 || k <= 0) st.mode = kSelEmpty;
-    else if (k >= n) st.mode = kSelDone;  // every key selected: kstar = 0, istar = last
-    else st.mode = kSelSearch;
-  } else {
-    st = sel[s];
+    if (n <= 0 || k <= 0) {
+      st.mode = kSelEmpty;
+    } else if (k >= n) {
+      st.mode = kSelDone;  // every key selected: kstar = 0, istar = last
+      st.flags = kSelRemark;
+    } else {
+      st.mode = kSelSearch;
+      if (form == kSelFormWarm && st.guess == kNoGuess) {
+        // nothing was counted for this shard: full histogram first
+        if (threadIdx.x == 0) {
+          st.flags = kSelNeedHist | kSelNeedCollect | kSelRemark;
+          cand_cnt[s] = 0;
+          sel[s] = st;
+        }
+        return;
+      }
+    }
   }
   if (st.mode != kSelSearch) {
-    __syncthreads();  // every thread has read sel[s] before thread 0 rewrites it
     if (threadIdx.x == 0 && PASS == 0) sel[s] = st;
     for (int b = threadIdx.x; b < kCBins0; b += blockDim.x) row[b] = 0;
     return;
@@ -258,17 +544,24 @@ cselect_kernel(const int64_t* __restrict__ shard_start, const int64_t* __restric
   __syncthreads();
   for (int b = threadIdx.x; b < kCBins0; b += blockDim.x) row[b] = 0;
   if (threadIdx.x == 0) {
-    st.cprefix = (st.cprefix << WID) | sh_digit;
-    st.krem -= sh_above;
     if (PASS == 0) {
-      // candidates were staged during the histogram pass for buckets within
-      // one of the previous refresh's; otherwise a collect pass gathers them
-      const bool hit = st.guess != kNoGuess && sh_digit + 1 >= st.guess && sh_digit <= st.guess + 1;
+      // candidates were staged for buckets within one of the previous
+      // refresh's; otherwise a collect pass gathers them
+      const bool hit = form != kSelFormRerun && st.guess != kNoGuess && sh_digit + 1 >= st.guess &&
+                       sh_digit <= st.guess + 1;
       if (!hit) {
         cand_cnt[s] = 0;
-        st.flags = kSelNeedCollect;
+        if (form == kSelFormWarm) {
+          // a lumped bin: the counts are not a histogram; count the shard fully
+          st.flags = kSelNeedHist | kSelNeedCollect | kSelRemark;
+          sel[s] = st;
+          return;
+        }
+        st.flags = kSelNeedCollect | (form == kSelFormRerun ? kSelRemark : 0u);
       }
     }
+    st.cprefix = (st.cprefix << WID) | sh_digit;
+    st.krem -= sh_above;
     if (PASS == 5) {
       // the composite of the k_s-th largest parameter of the shard
       st.guess = (uint32_t)(st.cprefix >> 51);
@@ -312,7 +605,7 @@ chist_kernel(const int64_t* __restrict__ shard_start, const ShardSel* __restrict
   }
 }
 
-int mpass_grid(int64_t P, int64_t* segs_per_block) {
+int mpass_grid(int64_t P, int blocks_per_sm, int64_t* segs_per_block) {
   static int sms = 0;
   if (sms == 0) {
     int dev = 0, n = 0;
@@ -323,7 +616,7 @@ int mpass_grid(int64_t P, int64_t* segs_per_block) {
       sms = 148;
   }
   const int64_t nseg = (P + kMSeg - 1) / kMSeg;
-  const int64_t want = (int64_t)sms * 5;  // ~40 KB of shared memory per block: 5 per SM
+  const int64_t want = (int64_t)sms * blocks_per_sm;
   const int64_t grid = nseg < want ? nseg : want;
   *segs_per_block = (nseg + grid - 1) / grid;
   return (int)((nseg + *segs_per_block - 1) / *segs_per_block);
@@ -334,31 +627,59 @@ int mpass_grid(int64_t P, int64_t* segs_per_block) {
 // ------------------------------------------------------------------ launchers
 cudaError_t launch_chist0(const float* m, int64_t P, int W, const int64_t* shard_start,
                           const ShardSel* sel, uint32_t* hist, uint2* cand, uint32_t* cand_cnt,
-                          cudaStream_t st) {
+                          bool selective, cudaStream_t st) {
   int64_t spb = 1;
-  const int grid = mpass_grid(P, &spb);
-  mpass_kernel<true><<<grid, 256, 0, st>>>(m, P, W, shard_start, sel, hist, cand, cand_cnt, spb);
+  const int grid = mpass_grid(P, 5, &spb);
+  mpass_kernel<kMHist><<<grid, 256, 0, st>>>(m, P, W, shard_start, sel, hist, cand, cand_cnt, spb,
+                                             selective ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_spec(const float* m, int64_t P, int W, const int64_t* shard_start,
+                        const ShardSel* sel, uint2* cand, uint32_t* cand_cnt, uint32_t* above_cnt,
+                        uint32_t* bits, uint32_t* tile_cnt, cudaStream_t st) {
+  int64_t spb = 1;
+  const int grid = mpass_grid(P, kSpecBlocksPerSm, &spb);
+  spec_kernel<<<grid, 256, 0, st>>>(m, P, W, shard_start, sel, cand, cand_cnt, above_cnt, bits,
+                                    tile_cnt, spb);
   return cudaGetLastError();
 }
 
 cudaError_t launch_collect(const float* m, int64_t P, int W, const int64_t* shard_start,
                            const ShardSel* sel, uint2* cand, uint32_t* cand_cnt, cudaStream_t st) {
   int64_t spb = 1;
-  const int grid = mpass_grid(P, &spb);
-  mpass_kernel<false><<<grid, 256, 0, st>>>(m, P, W, shard_start, sel, nullptr, cand, cand_cnt,
-                                            spb);
+  const int grid = mpass_grid(P, 5, &spb);
+  mpass_kernel<kMCollect><<<grid, 256, 0, st>>>(m, P, W, shard_start, sel, nullptr, cand, cand_cnt,
+                                                spb, 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_whist(int W, int blocks_per_shard, const int64_t* shard_start,
+                         const ShardSel* sel, const uint2* cand, const uint32_t* cand_cnt,
+                         const uint32_t* above_cnt, uint32_t* hist, cudaStream_t st) {
+  dim3 grid((unsigned)blocks_per_shard, (unsigned)W);
+  whist_kernel<<<grid, 256, 0, st>>>(shard_start, sel, cand, cand_cnt, above_cnt, hist);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fixup(const int64_t* shard_start, const ShardSel* sel, const uint2* cand,
+                         const uint32_t* cand_cnt, int W, int blocks_per_shard, uint32_t* bits,
+                         uint32_t* tile_cnt, cudaStream_t st) {
+  dim3 grid((unsigned)blocks_per_shard, (unsigned)W);
+  fixup_kernel<<<grid, 256, 0, st>>>(shard_start, sel, cand, cand_cnt, bits, tile_cnt);
   return cudaGetLastError();
 }
 
 cudaError_t launch_cselect(int pass, int W, const int64_t* shard_start, const int64_t* shard_k,
-                           ShardSel* sel, uint32_t* hist, uint32_t* cand_cnt, cudaStream_t st) {
+                           ShardSel* sel, uint32_t* hist, uint32_t* cand_cnt, int form,
+                           cudaStream_t st) {
   switch (pass) {
-    case 0: cselect_kernel<0><<<W, 256, 0, st>>>(shard_start, shard_k, sel, hist, cand_cnt); break;
-    case 1: cselect_kernel<1><<<W, 256, 0, st>>>(shard_start, shard_k, sel, hist, cand_cnt); break;
-    case 2: cselect_kernel<2><<<W, 256, 0, st>>>(shard_start, shard_k, sel, hist, cand_cnt); break;
-    case 3: cselect_kernel<3><<<W, 256, 0, st>>>(shard_start, shard_k, sel, hist, cand_cnt); break;
-    case 4: cselect_kernel<4><<<W, 256, 0, st>>>(shard_start, shard_k, sel, hist, cand_cnt); break;
-    default: cselect_kernel<5><<<W, 256, 0, st>>>(shard_start, shard_k, sel, hist, cand_cnt); break;
+    case 0: cselect_kernel<0><<<W, 256, 0, st>>>(shard_start, shard_k, sel, hist, cand_cnt, form); break;
+    case 1: cselect_kernel<1><<<W, 256, 0, st>>>(shard_start, shard_k, sel, hist, cand_cnt, form); break;
+    case 2: cselect_kernel<2><<<W, 256, 0, st>>>(shard_start, shard_k, sel, hist, cand_cnt, form); break;
+    case 3: cselect_kernel<3><<<W, 256, 0, st>>>(shard_start, shard_k, sel, hist, cand_cnt, form); break;
+    case 4: cselect_kernel<4><<<W, 256, 0, st>>>(shard_start, shard_k, sel, hist, cand_cnt, form); break;
+    default: cselect_kernel<5><<<W, 256, 0, st>>>(shard_start, shard_k, sel, hist, cand_cnt, form); break;
   }
   return cudaGetLastError();
 }

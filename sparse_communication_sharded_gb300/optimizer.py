@@ -73,6 +73,12 @@ class Scape:
     def set_variant(self, flags):
         C.scape_set_variant(self.h, flags)
 
+    def set_fusion(self, level):
+        """How much of the step the compaction pass does: C.FUSE_NONE (separate
+        reduce and adams_sparse launches), C.FUSE_SUM (it writes g_bar) or
+        C.FUSE_UPDATE (it also applies AdamS); results are bit-identical."""
+        C.scape_set_fusion(self.h, level)
+
     def dense_adams_step(self, grads):
         """Dense AdamS baseline on the mean gradient (no error feedback, no mask)."""
         C.scape_dense_adams_step(self.h, [g.data_ptr() for g in grads], self._stream())

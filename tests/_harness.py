@@ -49,7 +49,7 @@ class Report:
 
 
 def run_full_trajectory(wl: synth.Workload, device, steps: int, seed: int = 0,
-                        grad_offset_elems: int = 0, variant: int = 0):
+                        grad_offset_elems: int = 0, variant: int = 0, fusion=None):
     """Whole problem on both sides (small sizes): compare every step."""
     P, W, s = wl.P, wl.W, wl.sparsity
     gdt = torch.bfloat16 if wl.grad_dtype == "bf16" else torch.float32
@@ -59,6 +59,8 @@ def run_full_trajectory(wl: synth.Workload, device, steps: int, seed: int = 0,
     opt = make_opt(params, W, s, gdt)
     if variant:
         opt.set_variant(variant)
+    if fusion is not None:
+        opt.set_fusion(fusion)
     st = O.new_state(w0.numpy(), W, s, HP)
     rep = Report()
     # optional misaligned gradient buffers (scalar path)

@@ -13,6 +13,7 @@ import torch
 
 from oracle import oracle as O
 from sparse_communication_sharded_gb300 import Scape, ScapeError, synth
+from sparse_communication_sharded_gb300 import _scape as C
 from tests._harness import HP, bits_to_bool, make_opt, run_full_trajectory, run_sampled_shards, u32
 
 pytestmark = pytest.mark.gpu
@@ -45,6 +46,17 @@ TRAJ = [
 def test_trajectory_matches_oracle(cuda_device, P, W, s, dtype, quant):
     rep = run_full_trajectory(_wl(P, W, s, dtype, quant=quant), cuda_device, steps=10)
     assert rep.exact, "trajectory not bit-identical to the oracle"
+
+
+@pytest.mark.parametrize("fusion", [C.FUSE_NONE, C.FUSE_SUM, C.FUSE_UPDATE])
+@pytest.mark.parametrize("P,W,s,dtype,quant", [TRAJ[1], TRAJ[2], TRAJ[4], TRAJ[6], TRAJ[7],
+                                                TRAJ[9]])
+def test_trajectory_every_fusion_level(cuda_device, fusion, P, W, s, dtype, quant):
+    """Separate launches (ordered sum, then unpack + AdamS), the sum inside the
+    compaction, and sum + update inside it all give the oracle's bits."""
+    rep = run_full_trajectory(_wl(P, W, s, dtype, quant=quant), cuda_device, steps=6,
+                              fusion=fusion)
+    assert rep.exact
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -97,6 +109,58 @@ def test_refresh_bit_exact_on_same_m(cuda_device, case, P, W, s):
     got_bits, got_idx, bits, idx = _refresh_on(cuda_device, m, W, s)
     assert np.array_equal(got_bits, bits)
     assert np.array_equal(got_idx, idx.view(np.uint32))
+
+
+# ------------------------------------------------------------ warm refresh (speculative bitmap)
+def _drift(m, r, rel):
+    return (m * (1.0 + rel * r.standard_normal(m.size))).astype(np.float32)
+
+
+def _mixed(m, r, W):
+    # every other shard's magnitudes jump by 8x (its threshold leaves the
+    # bucket window); the rest drift slightly
+    out = _drift(m, r, 0.01)
+    start, _ = O.layout(m.size, W, 0.5)
+    for s in range(0, W, 2):
+        out[start[s]:start[s + 1]] *= 8.0
+    return out
+
+
+WARM_CASES = {
+    "same": lambda m, r, W: m.copy(),
+    "drift": lambda m, r, W: _drift(m, r, 0.02),
+    "drift_large": lambda m, r, W: _drift(m, r, 0.3),
+    "scaled_up": lambda m, r, W: (m * 4.0).astype(np.float32),
+    "scaled_down": lambda m, r, W: (m * 0.25).astype(np.float32),
+    "permuted": lambda m, r, W: r.permutation(m),
+    "mixed": _mixed,
+    "levels": lambda m, r, W: (r.integers(-128, 128, m.size) * 2.0 ** -15).astype(np.float32),
+    "zeros": lambda m, r, W: np.zeros_like(m),
+}
+
+
+@pytest.mark.parametrize("case", sorted(WARM_CASES))
+@pytest.mark.parametrize("P,W,s", [(70001, 5, 0.9), (300000, 32, 0.99), (1 << 16, 4, 0.999),
+                                   (1500, 3, 0.5), (20000, 256, 0.9), (4096, 2, 0.0)])
+def test_warm_refresh_bit_exact(cuda_device, case, P, W, s):
+    """Refreshes after the first correct the previous refresh's bitmap; three in
+    a row (m1 cold, then m2 and m3 warm) must each equal the oracle's mask."""
+    r = np.random.default_rng(P + 7 * W)
+    m1 = (r.standard_normal(P) * 1e-3).astype(np.float32)
+    m2 = WARM_CASES[case](m1, r, W)
+    m3 = _drift(m2, r, 0.05)
+    params = torch.zeros(P, device=cuda_device)
+    opt = make_opt(params, W, s, torch.float32)
+    opt.step([torch.zeros(P, device=cuda_device) for _ in range(W)])
+    start, ks = O.layout(P, W, s)
+    for mh in (m1, m2, m3):
+        opt.m.copy_(torch.from_numpy(mh))
+        opt.refresh_mask()
+        torch.cuda.synchronize()
+        bits, idx = O.topk_mask(mh, start, ks)
+        assert np.array_equal(u32(opt.bits()), bits)
+        assert np.array_equal(u32(opt.idx()), idx.view(np.uint32))
+    opt.close()
 
 
 # ------------------------------------------------------------ lag, checkpoint, host path
@@ -168,19 +232,32 @@ def test_set_state_rejects_wrong_counts(cuda_device):
     opt.close()
 
 
-def test_host_buffer_path_matches_device_path(cuda_device):
-    P, W, s = 50000, 4, 0.9
+@pytest.mark.parametrize("P,W,variant,fusion", [(50000, 4, 0, None), (30011, 32, 0, C.FUSE_UPDATE),
+                                                (30011, 32, 0, C.FUSE_SUM),
+                                                (30011, 32, 0, C.FUSE_NONE), (20000, 3, 1, None)])
+def test_host_buffer_path_matches_device_path(cuda_device, P, W, variant, fusion):
+    """scape_step_host (uploads in worker groups, the parameter download before
+    the update plus a patch of the changed coordinates, or after it under the
+    dense off-mask reading) leaves the same parameters on the host after every
+    step as the device path; the host output is poisoned before each step."""
+    s = 0.9
     wl = _wl(P, W, s, "bf16")
-    outs = []
+    per_step = []
     for host in (False, True):
         gen = synth.GradientStream(wl, seed=9, device="cpu")
         params = synth.init_params(P, seed=9).to(cuda_device)
         opt = make_opt(params, W, s, torch.bfloat16)
+        if variant:
+            opt.set_variant(variant)
+        if fusion is not None:
+            opt.set_fusion(fusion)
         dev = [torch.empty(P, dtype=torch.bfloat16, device=cuda_device) for _ in range(W)]
         pin = [torch.empty(P, dtype=torch.bfloat16).pin_memory() for _ in range(W)]
         out = torch.empty(P, dtype=torch.float32).pin_memory()
-        for _ in range(4):
+        got = []
+        for _ in range(5):
             grads = gen.next()
+            out.fill_(float("nan"))
             if host:
                 for p_, g in zip(pin, grads):
                     p_.copy_(g)
@@ -191,10 +268,12 @@ def test_host_buffer_path_matches_device_path(cuda_device):
                 opt.step(dev)
                 opt.refresh_mask()
                 out.copy_(params)
-        torch.cuda.synchronize()
-        outs.append(out.numpy().copy())
+            torch.cuda.synchronize()
+            got.append(out.numpy().copy())
+        per_step.append(got)
         opt.close()
-    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+    for a, b in zip(*per_step):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
 
 
 def test_state_errors(cuda_device):
@@ -226,6 +305,18 @@ def test_profiling_counts_launches(cuda_device):
     assert prof["ef_compact"][1] == 2 and prof["dense_step"][1] == 1
     assert prof["ef_compact"][0] > 0
     assert opt.launch_count() - n0 == sum(n for _, n in prof.values())
+    # launches of one sparse step at each fusion level
+    for level, n_red, n_upd in ((C.FUSE_NONE, 1, 1), (C.FUSE_SUM, 0, 1), (C.FUSE_UPDATE, 0, 0)):
+        opt.set_fusion(level)
+        opt.profile_reset()
+        opt.step(g)
+        torch.cuda.synchronize()
+        opt.profile_collect()
+        prof = opt.profile_read()
+        assert prof["ef_compact"][1] == 1
+        assert (prof["reduce"][1], prof["adams_sparse"][1]) == (n_red, n_upd), level
+    with pytest.raises(ScapeError):
+        opt.set_fusion(3)
     opt.close()
 
 

@@ -34,6 +34,14 @@ def test_variant_trajectory_matches_oracle(cuda_device, variant, P, W, s, dtype)
     assert rep.exact
 
 
+@pytest.mark.parametrize("fusion", [0, 1])
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_variant_trajectory_other_fusion_levels(cuda_device, variant, fusion):
+    rep = run_full_trajectory(_wl(70001, 8, 0.99, "bf16"), cuda_device, steps=6, variant=variant,
+                              fusion=fusion)
+    assert rep.exact
+
+
 def test_unknown_variant_flag_is_rejected(cuda_device):
     opt = make_opt(torch.zeros(64, device=cuda_device), 2, 0.5, torch.float32)
     with pytest.raises(C.ScapeError):
