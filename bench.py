@@ -164,6 +164,40 @@ def _mem_available():
     return 0
 
 
+def _parse_cpulist(text):
+    cpus = set()
+    for part in text.strip().split(","):
+        if not part:
+            continue
+        if "-" in part:
+            a, b = part.split("-")
+            cpus.update(range(int(a), int(b) + 1))
+        else:
+            cpus.add(int(part))
+    return cpus
+
+
+def _bind_near_gpu(dev):
+    """Run this process on the host cores attached to the GPU's socket, so
+    that page-locked buffers allocated afterwards sit in that socket's memory
+    (first touch) and host<->device copies do not cross the socket link.
+    Returns the cores used, or None if the topology is not readable."""
+    import torch
+
+    try:
+        pr = torch.cuda.get_device_properties(dev)
+        path = "/sys/bus/pci/devices/%04x:%02x:%02x.0/local_cpulist" % (
+            pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+        with open(path) as f:
+            cpus = _parse_cpulist(f.read()) & os.sched_getaffinity(0)
+        if not cpus:
+            return None
+        os.sched_setaffinity(0, cpus)
+        return sorted(cpus)
+    except (AttributeError, OSError, ValueError):
+        return None
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -261,7 +295,7 @@ def bench_gpu(args, wl):
     seed = 1000 * rank
     params = synth.init_params(P, seed=seed, device=dev)
     opt = pkg.Scape(params, W, wl.sparsity, layer_numel=[n for _, n in wl.layers],
-                    grad_dtype=gdt, residuals=args.residuals)
+                    grad_dtype=gdt, residuals=args.residuals, staging_rows=args.staging_rows)
     opt.set_fusion(FUSION[args.fusion])
     gen = synth.GradientStream(wl, seed=seed, device=dev)
     grads = gen.alloc()
@@ -356,6 +390,8 @@ def bench_gpu(args, wl):
             "config": {"workload": wl.name, "P": P, "W": W, "sparsity": wl.sparsity,
                        "k": opt.k, "grad_dtype": wl.grad_dtype, "state_dtype": "f32",
                        "residuals": args.residuals, "fusion": args.fusion,
+                       "staging_rows": (opt.staging.numel() // (4 * ((P + 63) // 64 * 64))
+                                        if opt.staging is not None else 0),
                        "l2": "inputs larger than L2 (gradients + residuals far beyond 129 MB)",
                        "parallelism": f"{ws} independent problems (weak)"},
             "hbm_gbs": alg["total"] / (t_max / 1000.0) / 1e9,
@@ -440,6 +476,7 @@ def bench_e2e(opt, wl, dev_grads, steps, dev, shared_source=False):
     gdt = dev_grads[0].dtype
     esz = dev_grads[0].element_size()
     need = W * P * esz + 4 * P
+    near = _bind_near_gpu(dev)
     if not shared_source and _mem_available() > 3 * need:
         host = [torch.empty(P, dtype=gdt).pin_memory() for _ in range(W)]
         shared = False
@@ -464,11 +501,28 @@ def bench_e2e(opt, wl, dev_grads, steps, dev, shared_source=False):
         opt.step_host(host, dev_grads, out)
         st.synchronize()
         times.append(time.perf_counter() - t0)
-    secs = sum(times) / len(times)
+    # median step: a single step slowed by the host (other tenants, page
+    # reclaim) does not set the figure; every step is listed in ms_each
+    secs = statistics.median(times)
+    # the host link alone on this machine: the same uploads and download as plain
+    # copies with no kernels, for reading the end-to-end number against it
+    link = []
+    for _ in range(max(steps, 2)):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for h_, d in zip(host, dev_grads):
+            d.copy_(h_, non_blocking=True)
+        out.copy_(opt.params, non_blocking=True)
+        torch.cuda.synchronize()
+        link.append(time.perf_counter() - t0)
     del host
     return {"value": P / secs, "unit": UNIT, "h2d_bytes_per_step": W * P * esz,
             "d2h_bytes_per_step": 4 * P, "ms_per_step": 1000 * secs,
             "ms_each": [1000 * x for x in times],
+            "host_cores": f"{len(near)} cores local to the GPU" if near else "unbound",
+            "min_ms": 1000 * min(times),
+            "link_only_ms": {"median": 1000 * statistics.median(link), "min": 1000 * min(link),
+                             "each": [1000 * x for x in link]},
             "shared_host_source": shared}
 
 
@@ -479,10 +533,13 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="llama500m")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-steps", type=int, default=2)
     ap.add_argument("--residuals", default="device", choices=["device", "host"],
                     help="error-feedback buffers in HBM or in pinned host memory")
+    ap.add_argument("--staging-rows", type=int, default=None,
+                    help="with --residuals host: device rows staging the residuals "
+                         "(default min(W, 12); 0 = kernels access host memory in place)")
     ap.add_argument("--fusion", default="sum", choices=sorted(FUSION),
                     help="what the compaction pass also does: none (separate reduce and "
                          "adams_sparse), sum (writes g_bar), update (also AdamS)")

@@ -197,6 +197,25 @@ enum scape_fusion { SCAPE_FUSE_NONE = 0, SCAPE_FUSE_SUM = 1, SCAPE_FUSE_UPDATE =
 int scape_set_fusion(scape_t *h, int level);
 
 /*
+ * Device staging for residuals bound in host memory (the pages keep the
+ * error-feedback buffers on the CPU side, "SCAPE" Sec. I).  With a staging
+ * buffer bound, every sparse scape_step() moves the residuals through it in
+ * worker groups of rows/3: one group copies in on an internal stream while
+ * the previous one is compacted on `stream` and the one before copies its
+ * updated residuals back on a second internal stream, so both directions of
+ * the host link are in use and the compaction reads HBM.  Without one (NULL
+ * or 0 bytes, the default) the kernels access host residuals in place.
+ * Ignored while the residuals are device memory; the dense first step,
+ * scape_step_host() and the union baseline always access them in place.
+ * scape_residual_staging_bytes() gives the size for `rows` residual rows
+ * (rows >= 3; each row is P floats rounded up to 64).
+ *   device_buffer  caller-owned device memory, 16-byte aligned
+ * Errors: SCAPE_EINVAL if the buffer is misaligned or holds fewer than 3 rows.
+ */
+int scape_residual_staging_bytes(const scape_t *h, int rows, size_t *bytes);
+int scape_set_residual_staging(scape_t *h, void *device_buffer, size_t bytes);
+
+/*
  * Dense baselines the pages compare SCAPE against ("SCAPE" abstract, Sec. I),
  * on the handle's bound w and m: the gradient is the plain ordered mean of
  * the W workers' gradients (no error feedback, no mask; residuals untouched)

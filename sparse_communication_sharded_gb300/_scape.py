@@ -47,6 +47,8 @@ _PROTOS = {
     "scape_set_lr": (_i32, [_vp, _f32]),
     "scape_set_variant": (_i32, [_vp, _i32]),
     "scape_set_fusion": (_i32, [_vp, _i32]),
+    "scape_residual_staging_bytes": (_i32, [_vp, _i32, ctypes.POINTER(ctypes.c_size_t)]),
+    "scape_set_residual_staging": (_i32, [_vp, _vp, ctypes.c_size_t]),
     "scape_dense_adams_step": (_i32, [_vp, _vp, _vp]),
     "scape_union_workspace_bytes": (_i32, [_vp, _i64, _vp]),
     "scape_union_step": (_i32, [_vp, _vp, _vp, ctypes.c_size_t, _i64, _vp, _vp]),
@@ -163,6 +165,16 @@ FUSE_NONE, FUSE_SUM, FUSE_UPDATE = 0, 1, 2
 
 def scape_set_fusion(h, level):
     _check(h, load().scape_set_fusion(h, int(level)))
+
+
+def scape_residual_staging_bytes(h, rows):
+    n = ctypes.c_size_t(0)
+    _check(h, load().scape_residual_staging_bytes(h, int(rows), ctypes.byref(n)))
+    return n.value
+
+
+def scape_set_residual_staging(h, ptr, nbytes):
+    _check(h, load().scape_set_residual_staging(h, ptr, int(nbytes)))
 
 
 def scape_dense_adams_step(h, grad_ptrs, stream=0):

@@ -75,6 +75,12 @@ struct scape {
   cudaStream_t copy_stream = nullptr, down_stream = nullptr;
   cudaEvent_t ev_start = nullptr, ev_updated = nullptr, ev_done = nullptr, ev_down = nullptr;
   cudaEvent_t ev_group[kMaxGroups] = {};
+  // residuals in host memory moved through a device staging buffer
+  bool e_on_host = false;          // every e^w is host memory
+  float* stage = nullptr;          // staging buffer (caller-owned device memory)
+  int stage_workers = 0;           // residual rows it holds
+  int64_t stage_stride = 0;        // floats per row (P rounded up to 64)
+  std::vector<cudaEvent_t> ev_in, ev_comp, ev_out;  // per worker group
   // profiling
   bool prof = false;
   std::vector<ProfRec> pending;
@@ -225,6 +231,73 @@ int rebuild_from_bits(scape_t* h, cudaStream_t st, bool counts_ready) {
                     [&] { return launch_index(h->bits(), h->P, h->tile_base(), h->idx(), h->k, st); });
 }
 
+// Internal streams and events of the pipelined paths (created on first use).
+int ensure_aux(scape_t* h) {
+  if (h->aux_ready) return SCAPE_OK;
+  cudaError_t e = cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->down_stream, cudaStreamNonBlocking);
+  for (auto* ev : {&h->ev_start, &h->ev_updated, &h->ev_done, &h->ev_down})
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+  for (int g = 0; g < scape_t::kMaxGroups && e == cudaSuccess; ++g)
+    e = cudaEventCreateWithFlags(&h->ev_group[g], cudaEventDisableTiming);
+  if (e != cudaSuccess) return cuda_fail(h, e, "stream/event setup");
+  h->aux_ready = true;
+  return SCAPE_OK;
+}
+
+// A sparse step whose residuals live in host memory, moved through the
+// device staging buffer in worker groups: three groups are in flight, one
+// copying in (copy stream), one being compacted (`st`), one copying back
+// (download stream), so both directions of the host link stay busy.  The
+// staging rows of group g are reused by group g + 3 once its copy-back ended.
+int step_staged(scape_t* h, const WorkerPtrs& grads, bool vec, const AdamsConst& c,
+                cudaStream_t st) {
+  int rc = ensure_aux(h);
+  if (rc) return rc;
+  const int gsz = h->stage_workers / 3;
+  const int G = (h->W + gsz - 1) / gsz;
+  cudaError_t e = cudaSuccess;
+  for (auto* v : {&h->ev_in, &h->ev_comp, &h->ev_out})
+    while ((int)v->size() < G && e == cudaSuccess) {
+      cudaEvent_t ev = nullptr;
+      e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+      if (e == cudaSuccess) v->push_back(ev);
+    }
+  if (e != cudaSuccess) return cuda_fail(h, e, "scape_step: staging events");
+  cudaStream_t cp = h->copy_stream, dn = h->down_stream;
+  const size_t eb = (size_t)h->P * 4;
+  e = cudaEventRecord(h->ev_start, st);  // the residuals' earlier users
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(cp, h->ev_start, 0);
+  for (int g = 0; g < G && e == cudaSuccess; ++g) {
+    const int w0 = g * gsz, w1 = w0 + gsz < h->W ? w0 + gsz : h->W;
+    float* rows = h->stage + (int64_t)(g % 3) * gsz * h->stage_stride;
+    if (g >= 3) e = cudaStreamWaitEvent(cp, h->ev_out[g - 3], 0);
+    for (int w = w0; w < w1 && e == cudaSuccess; ++w)
+      e = cudaMemcpyAsync(rows + (int64_t)(w - w0) * h->stage_stride, h->e[w], eb,
+                          cudaMemcpyHostToDevice, cp);
+    if (e == cudaSuccess) e = cudaEventRecord(h->ev_in[g], cp);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_in[g], 0);
+    if (e != cudaSuccess) break;
+    WorkerPtrs p = grads;
+    for (int w = w0; w < w1; ++w) p.e[w] = rows + (int64_t)(w - w0) * h->stage_stride;
+    rc = enqueue_compact(h, p, w0, w1, vec, c, st);
+    if (rc) return rc;
+    e = cudaEventRecord(h->ev_comp[g], st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(dn, h->ev_comp[g], 0);
+    for (int w = w0; w < w1 && e == cudaSuccess; ++w)
+      e = cudaMemcpyAsync(h->e[w], rows + (int64_t)(w - w0) * h->stage_stride, eb,
+                          cudaMemcpyDeviceToHost, dn);
+    if (e == cudaSuccess) e = cudaEventRecord(h->ev_out[g], dn);
+  }
+  if (e != cudaSuccess) return cuda_fail(h, e, "scape_step: residual staging");
+  rc = enqueue_update(h, c, st);
+  if (rc) return rc;
+  // the step is complete once the last residuals are home
+  e = cudaStreamWaitEvent(st, h->ev_out[G - 1], 0);
+  if (e != cudaSuccess) return cuda_fail(h, e, "scape_step: stream wait");
+  return SCAPE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -331,6 +404,8 @@ void scape_destroy(scape_t* h) {
     cudaStreamDestroy(h->copy_stream);
     cudaStreamDestroy(h->down_stream);
   }
+  for (auto* v : {&h->ev_in, &h->ev_comp, &h->ev_out})
+    for (auto ev : *v) cudaEventDestroy(ev);
   delete h;
 }
 
@@ -372,6 +447,17 @@ int scape_bind(scape_t* h, float* params, float* m, float* const* host_e_ptrs, v
     if (!aligned16(host_e_ptrs[w]))
       return fail(h, SCAPE_EINVAL, "scape_bind: residuals must be 16-byte aligned");
     h->e[w] = host_e_ptrs[w];
+  }
+  // residuals in host memory (page-locked, or pageable where the device can
+  // address it): candidates for the staged step
+  h->e_on_host = true;
+  for (int w = 0; w < h->W; ++w) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, h->e[w]) != cudaSuccess) {
+      (void)cudaGetLastError();
+      continue;  // not known to CUDA: host memory
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) h->e_on_host = false;
   }
   h->w = params;
   h->m = m;
@@ -419,6 +505,10 @@ int scape_step(scape_t* h, const void* const* host_grad_ptrs, void* stream) {
     });
     if (rc) return rc;
     h->buffers_valid = false;
+  } else if (h->e_on_host && h->stage) {
+    rc = step_staged(h, p, vec, c, st);
+    if (rc) return rc;
+    h->buffers_valid = true;
   } else {
     rc = enqueue_compact(h, p, 0, h->W, vec, c, st);
     if (rc) return rc;
@@ -552,6 +642,33 @@ int scape_refresh_mask(scape_t* h, void* stream) {
   if (rc) return rc;
   h->warm = true;
   h->mask_ready = true;
+  return SCAPE_OK;
+}
+
+int scape_set_residual_staging(scape_t* h, void* device_buffer, size_t bytes) {
+  if (!h) return SCAPE_EINVAL;
+  const int64_t stride = (h->P + 63) / 64 * 64;
+  if (!device_buffer || bytes == 0) {
+    h->stage = nullptr;
+    h->stage_workers = 0;
+    return SCAPE_OK;
+  }
+  if (!aligned16(device_buffer))
+    return fail(h, SCAPE_EINVAL, "scape_set_residual_staging: buffer must be 16-byte aligned");
+  const int64_t rows = (int64_t)(bytes / ((size_t)stride * 4));
+  if (rows < 3)
+    return fail(h, SCAPE_EINVAL,
+                "scape_set_residual_staging: buffer holds fewer than 3 residual rows");
+  h->stage = static_cast<float*>(device_buffer);
+  h->stage_workers = (int)(rows < h->W ? rows : h->W);
+  if (h->stage_workers < 3) h->stage_workers = 3;  // W < 3: groups of one worker
+  h->stage_stride = stride;
+  return SCAPE_OK;
+}
+
+int scape_residual_staging_bytes(const scape_t* h, int rows, size_t* bytes) {
+  if (!h || !bytes || rows < 3) return SCAPE_EINVAL;
+  *bytes = (size_t)rows * (size_t)((h->P + 63) / 64 * 64) * 4;
   return SCAPE_OK;
 }
 
@@ -864,15 +981,9 @@ int scape_step_host(scape_t* h, const void* const* host_grads_src, void* const* 
     if (e != cudaSuccess) return cuda_fail(h, e, "scape_step_host: parameter download");
     return SCAPE_OK;
   }
-  if (!h->aux_ready) {
-    e = cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking);
-    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->down_stream, cudaStreamNonBlocking);
-    for (auto* ev : {&h->ev_start, &h->ev_updated, &h->ev_done, &h->ev_down})
-      if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
-    for (int g = 0; g < scape_t::kMaxGroups && e == cudaSuccess; ++g)
-      e = cudaEventCreateWithFlags(&h->ev_group[g], cudaEventDisableTiming);
-    if (e != cudaSuccess) return cuda_fail(h, e, "scape_step_host: stream/event setup");
-    h->aux_ready = true;
+  {
+    const int rc = ensure_aux(h);
+    if (rc) return rc;
   }
   // Parameters: under the paper's reading a step changes w only at its k
   // selected coordinates, so the dense download of w runs first (the previous

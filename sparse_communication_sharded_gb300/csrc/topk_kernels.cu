@@ -212,7 +212,11 @@ mpass_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __res
 //    from one pointer), so the ballot of "selected" for (h, q) is bitmap word
 //    32h + 4w + q and lane 0 stores a warp's four words with one 16-byte store.
 //    The next tile's values are loaded while the current one is processed.
-//  * Candidates whose bucket is within one of `guess` are staged as in mpass.
+//  * Candidates whose bucket is within one of `guess` are staged per lane:
+//    lane l appends to its own column of the warp's shared-memory buffer
+//    (slot j at j * 32 + l), one predicated store per hit, with no warp-wide
+//    step per parameter; a warp-wide prefix sum places the columns in the
+//    shard's candidate range when one of them fills up.
 //  * above_cnt[s] gets the popcount of those tiles plus the number of
 //    parameters above the window in the partial pieces.  Parameters above the
 //    window are all selected by the previous threshold, so whist recovers the
@@ -221,13 +225,14 @@ mpass_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __res
 // Partial pieces (shard boundaries inside a tile, the ragged end) are only
 // staged and counted; the remark kernel writes their bits.
 constexpr int kSpecBlocksPerSm = 4;
+constexpr int kLaneSlots = 16;  // staged candidates per lane
 
 __global__ void __launch_bounds__(256, kSpecBlocksPerSm)
 spec_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __restrict__ shard_start,
             const ShardSel* __restrict__ sel, uint2* __restrict__ cand,
             uint32_t* __restrict__ cand_cnt, uint32_t* __restrict__ above_cnt,
             uint32_t* __restrict__ bits, uint32_t* __restrict__ tile_cnt, int64_t segs_per_block) {
-  __shared__ uint2 wbuf[8][kWarpStage];
+  __shared__ uint2 lbuf[8][kLaneSlots * 32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t nseg = (P + kMSeg - 1) / kMSeg;
   const int64_t g0 = (int64_t)blockIdx.x * segs_per_block;
@@ -242,20 +247,25 @@ spec_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __rest
       any |= sel[q].guess != kNoGuess;
     if (!any) return;
   }
-  const uint32_t lt_mask = (1u << lane) - 1u;
-  uint2* const mybuf = wbuf[warp];
-  uint32_t wn = 0;  // entries in this warp's buffer (same value in every lane)
+  uint2* const col = lbuf[warp] + lane;  // this lane's column: slot j at col[32 * j]
+  uint32_t nl = 0;                       // this lane's staged candidates
 
-  auto flush_warp = [&](int shard) {
-    if (wn == 0) return;
-    __syncwarp();
+  // place every lane's column in the shard's candidate range
+  auto flush_lanes = [&](int shard) {
+    uint32_t incl = nl;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+    if (total == 0) return;
     uint32_t base = 0;
-    if (lane == 0) base = atomicAdd(cand_cnt + shard, wn);
+    if (lane == 0) base = atomicAdd(cand_cnt + shard, total);
     base = __shfl_sync(0xffffffffu, base, 0);
-    uint2* out = cand + __ldg(shard_start + shard) + base;
-    for (uint32_t j = lane; j < wn; j += 32) out[j] = mybuf[j];
-    __syncwarp();
-    wn = 0;
+    uint2* out = cand + __ldg(shard_start + shard) + base + (incl - nl);
+    for (uint32_t j = 0; j < nl; ++j) out[j] = col[32 * j];
+    nl = 0;
   };
 
   uint32_t pos = r0;
@@ -276,16 +286,12 @@ spec_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __rest
       auto piece = [&](uint32_t a, uint32_t b) {
         for (uint32_t b0 = a; b0 < b; b0 += 256) {
           const uint32_t i = b0 + threadIdx.x;
-          const bool in = i < b;
-          const uint32_t key = in ? magnitude_key(__ldcs(m + i)) : 0u;
-          acount += (in && key >= top_key) ? 1u : 0u;
-          const bool hit = in && key - wkey_lo < wkey_n;
-          const uint32_t ball = __ballot_sync(0xffffffffu, hit);
-          if (ball) {
-            if (hit) mybuf[wn + __popc(ball & lt_mask)] = make_uint2(key, i);
-            wn += __popc(ball);
-            if (wn > kWarpStage - 32) flush_warp(s);
+          if (i < b) {
+            const uint32_t key = magnitude_key(__ldcs(m + i));
+            acount += key >= top_key ? 1u : 0u;
+            if (key - wkey_lo < wkey_n) col[32 * nl++] = make_uint2(key, i);
           }
+          if (__any_sync(0xffffffffu, nl == kLaneSlots)) flush_lanes(s);
         }
       };
 
@@ -294,7 +300,7 @@ spec_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __rest
         piece(pos, end);
       } else {
         piece(pos, ta * kMSeg);
-        if (wn > kWarpStage - 256) flush_warp(s);  // a tile adds at most 256 per warp
+        if (__any_sync(0xffffffffu, nl > kLaneSlots - 8)) flush_lanes(s);  // a tile adds <= 8
         const uint32_t t_is = istar / kMSeg;  // the tile holding istar
         const int lim = (int)(istar - t_is * kMSeg);
         const float* p = m + (size_t)ta * kMSeg + 128 * warp + lane;
@@ -314,30 +320,14 @@ spec_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __rest
           uint32_t tc = 0;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            uint32_t key[4], wd[4], hb[4];
+            uint32_t wd[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) key[q] = magnitude_key(xc[4 * h + q]);
-            if (!mixed) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q) wd[q] = __ballot_sync(0xffffffffu, key[q] >= thr);
-            } else {
-#pragma unroll
-              for (int q = 0; q < 4; ++q)
-                wd[q] = __ballot_sync(
-                    0xffffffffu,
-                    key[q] >= kstar + (uint32_t)(1024 * h + 128 * warp + 32 * q + lane > lim));
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              hb[q] = __ballot_sync(0xffffffffu, key[q] - wkey_lo < wkey_n);
-            if ((hb[0] | hb[1] | hb[2] | hb[3]) != 0u) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                if ((hb[q] >> lane) & 1u)
-                  mybuf[wn + __popc(hb[q] & lt_mask)] =
-                      make_uint2(key[q], ibase + 1024 * h + 32 * q);
-                wn += __popc(hb[q]);
-              }
+            for (int q = 0; q < 4; ++q) {
+              const uint32_t key = magnitude_key(xc[4 * h + q]);
+              const uint32_t tq =
+                  mixed ? kstar + (uint32_t)(1024 * h + 128 * warp + 32 * q + lane > lim) : thr;
+              wd[q] = __ballot_sync(0xffffffffu, key >= tq);
+              if (key - wkey_lo < wkey_n) col[32 * nl++] = make_uint2(key, ibase + 1024 * h + 32 * q);
             }
             if (lane == 0) {
               *reinterpret_cast<uint4*>(bw + 32 * h) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
@@ -348,7 +338,7 @@ spec_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __rest
             atomicAdd(tile_cnt + t, tc);
             acount += tc;
           }
-          if (wn > kWarpStage - 256) flush_warp(s);
+          if (__any_sync(0xffffffffu, nl > kLaneSlots - 8)) flush_lanes(s);
           p += kMSeg;
           bw += kMSeg / 32;
           if (t + 1 < tb) {
@@ -358,7 +348,7 @@ spec_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __rest
         }
         piece(tb * kMSeg, end);
       }
-      flush_warp(s);
+      flush_lanes(s);
       const uint32_t a = __reduce_add_sync(0xffffffffu, acount);
       if (lane == 0 && a) atomicAdd(above_cnt + s, a);
     }

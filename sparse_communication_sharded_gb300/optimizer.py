@@ -17,10 +17,13 @@ class Scape:
 
     def __init__(self, params: torch.Tensor, W: int, sparsity: float, *, layer_numel=None,
                  lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1,
-                 grad_dtype=torch.bfloat16, residuals: str = "device"):
+                 grad_dtype=torch.bfloat16, residuals: str = "device", staging_rows=None):
         """residuals: "device" (HBM) or "host": the W error-feedback buffers
-        live in pinned host memory, which the kernels read and write in place
-        over the host link (keeps W*P*4 bytes out of HBM)."""
+        live in pinned host memory (keeps W*P*4 bytes out of HBM).  With host
+        residuals, staging_rows (default min(W, 12); 0 for none) residual rows
+        of device memory stage them: sparse steps copy them in and out in
+        worker groups, overlapped with the compaction; without staging the
+        kernels read and write them in place over the host link."""
         if not params.is_cuda or params.dtype != torch.float32 or not params.is_contiguous():
             raise ValueError("params must be a contiguous float32 CUDA tensor")
         P = params.numel()
@@ -48,6 +51,14 @@ class Scape:
         self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
         C.scape_bind(self.h, params.data_ptr(), self.m.data_ptr(), [x.data_ptr() for x in self.e],
                      self.workspace.data_ptr(), self.ws_bytes)
+        self.staging = None
+        if residuals == "host":
+            rows = min(W, 12) if staging_rows is None else int(staging_rows)
+            if rows:
+                rows = max(rows, 3)
+                nbytes = C.scape_residual_staging_bytes(self.h, rows)
+                self.staging = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+                C.scape_set_residual_staging(self.h, self.staging.data_ptr(), nbytes)
 
     # ----------------------------------------------------------- hot path
     @staticmethod

@@ -222,6 +222,53 @@ def test_checkpoint_resume_bit_identical(cuda_device):
     assert np.array_equal(a[3], b[3])
 
 
+def test_resume_into_a_live_handle(cuda_device):
+    """set_state on a handle that already ran another trajectory: its next
+    refresh starts from thresholds of unrelated data and must still give the
+    same result as a fresh handle resumed from the same checkpoint."""
+    P, W, s = 70001, 5, 0.99
+    wl = _wl(P, W, s, "bf16")
+
+    def trajectory(seed, steps):
+        gen = synth.GradientStream(wl, seed=seed, device=cuda_device)
+        params = synth.init_params(P, seed=seed, device=cuda_device)
+        opt = make_opt(params, W, s, torch.bfloat16)
+        bufs = gen.alloc()
+        for _ in range(steps):
+            gen.next_into(bufs)
+            opt.step(bufs)
+            opt.refresh_mask()
+        return opt, params, gen, bufs
+
+    # the checkpoint: 4 steps of seed 21
+    src, sp, _, _ = trajectory(21, 4)
+    ckpt = (sp.clone(), src.m.clone(), [x.clone() for x in src.e], src.bits().clone(), src.t)
+    src.close()
+    outs = []
+    for live in (False, True):
+        if live:
+            opt, params, _, _ = trajectory(22, 6)  # a different run on the same handle
+            params.copy_(ckpt[0])
+        else:
+            params = ckpt[0].clone()
+            opt = make_opt(params, W, s, torch.bfloat16)
+        opt.m.copy_(ckpt[1])
+        for dst, x in zip(opt.e, ckpt[2]):
+            dst.copy_(x)
+        opt.set_state(ckpt[4], ckpt[3])
+        gen = synth.GradientStream(wl, seed=23, device=cuda_device)
+        bufs = gen.alloc()
+        for _ in range(4):
+            gen.next_into(bufs)
+            opt.step(bufs)
+            opt.refresh_mask()
+        torch.cuda.synchronize()
+        outs.append((u32(params), u32(opt.m), u32(opt.bits()), u32(opt.idx())))
+        opt.close()
+    for a, b in zip(*outs):
+        assert np.array_equal(a, b)
+
+
 def test_set_state_rejects_wrong_counts(cuda_device):
     P, W, s = 10000, 4, 0.9
     params = torch.zeros(P, device=cuda_device)
@@ -342,17 +389,23 @@ def test_flat_sweep_largest_point_sampled(cuda_device):
 
 
 # ------------------------------------------------------------ residuals in host memory
-@pytest.mark.parametrize("P,W,s,dtype", [(70001, 4, 0.99, "bf16"), (4096, 2, 0.9, "f32")])
-def test_host_resident_residuals_match_oracle(cuda_device, P, W, s, dtype):
+@pytest.mark.parametrize("P,W,s,dtype", [(70001, 4, 0.99, "bf16"), (4096, 2, 0.9, "f32"),
+                                         (50003, 13, 0.99, "bf16")])
+@pytest.mark.parametrize("staging", [0, 3, 4, 7, 64])
+def test_host_resident_residuals_match_oracle(cuda_device, P, W, s, dtype, staging):
     """Error-feedback buffers in pinned host memory, read and written in place
-    by the kernels: same trajectory as the oracle, bit for bit."""
+    by the kernels (staging 0), or moved through a device staging buffer of
+    that many rows in worker groups: same trajectory as the oracle, bit for
+    bit."""
     gdt = torch.bfloat16 if dtype == "bf16" else torch.float32
     wl = _wl(P, W, s, dtype)
     gen = synth.GradientStream(wl, seed=8, device="cpu")
     w0 = synth.init_params(P, seed=8)
     params = w0.to(cuda_device)
     opt = Scape(params, W, s, lr=HP.lr, beta1=HP.beta1, beta2=HP.beta2, eps=HP.eps,
-                weight_decay=HP.weight_decay, grad_dtype=gdt, residuals="host")
+                weight_decay=HP.weight_decay, grad_dtype=gdt, residuals="host",
+                staging_rows=staging)
+    assert (opt.staging is None) == (staging == 0)
     assert not opt.e[0].is_cuda
     st = O.new_state(w0.numpy(), W, s, HP)
     for _ in range(6):
