@@ -52,7 +52,7 @@ struct ShardSel {
   uint32_t guess;     // first-digit bucket of the previous refresh (0xFFFFFFFF: none)
   uint32_t flags;     // kSelNeedCollect, kSelRemark, kSelNeedHist
   uint32_t kstar_prev;  // the threshold the speculative bitmap was written with
-  uint32_t pad;
+  uint32_t guess_prev;  // first-digit bucket of the refresh before (0xFFFFFFFF: none)
   int64_t istar_prev;
 };
 constexpr uint32_t kNoGuess = 0xFFFFFFFFu;

@@ -38,6 +38,34 @@ __device__ __forceinline__ uint64_t composite(uint32_t key, uint32_t i) {
   return ((uint64_t)key << 32) | (uint64_t)(0xFFFFFFFFu - i);
 }
 
+// The first-digit buckets [lo, hi] a refresh stages candidates from: one
+// either side of the previous threshold's bucket, stretched toward the bucket
+// the last two thresholds extrapolate to (at most kMaxTrend buckets on),
+// because early in training the first moments grow from step to step and the
+// threshold drifts the same way.  hi may be 4096 (no such digit).  With no
+// previous bucket the window is empty (lo > hi).
+constexpr int kMaxTrend = 3;
+constexpr int kMaxWindow = 2 * 1 + kMaxTrend + 1;  // buckets in the widest window
+
+__device__ __forceinline__ void bucket_window(const ShardSel& q, uint32_t& lo, uint32_t& hi) {
+  if (q.guess == kNoGuess) {
+    lo = 1;
+    hi = 0;
+    return;
+  }
+  int a = (int)q.guess, b = (int)q.guess;
+  if (q.guess_prev != kNoGuess) {
+    int d = (int)q.guess - (int)q.guess_prev;
+    d = d > kMaxTrend ? kMaxTrend : (d < -kMaxTrend ? -kMaxTrend : d);
+    int pred = (int)q.guess + d;
+    pred = pred < 0 ? 0 : (pred > kCBins0 - 1 ? kCBins0 - 1 : pred);
+    a = pred < a ? pred : a;
+    b = pred > b ? pred : b;
+  }
+  lo = (uint32_t)(a > 0 ? a - 1 : 0);
+  hi = (uint32_t)(b + 1);
+}
+
 // ------------------------------------------------------------------ passes over m
 // mpass: the histogram and collect reads of m.  Blocks are persistent: block b
 // walks a contiguous run of 2048-parameter segments (the mark tiles),
@@ -137,8 +165,9 @@ mpass_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __res
         if (!HIST) {
           wlo = (uint32_t)ss.cprefix;
         } else if (ss.guess != kNoGuess && !selective) {
-          wlo = ss.guess > 0 ? ss.guess - 1 : 0;
-          wwid = ss.guess + 1 - wlo;
+          uint32_t hi;
+          bucket_window(ss, wlo, hi);
+          wwid = hi - wlo;
         }
       }
       const int64_t lo = max(seg0, __ldg(shard_start + s)), hi = min(seg1, s_hi);
@@ -274,10 +303,11 @@ spec_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __rest
     const uint32_t end = min((uint32_t)__ldg(shard_start + s + 1), r1);
     const ShardSel ss = sel[s];
     if (ss.guess != kNoGuess) {
-      const uint32_t wlo = ss.guess > 0 ? ss.guess - 1 : 0;
+      uint32_t wlo, whi;
+      bucket_window(ss, wlo, whi);
       const uint32_t wkey_lo = wlo << 19;                   // window: key - wkey_lo < wkey_n
-      const uint32_t wkey_n = (ss.guess + 2 - wlo) << 19;
-      const uint32_t top_key = (ss.guess + 2) << 19;        // keys >= top_key: above it
+      const uint32_t wkey_n = (whi + 1 - wlo) << 19;
+      const uint32_t top_key = (whi + 1) << 19;             // keys >= top_key: above it
       const uint32_t kstar = ss.kstar;
       const uint32_t istar = (uint32_t)ss.istar;
       uint32_t acount = 0;  // this thread's share of above_cnt[s]
@@ -358,8 +388,8 @@ spec_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __rest
 
 // ------------------------------------------------------------------ whist
 // Warm refresh, grid (G, W): the first-digit histogram of shard s from its
-// staged window candidates, with the parameters above and below the window
-// lumped into the two bins next to it.  cselect pass 0 then finds the
+// staged window candidates (bucket_window), with the parameters above and
+// below the window lumped into the two bins next to it.  cselect pass 0 then finds the
 // threshold bucket as on a full histogram; a lumped bin means a miss.
 //   above = above_cnt[s] - (staged candidates the previous threshold selected
 //           inside whole single-shard tiles)
@@ -369,39 +399,43 @@ __global__ void __launch_bounds__(256)
 whist_kernel(const int64_t* __restrict__ shard_start, const ShardSel* __restrict__ sel,
              const uint2* __restrict__ cand, const uint32_t* __restrict__ cand_cnt,
              const uint32_t* __restrict__ above_cnt, uint32_t* __restrict__ hist) {
-  __shared__ uint32_t sh[4];  // three window bins, then the selected count
+  __shared__ uint32_t sh[kMaxWindow + 1];  // the window's bins, then the selected count
   const int s = blockIdx.y;
   const ShardSel ss = sel[s];
-  const uint32_t guess = ss.guess;
-  if (guess == kNoGuess) return;
-  const uint32_t wlo = guess > 0 ? guess - 1 : 0;
+  if (ss.guess == kNoGuess) return;
+  uint32_t wlo, whi;
+  bucket_window(ss, wlo, whi);
+  const uint32_t nb = whi - wlo + 1;  // <= kMaxWindow
   const uint64_t k_old = composite(ss.kstar, (uint32_t)ss.istar);
   const int64_t s_lo = shard_start[s], s_hi = shard_start[s + 1];
-  if (threadIdx.x < 4) sh[threadIdx.x] = 0;
+  if (threadIdx.x <= kMaxWindow) sh[threadIdx.x] = 0;
   __syncthreads();
   const uint32_t cnt = cand_cnt[s];
   const uint2* c = cand + s_lo;
   for (uint32_t j = blockIdx.x * blockDim.x + threadIdx.x; j < cnt; j += gridDim.x * blockDim.x) {
     const uint2 v = __ldg(c + j);
-    const uint32_t b = (v.x >> 19) - wlo;  // in [0, 3) for staged candidates
-    if (b < 3u) atomicAdd(&sh[b], 1u);
+    const uint32_t b = (v.x >> 19) - wlo;  // < nb for staged candidates
+    if (b < nb) atomicAdd(&sh[b], 1u);
     const int64_t t0 = (int64_t)(v.y / kTile) * kTile;
-    if (composite(v.x, v.y) >= k_old && t0 >= s_lo && t0 + kTile <= s_hi) atomicAdd(&sh[3], 1u);
+    if (composite(v.x, v.y) >= k_old && t0 >= s_lo && t0 + kTile <= s_hi)
+      atomicAdd(&sh[kMaxWindow], 1u);
   }
   __syncthreads();
   uint32_t* row = hist + (int64_t)s * kCBins0;
-  if (threadIdx.x < 3 && sh[threadIdx.x]) atomicAdd(row + wlo + threadIdx.x, sh[threadIdx.x]);
+  if (threadIdx.x < nb && wlo + threadIdx.x < (uint32_t)kCBins0 && sh[threadIdx.x])
+    atomicAdd(row + wlo + threadIdx.x, sh[threadIdx.x]);
   if (threadIdx.x == 0) {
-    // digits above guess + 1 exist only if guess + 2 <= 4095; below wlo only if guess >= 2
+    // digits above whi exist only if whi + 1 <= 4095; below wlo only if wlo >= 1
     const uint32_t a = blockIdx.x == 0 ? above_cnt[s] : 0u;
     const uint32_t n = (uint32_t)(s_hi - s_lo);
-    if (guess + 2 < (uint32_t)kCBins0) {
-      const uint32_t v = a - sh[3];
-      if (v) atomicAdd(row + guess + 2, v);
+    const uint32_t selc = sh[kMaxWindow];
+    if (whi + 1 < (uint32_t)kCBins0) {
+      const uint32_t v = a - selc;
+      if (v) atomicAdd(row + whi + 1, v);
     }
-    if (guess >= 2) {
-      const uint32_t v = (blockIdx.x == 0 ? n - cnt - a : 0u) + sh[3];
-      if (v) atomicAdd(row + guess - 2, v);
+    if (wlo >= 1) {
+      const uint32_t v = (blockIdx.x == 0 ? n - cnt - a : 0u) + selc;
+      if (v) atomicAdd(row + wlo - 1, v);
     }
   }
 }
@@ -535,10 +569,12 @@ cselect_kernel(const int64_t* __restrict__ shard_start, const int64_t* __restric
   for (int b = threadIdx.x; b < kCBins0; b += blockDim.x) row[b] = 0;
   if (threadIdx.x == 0) {
     if (PASS == 0) {
-      // candidates were staged for buckets within one of the previous
-      // refresh's; otherwise a collect pass gathers them
-      const bool hit = form != kSelFormRerun && st.guess != kNoGuess && sh_digit + 1 >= st.guess &&
-                       sh_digit <= st.guess + 1;
+      // candidates were staged for the buckets of bucket_window(); otherwise a
+      // collect pass gathers them
+      uint32_t wlo, whi;
+      bucket_window(st, wlo, whi);
+      const bool hit = form != kSelFormRerun && sh_digit >= wlo && sh_digit <= whi;
+      if (form != kSelFormRerun) st.guess_prev = st.guess;  // the trend of the next window
       if (!hit) {
         cand_cnt[s] = 0;
         if (form == kSelFormWarm) {

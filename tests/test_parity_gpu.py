@@ -163,6 +163,29 @@ def test_warm_refresh_bit_exact(cuda_device, case, P, W, s):
     opt.close()
 
 
+@pytest.mark.parametrize("rate", [1.12, 1.3, 0.85, 1.02])
+@pytest.mark.parametrize("P,W,s", [(70001, 5, 0.9), (300000, 32, 0.99)])
+def test_warm_refresh_trending_threshold(cuda_device, rate, P, W, s):
+    """First moments growing (or shrinking) by a steady factor per refresh,
+    as early in training: the staged window follows the thresholds' trend;
+    every refresh must still equal the oracle's mask."""
+    r = np.random.default_rng(P + W)
+    base = (r.standard_normal(P) * 1e-3).astype(np.float32)
+    params = torch.zeros(P, device=cuda_device)
+    opt = make_opt(params, W, s, torch.float32)
+    opt.step([torch.zeros(P, device=cuda_device) for _ in range(W)])
+    start, ks = O.layout(P, W, s)
+    for t in range(7):
+        mh = _drift((base * rate ** t).astype(np.float32), r, 0.01)
+        opt.m.copy_(torch.from_numpy(mh))
+        opt.refresh_mask()
+        torch.cuda.synchronize()
+        bits, idx = O.topk_mask(mh, start, ks)
+        assert np.array_equal(u32(opt.bits()), bits), t
+        assert np.array_equal(u32(opt.idx()), idx.view(np.uint32)), t
+    opt.close()
+
+
 # ------------------------------------------------------------ lag, checkpoint, host path
 def test_lag_step_uses_previous_refresh(cuda_device):
     P, W, s = 40000, 4, 0.9
