@@ -433,76 +433,75 @@ scan_add_kernel(uint32_t* __restrict__ base, int64_t n, const uint32_t* __restri
 }
 
 // ------------------------------------------------------------------ index
-// idx[rank] = i for every set bit, ranks ascending.
-// Sparse masks (under ~5% set): one warp per tile (eight tiles per block);
-// lane l owns bitmap words 2l and 2l + 1 and writes its few set positions
-// straight to their ranks.
-__global__ void __launch_bounds__(256)
-index_sparse_kernel(const uint32_t* __restrict__ bits, int64_t P, int64_t ntiles,
-                    const uint32_t* __restrict__ tile_base, uint32_t* __restrict__ idx) {
-  const int lane = threadIdx.x & 31;
-  const int64_t tile = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (tile >= ntiles) return;
-  const int64_t nwords = (P + 31) / 32;
-  const int64_t w0 = tile * kTileWords + 2 * lane;
-  uint32_t a = w0 < nwords ? __ldg(bits + w0) : 0u;
-  uint32_t b = w0 + 1 < nwords ? __ldg(bits + w0 + 1) : 0u;
-  const uint32_t c = __popc(a) + __popc(b);
-  uint32_t x = c;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  uint32_t* out = idx + __ldg(tile_base + tile) + (x - c);
-  const uint32_t ia = (uint32_t)(w0 * 32), ib = ia + 32;
-  while (a) {
-    *out++ = ia + (uint32_t)(__ffs(a) - 1);
-    a &= a - 1;
-  }
-  while (b) {
-    *out++ = ib + (uint32_t)(__ffs(b) - 1);
-    b &= b - 1;
-  }
-}
-
-// Denser masks: one warp per tile (four tiles per block); lane l writes its
-// set positions into the warp's shared-memory buffer at its exclusive offset,
-// then the warp copies the tile's contiguous run of indices out with
-// coalesced stores.
-__global__ void __launch_bounds__(128)
-index_dense_kernel(const uint32_t* __restrict__ bits, int64_t P, int64_t ntiles,
+// idx[rank] = i for every set bit, ranks ascending.  Persistent warps, one
+// 2048-parameter tile at a time (lane l owns bitmap words 2l and 2l + 1); the
+// next tile's words and rank base are loaded before the current tile's
+// indices are written, so a warp is not idle for a load round trip per tile.
+// STAGED (denser masks): lanes write their set positions into the warp's
+// shared-memory buffer at their exclusive offsets and the warp copies the
+// tile's contiguous run out with coalesced stores; otherwise (sparse masks)
+// each lane writes its few positions straight to their ranks.
+template <bool STAGED>
+__global__ void __launch_bounds__(STAGED ? 128 : 256)
+index_kernel(const uint32_t* __restrict__ bits, int64_t P, int64_t ntiles,
              const uint32_t* __restrict__ tile_base, uint32_t* __restrict__ idx) {
-  __shared__ uint32_t buf[4][kTile];
+  constexpr int kWarps = STAGED ? 4 : 8;  // staged: 8 KB of shared memory per warp
+  __shared__ uint32_t buf[STAGED ? kWarps : 1][STAGED ? kTile : 1];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t tile = (int64_t)blockIdx.x * 4 + warp;
-  if (tile >= ntiles) return;
   const int64_t nwords = (P + 31) / 32;
-  const int64_t w0 = tile * kTileWords + 2 * lane;
-  uint32_t a = w0 < nwords ? __ldg(bits + w0) : 0u;
-  uint32_t b = w0 + 1 < nwords ? __ldg(bits + w0 + 1) : 0u;
-  const uint32_t c = __popc(a) + __popc(b);
-  uint32_t x = c;
+  const int64_t stride = (int64_t)gridDim.x * kWarps;
+  int64_t tile = (int64_t)blockIdx.x * kWarps + warp;
+  if (tile >= ntiles) return;
+  auto load = [&](int64_t t, uint32_t& a, uint32_t& b, uint32_t& base) {
+    const int64_t w0 = t * kTileWords + 2 * lane;
+    a = w0 < nwords ? __ldg(bits + w0) : 0u;
+    b = w0 + 1 < nwords ? __ldg(bits + w0 + 1) : 0u;
+    base = __ldg(tile_base + t);
+  };
+  uint32_t a, b, base;
+  load(tile, a, b, base);
+  for (; tile < ntiles; tile += stride) {
+    uint32_t na = 0, nb = 0, nbase = 0;
+    if (tile + stride < ntiles) load(tile + stride, na, nb, nbase);
+    const uint32_t c = __popc(a) + __popc(b);
+    uint32_t x = c;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    const uint32_t ia = (uint32_t)((tile * kTileWords + 2 * lane) * 32), ib = ia + 32;
+    if (STAGED) {
+      const uint32_t total = __shfl_sync(0xffffffffu, x, 31);
+      uint32_t* sb = buf[warp];
+      uint32_t o = x - c;
+      while (a) {
+        sb[o++] = ia + (uint32_t)(__ffs(a) - 1);
+        a &= a - 1;
+      }
+      while (b) {
+        sb[o++] = ib + (uint32_t)(__ffs(b) - 1);
+        b &= b - 1;
+      }
+      __syncwarp();
+      uint32_t* out = idx + base;
+      for (uint32_t j = lane; j < total; j += 32) out[j] = sb[j];
+      __syncwarp();  // the buffer is rewritten for the next tile
+    } else {
+      uint32_t* out = idx + base + (x - c);
+      while (a) {
+        *out++ = ia + (uint32_t)(__ffs(a) - 1);
+        a &= a - 1;
+      }
+      while (b) {
+        *out++ = ib + (uint32_t)(__ffs(b) - 1);
+        b &= b - 1;
+      }
+    }
+    a = na;
+    b = nb;
+    base = nbase;
   }
-  const uint32_t total = __shfl_sync(0xffffffffu, x, 31);
-  uint32_t* sb = buf[warp];
-  uint32_t o = x - c;
-  const uint32_t ia = (uint32_t)(w0 * 32), ib = ia + 32;
-  while (a) {
-    sb[o++] = ia + (uint32_t)(__ffs(a) - 1);
-    a &= a - 1;
-  }
-  while (b) {
-    sb[o++] = ib + (uint32_t)(__ffs(b) - 1);
-    b &= b - 1;
-  }
-  __syncwarp();
-  uint32_t* out = idx + __ldg(tile_base + tile);
-  for (uint32_t j = lane; j < total; j += 32) out[j] = sb[j];
 }
 
 // Per-shard popcount of a bitmap plus the count of bits set past P (in
@@ -616,13 +615,26 @@ cudaError_t launch_scan(const uint32_t* tile_cnt, int64_t ntiles, uint32_t* tile
 cudaError_t launch_index(const uint32_t* bits, int64_t P, const uint32_t* tile_base,
                          uint32_t* idx, int64_t k, cudaStream_t st) {
   const int64_t ntiles = (P + kTile - 1) / kTile;
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+      sms = n;
+    else
+      sms = 148;
+  }
   // measured on GB300: direct stores win at 1% density, staged stores at 10%
-  if (k >= 0 && k * 20 < P)
-    index_sparse_kernel<<<(unsigned)((ntiles + 7) / 8), 256, 0, st>>>(bits, P, ntiles, tile_base,
-                                                                      idx);
+  const bool staged = !(k >= 0 && k * 20 < P);
+  // persistent: staged blocks (4 warps, 32 KB) 6 per SM, direct ones (8 warps) 8 per SM
+  const int warps = staged ? 4 : 8;
+  const int64_t want = (int64_t)sms * (staged ? 6 : 8);
+  const int64_t need = (ntiles + warps - 1) / warps;
+  const unsigned grid = (unsigned)(need < want ? need : want);
+  if (staged)
+    index_kernel<true><<<grid, 128, 0, st>>>(bits, P, ntiles, tile_base, idx);
   else
-    index_dense_kernel<<<(unsigned)((ntiles + 3) / 4), 128, 0, st>>>(bits, P, ntiles, tile_base,
-                                                                     idx);
+    index_kernel<false><<<grid, 256, 0, st>>>(bits, P, ntiles, tile_base, idx);
   return cudaGetLastError();
 }
 

@@ -277,7 +277,14 @@ spec_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __rest
     if (!any) return;
   }
   uint2* const col = lbuf[warp] + lane;  // this lane's column: slot j at col[32 * j]
+  const uint32_t col_s = (uint32_t)__cvta_generic_to_shared(col);
   uint32_t nl = 0;                       // this lane's staged candidates
+  // append (key, i) to this lane's column: a 32-bit shared-memory address
+  auto put = [&](uint32_t key, uint32_t i) {
+    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(col_s + 256u * nl), "r"(key), "r"(i)
+                 : "memory");
+    ++nl;
+  };
 
   // place every lane's column in the shard's candidate range
   auto flush_lanes = [&](int shard) {
@@ -319,7 +326,7 @@ spec_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __rest
           if (i < b) {
             const uint32_t key = magnitude_key(__ldcs(m + i));
             acount += key >= top_key ? 1u : 0u;
-            if (key - wkey_lo < wkey_n) col[32 * nl++] = make_uint2(key, i);
+            if (key - wkey_lo < wkey_n) put(key, i);
           }
           if (__any_sync(0xffffffffu, nl == kLaneSlots)) flush_lanes(s);
         }
@@ -351,13 +358,22 @@ spec_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __rest
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             uint32_t wd[4];
+            if (!mixed) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const uint32_t key = magnitude_key(xc[4 * h + q]);
-              const uint32_t tq =
-                  mixed ? kstar + (uint32_t)(1024 * h + 128 * warp + 32 * q + lane > lim) : thr;
-              wd[q] = __ballot_sync(0xffffffffu, key >= tq);
-              if (key - wkey_lo < wkey_n) col[32 * nl++] = make_uint2(key, ibase + 1024 * h + 32 * q);
+              for (int q = 0; q < 4; ++q) {
+                const uint32_t key = magnitude_key(xc[4 * h + q]);
+                wd[q] = __ballot_sync(0xffffffffu, key >= thr);
+                if (key - wkey_lo < wkey_n) put(key, ibase + 1024 * h + 32 * q);
+              }
+            } else {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const uint32_t key = magnitude_key(xc[4 * h + q]);
+                wd[q] = __ballot_sync(
+                    0xffffffffu,
+                    key >= kstar + (uint32_t)(1024 * h + 128 * warp + 32 * q + lane > lim));
+                if (key - wkey_lo < wkey_n) put(key, ibase + 1024 * h + 32 * q);
+              }
             }
             if (lane == 0) {
               *reinterpret_cast<uint4*>(bw + 32 * h) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
