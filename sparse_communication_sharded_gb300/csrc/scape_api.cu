@@ -53,7 +53,7 @@ struct scape {
   // workspace offsets (bytes)
   size_t off_bits = 0, off_idx = 0, off_tbase = 0, off_tcnt = 0, off_pack = 0, off_gbar = 0,
          off_hist = 0, off_sel = 0, off_cand = 0, off_ccnt = 0, off_scan = 0, off_sstart = 0,
-         off_sk = 0, off_counts = 0,
+         off_sk = 0, off_counts = 0, off_nar = 0,
          ws_need = 0;
   // bound memory
   bool bound = false;
@@ -102,6 +102,8 @@ struct scape {
   uint2* cand() const { return at<uint2>(off_cand); }
   uint32_t* cand_cnt() const { return at<uint32_t>(off_ccnt); }
   uint32_t* above_cnt() const { return at<uint32_t>(off_ccnt) + W; }
+  uint32_t* nar_cnt() const { return at<uint32_t>(off_ccnt) + 2 * W; }
+  uint2* nar() const { return at<uint2>(off_nar); }
   uint32_t* scan_scratch() const { return at<uint32_t>(off_scan); }
   int64_t* d_shard_start() const { return at<int64_t>(off_sstart); }
   int64_t* d_shard_k() const { return at<int64_t>(off_sk); }
@@ -378,7 +380,8 @@ int scape_create(scape_t** out, int n_layers, const int64_t* host_layer_numel, i
   h->off_sel = carve((size_t)W * sizeof(ShardSel));
   // candidates of shard s live in [shard_start[s], shard_start[s+1]): capacity = shard size
   h->off_cand = carve((size_t)P * sizeof(uint2));
-  h->off_ccnt = carve((size_t)W * 2 * 4);  // candidate counts, then counts above the window
+  h->off_ccnt = carve((size_t)W * 3 * 4);  // candidate, above-window and narrow-row counts
+  h->off_nar = carve((size_t)W * kNarrowCap * sizeof(uint2));
   h->off_scan = carve((size_t)scan_scratch_words(h->ntiles) * 4);
   h->off_sstart = carve((size_t)(W + 1) * 8);
   h->off_sk = carve((size_t)W * 8);
@@ -527,7 +530,7 @@ int enqueue_radix(scape_t* h, cudaStream_t st) {
   for (int pass = 1; pass <= 5; ++pass) {
     int rc = run_kernel(h, kKCandHist, st, [&] {
       return launch_chist(pass, h->W, h->cand_blocks, h->d_shard_start(), h->sel(), h->cand(),
-                          h->cand_cnt(), h->hist(), st);
+                          h->cand_cnt(), h->hist(), h->nar(), h->nar_cnt(), kNarrowCap, st);
     });
     if (rc) return rc;
     rc = run_kernel(h, kKCandSelect, st, [&] {
@@ -545,7 +548,7 @@ int refresh_cold(scape_t* h, cudaStream_t st) {
   int rc;
   if (!h->all_dense) {
     cudaError_t e = cudaMemsetAsync(h->hist(), 0, (size_t)h->W * kCandBins0 * 4, st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(h->cand_cnt(), 0, (size_t)h->W * 2 * 4, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->cand_cnt(), 0, (size_t)h->W * 3 * 4, st);
     if (e != cudaSuccess) return cuda_fail(h, e, "scape_refresh_mask: histogram clear");
     rc = run_kernel(h, kKCandHist0, st, [&] {
       return launch_chist0(h->m, h->P, h->W, h->d_shard_start(), h->sel(), h->hist(), h->cand(),
@@ -580,7 +583,7 @@ int refresh_cold(scape_t* h, cudaStream_t st) {
 // bucket window) return at once when no shard needs them.
 int refresh_warm(scape_t* h, cudaStream_t st) {
   cudaError_t e = cudaMemsetAsync(h->hist(), 0, (size_t)h->W * kCandBins0 * 4, st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(h->cand_cnt(), 0, (size_t)h->W * 2 * 4, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(h->cand_cnt(), 0, (size_t)h->W * 3 * 4, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(h->tile_cnt(), 0, (size_t)h->ntiles * 4, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "scape_refresh_mask: count clear");
   int rc = run_kernel(h, kKSpecMark, st, [&] {
@@ -841,7 +844,8 @@ int scape_union_step(scape_t* h, const void* const* host_grad_ptrs, void* worksp
       if (rc) return rc;
       for (int pass = 1; pass <= 5; ++pass) {
         rc = run_kernel(h, kKCandHist, st, [&] {
-          return launch_chist(pass, 1, 1200, ustart, sw, ucand, ucnt, uhist, st);
+          return launch_chist(pass, 1, 1200, ustart, sw, ucand, ucnt, uhist, nullptr, nullptr, 0,
+                              st);
         });
         if (rc) return rc;
         rc = run_kernel(h, kKCandSelect, st,

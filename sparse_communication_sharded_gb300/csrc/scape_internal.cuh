@@ -287,9 +287,13 @@ cudaError_t launch_cselect(int pass, int W, const int64_t* shard_start, const in
                            cudaStream_t st);
 cudaError_t launch_collect(const float* m, int64_t P, int W, const int64_t* shard_start,
                            const ShardSel* sel, uint2* cand, uint32_t* cand_cnt, cudaStream_t st);
+// nar (optional): per-shard rows of nar_cap candidates, counts in nar_cnt
+// (zeroed before pass 2): pass 2 narrows the list there for passes 3 to 5.
+constexpr uint32_t kNarrowCap = 4096;
 cudaError_t launch_chist(int pass, int W, int blocks_per_shard, const int64_t* shard_start,
                          const ShardSel* sel, const uint2* cand, const uint32_t* cand_cnt,
-                         uint32_t* hist, cudaStream_t st);
+                         uint32_t* hist, uint2* nar, uint32_t* nar_cnt, uint32_t nar_cap,
+                         cudaStream_t st);
 cudaError_t launch_shard_count(const uint32_t* bits, int64_t P, int64_t nwords, int W,
                                uint32_t* counts, cudaStream_t st);
 

@@ -618,11 +618,17 @@ cselect_kernel(const int64_t* __restrict__ shard_start, const int64_t* __restric
 // ------------------------------------------------------------------ chist 1..5
 // grid (G, W): blocks of shard s stride over its candidates, histogramming the
 // pass's digit of the composite key among those matching the prefix.
+// With a narrow list (nar != nullptr): pass 2 also appends the candidates
+// that match the 23-bit prefix -- the only ones passes 3 to 5 look at -- to
+// the shard's row of `nar` (capacity nar_cap, count in nar_cnt[s]); passes 3
+// to 5 then read that short row instead of the whole window list, unless it
+// overflowed.
 template <int PASS>
 __global__ void __launch_bounds__(256)
 chist_kernel(const int64_t* __restrict__ shard_start, const ShardSel* __restrict__ sel,
              const uint2* __restrict__ cand, const uint32_t* __restrict__ cand_cnt,
-             uint32_t* __restrict__ hist) {
+             uint32_t* __restrict__ hist, uint2* __restrict__ nar, uint32_t* __restrict__ nar_cnt,
+             uint32_t nar_cap) {
   constexpr int WID = PASS == 5 ? 7 : 11;
   constexpr int NB = 1 << WID;
   constexpr int SHIFT = PASS == 1 ? 40 : PASS == 2 ? 29 : PASS == 3 ? 18 : PASS == 4 ? 7 : 0;
@@ -630,14 +636,28 @@ chist_kernel(const int64_t* __restrict__ shard_start, const ShardSel* __restrict
   const int s = blockIdx.y;
   if (sel[s].mode != kSelSearch) return;
   const uint64_t prefix = sel[s].cprefix;
-  const uint32_t cnt = cand_cnt[s];
+  uint32_t cnt = cand_cnt[s];
   const uint2* c = cand + shard_start[s];
+  uint2* const row2 = nar ? nar + (int64_t)s * nar_cap : nullptr;
+  if (PASS >= 3 && nar) {
+    const uint32_t n2 = nar_cnt[s];
+    if (n2 <= nar_cap) {
+      cnt = n2;
+      c = row2;
+    }
+  }
   for (int b = threadIdx.x; b < NB; b += blockDim.x) sh[b] = 0;
   __syncthreads();
   for (uint32_t j = blockIdx.x * blockDim.x + threadIdx.x; j < cnt; j += gridDim.x * blockDim.x) {
     const uint2 v = __ldg(c + j);
     const uint64_t comp = composite(v.x, v.y);
-    if ((comp >> (SHIFT + WID)) == prefix) atomicAdd(&sh[(uint32_t)(comp >> SHIFT) & (NB - 1)], 1u);
+    if ((comp >> (SHIFT + WID)) == prefix) {
+      atomicAdd(&sh[(uint32_t)(comp >> SHIFT) & (NB - 1)], 1u);
+      if (PASS == 2 && nar) {
+        const uint32_t at = atomicAdd(nar_cnt + s, 1u);
+        if (at < nar_cap) row2[at] = v;
+      }
+    }
   }
   __syncthreads();
   uint32_t* row = hist + (int64_t)s * kCBins0;
@@ -728,14 +748,15 @@ cudaError_t launch_cselect(int pass, int W, const int64_t* shard_start, const in
 
 cudaError_t launch_chist(int pass, int W, int blocks_per_shard, const int64_t* shard_start,
                          const ShardSel* sel, const uint2* cand, const uint32_t* cand_cnt,
-                         uint32_t* hist, cudaStream_t st) {
+                         uint32_t* hist, uint2* nar, uint32_t* nar_cnt, uint32_t nar_cap,
+                         cudaStream_t st) {
   dim3 grid((unsigned)blocks_per_shard, (unsigned)W);
   switch (pass) {
-    case 1: chist_kernel<1><<<grid, 256, 0, st>>>(shard_start, sel, cand, cand_cnt, hist); break;
-    case 2: chist_kernel<2><<<grid, 256, 0, st>>>(shard_start, sel, cand, cand_cnt, hist); break;
-    case 3: chist_kernel<3><<<grid, 256, 0, st>>>(shard_start, sel, cand, cand_cnt, hist); break;
-    case 4: chist_kernel<4><<<grid, 256, 0, st>>>(shard_start, sel, cand, cand_cnt, hist); break;
-    default: chist_kernel<5><<<grid, 256, 0, st>>>(shard_start, sel, cand, cand_cnt, hist); break;
+    case 1: chist_kernel<1><<<grid, 256, 0, st>>>(shard_start, sel, cand, cand_cnt, hist, nar, nar_cnt, nar_cap); break;
+    case 2: chist_kernel<2><<<grid, 256, 0, st>>>(shard_start, sel, cand, cand_cnt, hist, nar, nar_cnt, nar_cap); break;
+    case 3: chist_kernel<3><<<grid, 256, 0, st>>>(shard_start, sel, cand, cand_cnt, hist, nar, nar_cnt, nar_cap); break;
+    case 4: chist_kernel<4><<<grid, 256, 0, st>>>(shard_start, sel, cand, cand_cnt, hist, nar, nar_cnt, nar_cap); break;
+    default: chist_kernel<5><<<grid, 256, 0, st>>>(shard_start, sel, cand, cand_cnt, hist, nar, nar_cnt, nar_cap); break;
   }
   return cudaGetLastError();
 }
