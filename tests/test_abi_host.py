@@ -118,3 +118,31 @@ def test_kernel_names(lib):
     names = [C.scape_kernel_name(i) for i in range(C.SCAPE_NUM_KERNELS)]
     assert len(set(names)) == C.SCAPE_NUM_KERNELS and all(names)
     assert C.scape_kernel_name(C.SCAPE_NUM_KERNELS) == ""
+
+
+def test_missing_library_fails_loudly(lib, monkeypatch):
+    monkeypatch.setattr(C, "_lib", None)
+    with pytest.raises(ImportError):
+        C.load("/nonexistent/libscape.so")
+
+
+def test_fusion_and_staging_validate_without_gpu(lib):
+    h = _create(P=10000, W=8)
+    for level in (C.FUSE_NONE, C.FUSE_SUM, C.FUSE_UPDATE):
+        C.scape_set_fusion(h, level)
+    with pytest.raises(C.ScapeError) as ei:
+        C.scape_set_fusion(h, 3)
+    assert ei.value.code == C.SCAPE_EINVAL
+    # rows are P rounded up to 64 floats
+    assert C.scape_residual_staging_bytes(h, 3) == 3 * 10048 * 4
+    with pytest.raises(C.ScapeError):
+        C.scape_residual_staging_bytes(h, 2)
+    with pytest.raises(C.ScapeError) as ei:        # fewer than three rows
+        C.scape_set_residual_staging(h, 4096, 2 * 10048 * 4)
+    assert ei.value.code == C.SCAPE_EINVAL
+    with pytest.raises(C.ScapeError) as ei:        # misaligned
+        C.scape_set_residual_staging(h, 4100, 3 * 10048 * 4)
+    assert ei.value.code == C.SCAPE_EINVAL
+    C.scape_set_residual_staging(h, 4096, 5 * 10048 * 4)
+    C.scape_set_residual_staging(h, None, 0)       # back to in place
+    C.scape_destroy(h)
