@@ -395,6 +395,9 @@ def test_profiling_counts_launches(cuda_device):
     ("gpt345m", 3, (0, 7)),
     ("llama500m", 3, (0, 17, 31)),
     ("llama1p8b", 2, (3,)),
+    # ten steps at full size: eight warm refreshes, each mask used by the next step
+    ("gpt345m", 10, (3,)),
+    ("llama500m", 10, (5,)),
 ])
 def test_full_size_sampled_shards(cuda_device, name, steps, shards):
     wl = synth.WORKLOADS[name]
