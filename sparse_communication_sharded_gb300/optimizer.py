@@ -42,7 +42,12 @@ class Scape:
         self.params = params
         self.m = torch.zeros(P, dtype=torch.float32, device=dev)
         if residuals == "device":
-            self.e = [torch.zeros(P, dtype=torch.float32, device=dev) for _ in range(W)]
+            # one allocation for all W residuals, rows 256-byte aligned: measured
+            # faster for the compaction than W separate allocations (26.5 vs
+            # 27.3 ms on the Llama-500M shape)
+            stride = (P + 63) // 64 * 64
+            self._e_storage = torch.zeros(W * stride, dtype=torch.float32, device=dev)
+            self.e = [self._e_storage[w * stride:w * stride + P] for w in range(W)]
         elif residuals == "host":
             self.e = [torch.zeros(P, dtype=torch.float32).pin_memory() for _ in range(W)]
         else:
