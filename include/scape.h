@@ -311,6 +311,10 @@ int scape_step_host(scape_t *h, const void *const *host_grads_src,
  */
 #define SCAPE_NUM_KERNELS 22
 int scape_profile_enable(scape_t *h, int on);
+/* Which kernels profiling brackets: bit i for kernel i (default: all).  Two
+ * event records per launch cost the GPU a few microseconds; a timing run can
+ * keep them to the kernels it reports. */
+int scape_profile_select(scape_t *h, uint32_t kernel_mask);
 int scape_profile_collect(scape_t *h);
 int scape_profile_read(const scape_t *h, double *host_ms, int64_t *host_launches);
 int scape_profile_reset(scape_t *h);

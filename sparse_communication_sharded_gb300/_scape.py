@@ -58,6 +58,7 @@ _PROTOS = {
     "scape_set_state": (_i32, [_vp, _i64, _vp, _vp]),
     "scape_step_host": (_i32, [_vp, _vp, _vp, _vp, _vp]),
     "scape_profile_enable": (_i32, [_vp, _i32]),
+    "scape_profile_select": (_i32, [_vp, ctypes.c_uint32]),
     "scape_profile_collect": (_i32, [_vp]),
     "scape_profile_read": (_i32, [_vp, _vp, _vp]),
     "scape_profile_reset": (_i32, [_vp]),
@@ -233,6 +234,18 @@ def scape_step_host(h, host_src_ptrs, dev_grad_ptrs, host_params_out_ptr, stream
 
 def scape_profile_enable(h, on=True):
     _check(h, load().scape_profile_enable(h, 1 if on else 0))
+
+
+def scape_profile_select(h, names_or_mask):
+    """Profile only some kernels: a bit mask, or an iterable of kernel names."""
+    if isinstance(names_or_mask, int):
+        mask = names_or_mask
+    else:
+        ids = {scape_kernel_name(i): i for i in range(SCAPE_NUM_KERNELS)}
+        mask = 0
+        for n in names_or_mask:
+            mask |= 1 << ids[n]
+    _check(h, load().scape_profile_select(h, mask & 0xFFFFFFFF))
 
 
 def scape_profile_collect(h):

@@ -83,6 +83,7 @@ struct scape {
   std::vector<cudaEvent_t> ev_in, ev_comp, ev_out;  // per worker group
   // profiling
   bool prof = false;
+  uint32_t prof_mask = 0xFFFFFFFFu;  // kernels whose launches are bracketed by events
   std::vector<ProfRec> pending;
   std::vector<cudaEvent_t> pool;
   double prof_ms[kNumKernels] = {};
@@ -137,14 +138,15 @@ cudaEvent_t take_event(scape_t* h) {
 template <class F>
 int run_kernel(scape_t* h, int kid, cudaStream_t st, F&& fn, int nlaunch = 1) {
   cudaEvent_t a = nullptr, b = nullptr;
-  if (h->prof) {
+  const bool timed = h->prof && ((h->prof_mask >> kid) & 1u);
+  if (timed) {
     a = take_event(h);
     b = take_event(h);
     if (a && b) cudaEventRecord(a, st);
   }
   const cudaError_t e = fn();
   h->launches += nlaunch;
-  if (h->prof && a && b) {
+  if (timed && a && b) {
     cudaEventRecord(b, st);
     h->pending.push_back({kid, nlaunch, a, b});
   }
@@ -1066,6 +1068,12 @@ int scape_step_host(scape_t* h, const void* const* host_grads_src, void* const* 
 int scape_profile_enable(scape_t* h, int on) {
   if (!h) return SCAPE_EINVAL;
   h->prof = on != 0;
+  return SCAPE_OK;
+}
+
+int scape_profile_select(scape_t* h, uint32_t kernel_mask) {
+  if (!h) return SCAPE_EINVAL;
+  h->prof_mask = kernel_mask;
   return SCAPE_OK;
 }
 

@@ -155,6 +155,10 @@ class Scape:
     def profile(self, on=True):
         C.scape_profile_enable(self.h, on)
 
+    def profile_select(self, names_or_mask):
+        """Bracket only these kernels (names or a bit mask) while profiling."""
+        C.scape_profile_select(self.h, names_or_mask)
+
     def profile_collect(self):
         C.scape_profile_collect(self.h)
 

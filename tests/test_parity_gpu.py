@@ -387,6 +387,15 @@ def test_profiling_counts_launches(cuda_device):
         assert (prof["reduce"][1], prof["adams_sparse"][1]) == (n_red, n_upd), level
     with pytest.raises(ScapeError):
         opt.set_fusion(3)
+    # profiling restricted to one kernel brackets only its launches
+    opt.profile_select(["ef_compact"])
+    opt.profile_reset()
+    opt.step(g)
+    opt.refresh_mask()
+    torch.cuda.synchronize()
+    opt.profile_collect()
+    prof = opt.profile_read()
+    assert {k for k, (_, n) in prof.items() if n} == {"ef_compact"}
     opt.close()
 
 
