@@ -1,21 +1,28 @@
-// refresh_kernels.cu -- partitioned top-k mask refresh of the SCAPE step.
+// refresh_kernels.cu -- partitioned top-k mask refresh of the SCAPE step:
+// bitmap, rank table and index list.
 //
 // For every optimizer shard s independently ("Sintesi Tecnica: SCAPE" Sec. 2,
-// partitioned mask synchronisation), select the k_s parameters with the
-// largest first-moment magnitude (key = bits(m) & 0x7FFFFFFF, so the order of
-// the keys as unsigned integers is the order of |m|), equal keys going to the
-// lower index.  The selection is an exact radix select:
+// partitioned mask synchronisation), the k_s parameters with the largest
+// first-moment magnitude (key = bits(m) & 0x7FFFFFFF, so the order of the keys
+// as unsigned integers is the order of |m|) are selected, equal keys going to
+// the lower index.  The threshold (kstar, istar) comes from the candidate
+// select of topk_kernels.cu; this file holds
+//   mark      the bitmap elementwise, bit_i = key_i > kstar || (key_i == kstar
+//             && i <= istar), with per-tile popcounts (or, in accumulate mode,
+//             OR-ed into an existing bitmap) -- the first refresh, and the
+//             union baseline;
+//   remark    the same for the tiles a warm refresh's speculative bitmap does
+//             not cover;
+//   scan      per-tile counts -> rank table; index the ascending index list;
+//   shard_count / tile_count   counts of a restored bitmap.
+// It also keeps an exact select that works on m alone, for the allocation-free
+// entry point (scape_static.cu), whose scratch cannot hold a candidate list:
 //   hist<0>/select<0>   11-bit digit 30..20 of every key of the shard
 //   hist<1>/select<1>   11-bit digit 19..9 of the keys matching the prefix
 //   hist<2>/select<2>    9-bit digit  8..0 of the keys matching the prefix
-// which fixes the threshold key kstar and how many keys equal to it are
-// selected (need).  When fewer than all equal keys are selected, tie_count and
-// tie_select find the index istar of the need-th equal key in index order.
-// The mark kernel then writes the bitmap elementwise
-//   bit_i = key_i > kstar  ||  (key_i == kstar && i <= istar)
-// with per-tile popcounts (or, in accumulate mode, ORs it into an existing
-// bitmap); scan turns per-tile counts into the rank table, and index writes
-// the ascending packed index list.
+// fix kstar and how many keys equal to it are selected (need); when fewer than
+// all equal keys are selected, tie_count and tie_select find the index istar of
+// the need-th equal key in index order.
 #include "scape_internal.cuh"
 
 namespace scapek {

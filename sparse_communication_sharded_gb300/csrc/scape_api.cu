@@ -2,8 +2,9 @@
 //
 // Holds the shard layout, the caller-bound device pointers, the step count and
 // the carve-up of the caller's workspace; enqueues the kernels of
-// step_kernels.cu and refresh_kernels.cu on the caller's stream.  Never
-// allocates device memory.
+// step_kernels.cu, topk_kernels.cu, refresh_kernels.cu and union_kernels.cu on
+// the caller's stream (plus internal copy streams for the host-memory paths).
+// Never allocates device memory.
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -584,8 +585,10 @@ int refresh_cold(scape_t* h, cudaStream_t st) {
 // holds; the kernels for the rare cases (a shard whose threshold left its
 // bucket window) return at once when no shard needs them.
 int refresh_warm(scape_t* h, cudaStream_t st) {
-  cudaError_t e = cudaMemsetAsync(h->hist(), 0, (size_t)h->W * kCandBins0 * 4, st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(h->cand_cnt(), 0, (size_t)h->W * 3 * 4, st);
+  // the histogram rows need no clearing: every refresh leaves them zero (each
+  // select pass clears the rows it read, and rows of shards no pass reads are
+  // never written); the cold refresh after a bind clears them once
+  cudaError_t e = cudaMemsetAsync(h->cand_cnt(), 0, (size_t)h->W * 3 * 4, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(h->tile_cnt(), 0, (size_t)h->ntiles * 4, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "scape_refresh_mask: count clear");
   int rc = run_kernel(h, kKSpecMark, st, [&] {
