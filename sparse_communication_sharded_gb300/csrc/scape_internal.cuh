@@ -252,7 +252,12 @@ constexpr int kScanLaunches = 3;
 cudaError_t launch_index(const uint32_t* bits, int64_t P, const uint32_t* tile_base,
                          uint32_t* idx, int64_t k, cudaStream_t st);
 // candidate-based exact top-k threshold (topk_kernels.cu)
-constexpr int kCandBins0 = 4096;
+// First digit of the candidate select: the top kDigit0 bits of the 31-bit
+// magnitude key (8 exponent bits + 5 mantissa bits: buckets 1/32 of an octave
+// wide), key >> kKeyShift0.
+constexpr int kDigit0 = 13;
+constexpr int kKeyShift0 = 31 - kDigit0;
+constexpr int kCandBins0 = 1 << kDigit0;
 // selective: only shards flagged kSelNeedHist, and nothing staged.
 cudaError_t launch_chist0(const float* m, int64_t P, int W, const int64_t* shard_start,
                           const ShardSel* sel, uint32_t* hist, uint2* cand, uint32_t* cand_cnt,

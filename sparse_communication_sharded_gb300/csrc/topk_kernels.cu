@@ -9,14 +9,14 @@
 // shard fixes the selection exactly: i is selected iff comp(i) >= kstar64.
 //
 // Cold refresh (no usable previous threshold):
-//   chist0    one read of m: per-shard histogram of composite bits 62..51
-//             (the top 12 bits of |m|); stages candidates near last step's
+//   chist0    one read of m: per-shard histogram of composite bits 62..50
+//             (the top 13 bits of |m|); stages candidates near last step's
 //             bucket
 //   cselect0  per shard: the bucket holding the k_s-th largest key
 //   collect   second read of m, only for shards whose bucket moved: (key,
 //             index) of every parameter in that bucket
 //   chist/cselect 1..5   radix passes over the candidates only, digits
-//             50..40, 39..29, 28..18, 17..7, 6..0 of the composite key
+//             49..39, 38..28, 27..17, 16..6, 5..0 of the composite key
 //   then the mark kernel writes the bitmap from (kstar, istar):
 //             bit_i = key_i > kstar || (key_i == kstar && i <= istar).
 // Warm refresh (every later one): the one read of m (spec) writes the bitmap
@@ -32,7 +32,7 @@
 namespace scapek {
 namespace {
 
-constexpr int kCBins0 = kCandBins0;  // 12-bit first digit
+constexpr int kCBins0 = kCandBins0;  // first digit: key >> kKeyShift0
 
 __device__ __forceinline__ uint64_t composite(uint32_t key, uint32_t i) {
   return ((uint64_t)key << 32) | (uint64_t)(0xFFFFFFFFu - i);
@@ -44,7 +44,7 @@ __device__ __forceinline__ uint64_t composite(uint32_t key, uint32_t i) {
 // because early in training the first moments grow from step to step and the
 // threshold drifts the same way.  hi may be 4096 (no such digit).  With no
 // previous bucket the window is empty (lo > hi).
-constexpr int kMaxTrend = 3;
+constexpr int kMaxTrend = 6;
 constexpr int kMaxWindow = 2 * 1 + kMaxTrend + 1;  // buckets in the widest window
 
 __device__ __forceinline__ void bucket_window(const ShardSel& q, uint32_t& lo, uint32_t& hi) {
@@ -71,7 +71,7 @@ __device__ __forceinline__ void bucket_window(const ShardSel& q, uint32_t& lo, u
 // walks a contiguous run of 2048-parameter segments (the mark tiles),
 // following the shard boundaries incrementally, so it meets at most a few of
 // them.  Per shard piece it
-//   HIST:    adds the 12-bit first digit of every key to a shared-memory
+//   HIST:    adds the 13-bit first digit of every key to a shared-memory
 //            histogram (flushed to the shard's row when the shard changes), and
 //            stages candidates whose digit lies within one bucket of the
 //            previous refresh's bucket (`guess`).  `selective`: only shards
@@ -82,7 +82,7 @@ __device__ __forceinline__ void bucket_window(const ShardSel& q, uint32_t& lo, u
 // append) and flushes it to the shard's range of `cand` with one global
 // atomic, so segments need no block-wide barrier.
 constexpr int kMSeg = 2048;       // parameters per segment (256 threads x 2 x float4)
-constexpr int kWarpStage = 384;   // staged candidates per warp
+constexpr int kWarpStage = 256;   // staged candidates per warp (48 KB of shared memory with the histogram)
 constexpr int kMHist = 0, kMCollect = 1;
 static_assert(kMSeg == kTile, "a segment is one mark tile");
 
@@ -184,7 +184,7 @@ mpass_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __res
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const uint32_t key = magnitude_key(x[q]);
-              const uint32_t d = key >> 19;
+              const uint32_t d = key >> kKeyShift0;
               if (HIST) atomicAdd(&sh[d], 1u);
               const bool hit = d - wlo <= wwid;
               const uint32_t ball = __ballot_sync(0xffffffffu, hit);
@@ -201,7 +201,7 @@ mpass_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __res
             const int64_t i = b0 + threadIdx.x;
             const bool in = i < hi;
             const uint32_t key = in ? magnitude_key(__ldcs(m + i)) : 0u;
-            const uint32_t d = key >> 19;
+            const uint32_t d = key >> kKeyShift0;
             if (HIST && in) atomicAdd(&sh[d], 1u);
             const bool hit = in && d - wlo <= wwid;
             const uint32_t ball = __ballot_sync(0xffffffffu, hit);
@@ -312,9 +312,9 @@ spec_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __rest
     if (ss.guess != kNoGuess) {
       uint32_t wlo, whi;
       bucket_window(ss, wlo, whi);
-      const uint32_t wkey_lo = wlo << 19;                   // window: key - wkey_lo < wkey_n
-      const uint32_t wkey_n = (whi + 1 - wlo) << 19;
-      const uint32_t top_key = (whi + 1) << 19;             // keys >= top_key: above it
+      const uint32_t wkey_lo = wlo << kKeyShift0;           // window: key - wkey_lo < wkey_n
+      const uint32_t wkey_n = (whi + 1 - wlo) << kKeyShift0;
+      const uint32_t top_key = (whi + 1) << kKeyShift0;     // keys >= top_key: above it
       const uint32_t kstar = ss.kstar;
       const uint32_t istar = (uint32_t)ss.istar;
       uint32_t acount = 0;  // this thread's share of above_cnt[s]
@@ -430,7 +430,7 @@ whist_kernel(const int64_t* __restrict__ shard_start, const ShardSel* __restrict
   const uint2* c = cand + s_lo;
   for (uint32_t j = blockIdx.x * blockDim.x + threadIdx.x; j < cnt; j += gridDim.x * blockDim.x) {
     const uint2 v = __ldg(c + j);
-    const uint32_t b = (v.x >> 19) - wlo;  // < nb for staged candidates
+    const uint32_t b = (v.x >> kKeyShift0) - wlo;  // < nb for staged candidates
     if (b < nb) atomicAdd(&sh[b], 1u);
     const int64_t t0 = (int64_t)(v.y / kTile) * kTile;
     if (composite(v.x, v.y) >= k_old && t0 >= s_lo && t0 + kTile <= s_hi)
@@ -441,7 +441,7 @@ whist_kernel(const int64_t* __restrict__ shard_start, const ShardSel* __restrict
   if (threadIdx.x < nb && wlo + threadIdx.x < (uint32_t)kCBins0 && sh[threadIdx.x])
     atomicAdd(row + wlo + threadIdx.x, sh[threadIdx.x]);
   if (threadIdx.x == 0) {
-    // digits above whi exist only if whi + 1 <= 4095; below wlo only if wlo >= 1
+    // digits above whi exist only if whi + 1 < kCBins0; below wlo only if wlo >= 1
     const uint32_t a = blockIdx.x == 0 ? above_cnt[s] : 0u;
     const uint32_t n = (uint32_t)(s_hi - s_lo);
     const uint32_t selc = sh[kMaxWindow];
@@ -505,7 +505,7 @@ __global__ void __launch_bounds__(256)
 cselect_kernel(const int64_t* __restrict__ shard_start, const int64_t* __restrict__ shard_k,
                ShardSel* __restrict__ sel, uint32_t* __restrict__ hist,
                uint32_t* __restrict__ cand_cnt, int form) {
-  constexpr int WID = PASS == 0 ? 12 : (PASS == 5 ? 7 : 11);
+  constexpr int WID = PASS == 0 ? kDigit0 : (PASS == 5 ? 63 - kDigit0 - 44 : 11);
   constexpr int NB = 1 << WID;
   constexpr int PER = NB >= 256 ? NB / 256 : 1;
   __shared__ uint32_t warp_tot[8];
@@ -606,7 +606,7 @@ cselect_kernel(const int64_t* __restrict__ shard_start, const int64_t* __restric
     st.krem -= sh_above;
     if (PASS == 5) {
       // the composite of the k_s-th largest parameter of the shard
-      st.guess = (uint32_t)(st.cprefix >> 51);
+      st.guess = (uint32_t)(st.cprefix >> (63 - kDigit0));
       st.kstar = (uint32_t)(st.cprefix >> 32);
       st.istar = (int64_t)(0xFFFFFFFFu - (uint32_t)(st.cprefix & 0xFFFFFFFFu));
       st.mode = kSelDone;
@@ -619,7 +619,7 @@ cselect_kernel(const int64_t* __restrict__ shard_start, const int64_t* __restric
 // grid (G, W): blocks of shard s stride over its candidates, histogramming the
 // pass's digit of the composite key among those matching the prefix.
 // With a narrow list (nar != nullptr): pass 2 also appends the candidates
-// that match the 23-bit prefix -- the only ones passes 3 to 5 look at -- to
+// that match the 24-bit prefix -- the only ones passes 3 to 5 look at -- to
 // the shard's row of `nar` (capacity nar_cap, count in nar_cnt[s]); passes 3
 // to 5 then read that short row instead of the whole window list, unless it
 // overflowed.
@@ -629,9 +629,9 @@ chist_kernel(const int64_t* __restrict__ shard_start, const ShardSel* __restrict
              const uint2* __restrict__ cand, const uint32_t* __restrict__ cand_cnt,
              uint32_t* __restrict__ hist, uint2* __restrict__ nar, uint32_t* __restrict__ nar_cnt,
              uint32_t nar_cap) {
-  constexpr int WID = PASS == 5 ? 7 : 11;
+  constexpr int WID = PASS == 5 ? 63 - kDigit0 - 44 : 11;
   constexpr int NB = 1 << WID;
-  constexpr int SHIFT = PASS == 1 ? 40 : PASS == 2 ? 29 : PASS == 3 ? 18 : PASS == 4 ? 7 : 0;
+  constexpr int SHIFT = PASS == 5 ? 0 : 63 - kDigit0 - 11 * PASS;
   __shared__ uint32_t sh[NB];
   const int s = blockIdx.y;
   if (sel[s].mode != kSelSearch) return;
@@ -691,7 +691,7 @@ cudaError_t launch_chist0(const float* m, int64_t P, int W, const int64_t* shard
                           const ShardSel* sel, uint32_t* hist, uint2* cand, uint32_t* cand_cnt,
                           bool selective, cudaStream_t st) {
   int64_t spb = 1;
-  const int grid = mpass_grid(P, 5, &spb);
+  const int grid = mpass_grid(P, 4, &spb);  // 48 KB of shared memory per block
   mpass_kernel<kMHist><<<grid, 256, 0, st>>>(m, P, W, shard_start, sel, hist, cand, cand_cnt, spb,
                                              selective ? 1 : 0);
   return cudaGetLastError();
