@@ -41,10 +41,11 @@ __device__ __forceinline__ uint64_t composite(uint32_t key, uint32_t i) {
 // The first-digit buckets [lo, hi] a refresh stages candidates from: one
 // either side of the previous threshold's bucket, stretched toward the bucket
 // the last two thresholds extrapolate to (at most kMaxTrend buckets on),
-// because early in training the first moments grow from step to step and the
-// threshold drifts the same way.  hi may be 4096 (no such digit).  With no
+// because early in training the first moments grow from step to step (the
+// exponential average starts from zero: about half an octave per step at the
+// third step with b1 = 0.9) and the threshold drifts the same way.  hi may be 4096 (no such digit).  With no
 // previous bucket the window is empty (lo > hi).
-constexpr int kMaxTrend = 6;
+constexpr int kMaxTrend = 16;
 constexpr int kMaxWindow = 2 * 1 + kMaxTrend + 1;  // buckets in the widest window
 
 __device__ __forceinline__ void bucket_window(const ShardSel& q, uint32_t& lo, uint32_t& hi) {
