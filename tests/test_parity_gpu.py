@@ -522,3 +522,69 @@ def test_maximum_size_properties(cuda_device):
     opt.close()
     del bufs, e_before
     torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------ writes stay inside their buffers
+_PAD_WORDS = 1024
+_CANARY = 0x7FBADBAD
+
+
+def _canaried(n, dtype, device):
+    """n elements of `dtype` followed by _PAD_WORDS canary words; returns the
+    element view and the 32-bit words behind it."""
+    esz = torch.empty(0, dtype=dtype).element_size()
+    words = (n * esz + 3) // 4
+    full = torch.full((words + _PAD_WORDS,), _CANARY, dtype=torch.int32, device=device)
+    view = full[:words].view(dtype)[:n]
+    return view, full, words
+
+
+@pytest.mark.parametrize("P,W,s,dtype", [(70001, 5, 0.9, "bf16"), (5003, 3, 0.99, "f32"),
+                                         (1 << 16, 4, 0.999, "bf16"), (3000, 256, 0.9, "f32")])
+def test_no_write_past_any_buffer(cuda_device, P, W, s, dtype):
+    """Every buffer the library writes (w, m, residuals, workspace, union
+    workspace) is followed by canary words; after dense, sparse and union
+    steps and cold and warm refreshes they must be intact."""
+    gdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    wl = _wl(P, W, s, dtype)
+    gen = synth.GradientStream(wl, seed=4, device="cpu")
+    checks = []
+    params, fp, wp = _canaried(P, torch.float32, cuda_device)
+    params.copy_(synth.init_params(P, seed=4))
+    m, fm, wm = _canaried(P, torch.float32, cuda_device)
+    m.zero_()
+    checks += [(fp, wp), (fm, wm)]
+    es = []
+    for _ in range(W):
+        e, fe, we = _canaried(P, torch.float32, cuda_device)
+        e.zero_()
+        es.append(e)
+        checks.append((fe, we))
+    gs = []
+    for _ in range(W):
+        g, fg, wg = _canaried(P, gdt, cuda_device)
+        gs.append(g)
+        checks.append((fg, wg))
+    h = C.scape_create([P], W, s, HP.beta1, HP.beta2, HP.lr, HP.eps, HP.weight_decay,
+                       C.SCAPE_BF16 if dtype == "bf16" else C.SCAPE_F32)
+    nws = C.scape_workspace_bytes(h)
+    ws, fws, wws = _canaried(nws, torch.uint8, cuda_device)
+    checks.append((fws, wws))
+    C.scape_bind(h, params.data_ptr(), m.data_ptr(), [e.data_ptr() for e in es], ws.data_ptr(),
+                 nws)
+    st = torch.cuda.current_stream().cuda_stream
+    for t in range(5):
+        for g, x in zip(gs, gen.next()):
+            g.copy_(x.to(cuda_device))
+        C.scape_step(h, [g.data_ptr() for g in gs], st)
+        C.scape_refresh_mask(h, st)
+    nu = C.scape_union_workspace_bytes(h, P)
+    uws, fu, wu = _canaried(nu, torch.uint8, cuda_device)
+    checks.append((fu, wu))
+    for g, x in zip(gs, gen.next()):
+        g.copy_(x.to(cuda_device))
+    C.scape_union_step(h, [g.data_ptr() for g in gs], uws.data_ptr(), nu, P, st)
+    torch.cuda.synchronize()
+    C.scape_destroy(h)
+    for full, words in checks:
+        assert bool((full[words:] == _CANARY).all())
