@@ -11,6 +11,8 @@
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "scape_internal.cuh"
 
 using namespace scapek;
@@ -145,7 +147,10 @@ int run_kernel(scape_t* h, int kid, cudaStream_t st, F&& fn, int nlaunch = 1) {
     b = take_event(h);
     if (a && b) cudaEventRecord(a, st);
   }
+  // a named host range per launch for timeline tools (no cost without one)
+  nvtxRangePushA(kKernelNames[kid]);
   const cudaError_t e = fn();
+  nvtxRangePop();
   h->launches += nlaunch;
   if (timed && a && b) {
     cudaEventRecord(b, st);
