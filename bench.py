@@ -46,6 +46,18 @@ def _grad_bytes(wl):
     return 2 if wl.grad_dtype == "bf16" else 4
 
 
+def mask_churn(prev_bits, bits, k):
+    """Fraction of the selected coordinates that changed between two masks:
+    |prev XOR new| / (2k), from the two bitmaps (int32 tensors of the same
+    length, any device).  0 for identical masks, 1 for disjoint ones."""
+    import torch
+
+    x = torch.bitwise_xor(prev_bits, bits).view(torch.uint8).to(torch.int64)
+    lut = torch.tensor([bin(v).count("1") for v in range(256)], dtype=torch.int64,
+                       device=x.device)
+    return float(lut[x].sum().item()) / (2.0 * k) if k else 0.0
+
+
 FUSION = {"none": 0, "sum": 1, "update": 2}  # scape_set_fusion levels
 
 
@@ -338,13 +350,18 @@ def bench_gpu(args, wl):
     prof_timed = opt.profile_read()
     clocks = clk.summary()
     # per-kernel breakdown: a few more steps with every kernel bracketed
+    # (and the mask's step-to-step churn: the temporal stability the lagged
+    # mask relies on)
     n_break = 3
     opt.profile_select(0xFFFFFFFF)
     opt.profile_reset()
+    churn = []
     for _ in range(n_break):
+        prev = opt.bits().clone()
         gen.next_into(grads)
         opt.step(grads)
         opt.refresh_mask()
+        churn.append(mask_churn(prev, opt.bits(), opt.k))
     torch.cuda.synchronize()
     opt.profile_collect()
     prof = opt.profile_read()
@@ -419,6 +436,7 @@ def bench_gpu(args, wl):
             "kernels": kernels,
             "kernels_measured_over": f"{n_break} profiled steps after the timed ones",
             "refresh_ms_per_step": refresh_ms,
+            "mask_churn_per_refresh": churn,
             "wall_ms_per_step": 1000.0 * sum(wall) / len(wall),
             "gpu_launches": launches,
             "clocks": clocks,

@@ -146,3 +146,14 @@ def test_fusion_and_staging_validate_without_gpu(lib):
     C.scape_set_residual_staging(h, 4096, 5 * 10048 * 4)
     C.scape_set_residual_staging(h, None, 0)       # back to in place
     C.scape_destroy(h)
+
+
+def test_mask_churn_counts_changed_coordinates():
+    import torch
+    import bench
+    a = torch.tensor([0b1011, 0, -1], dtype=torch.int32)     # 3 + 0 + 32 set bits
+    assert bench.mask_churn(a, a.clone(), 35) == 0.0
+    b = torch.tensor([0b0111, 0, -1], dtype=torch.int32)     # one bit moved
+    assert bench.mask_churn(a, b, 35) == 2 / 70
+    c = torch.tensor([0, -1, 0], dtype=torch.int32)          # disjoint, 32 set
+    assert abs(bench.mask_churn(torch.tensor([0, 0, -1], dtype=torch.int32), c, 32) - 1.0) < 1e-12
