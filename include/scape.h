@@ -155,6 +155,11 @@ int scape_step(scape_t *h, const void *const *host_grad_ptrs, void *stream);
  * SCAPE" Sec. 2), then the ascending packed index list and the per-tile rank
  * table the next step's compaction uses.  The mask comes from first-moment
  * statistics, not gradients ("SCAPE" Sec. I).
+ * The result is exact whatever the data.  Its cost is not: the first call
+ * after scape_bind() reads m two or three times; every later call reads it
+ * once, writing the bitmap from the previous threshold and correcting it,
+ * as long as each shard's threshold stays near the previous one (a shard
+ * whose threshold moved further is counted and re-marked in full).
  * Errors: SCAPE_ESTATE before the first step.
  */
 int scape_refresh_mask(scape_t *h, void *stream);
