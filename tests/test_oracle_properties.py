@@ -1,0 +1,68 @@
+"""Randomised properties of the oracle's layout and per-shard top-k (CPU
+only), checked against an independent brute force and against what the
+sharding and the keep-fraction require -- not against the oracle's own
+formulas.  Skipped where hypothesis is not installed."""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+hypothesis = pytest.importorskip("hypothesis")
+from hypothesis import given, settings, strategies as st  # noqa: E402
+
+from oracle import oracle as O  # noqa: E402
+from tests.test_oracle_pins import _bits_to_bool, _brute_topk  # noqa: E402
+
+_values = st.sampled_from([0.0, -0.0, 0.25, -0.25, 1e-40, -1e-40, 3.0, -3.0, 1e30,
+                           float("inf"), -float("inf"), 0.5, -0.5])
+
+
+@st.composite
+def _problem(draw):
+    P = draw(st.integers(1, 400))
+    W = draw(st.integers(1, 12))
+    s = draw(st.sampled_from([0.0, 0.5, 0.9, 0.99, 0.999, 0.123456, 0.7]))
+    mode = draw(st.sampled_from(["gauss", "levels", "mixed"]))
+    seed = draw(st.integers(0, 2**31 - 1))
+    rng = np.random.default_rng(seed)
+    if mode == "gauss":
+        m = rng.standard_normal(P).astype(np.float32)
+    elif mode == "levels":
+        m = (rng.integers(-4, 5, P) * 0.125).astype(np.float32)
+    else:
+        m = np.array(draw(st.lists(_values, min_size=P, max_size=P)), np.float32)
+    return m, W, s
+
+
+@settings(max_examples=150, deadline=None)
+@given(_problem())
+def test_layout_partitions_and_keeps_the_fraction(prob):
+    m, W, s = prob
+    P = m.size
+    start, k = O.layout(P, W, s)
+    assert start[0] == 0 and start[-1] == P
+    sizes = np.diff(start)
+    assert (sizes >= 0).all() and sizes.max() - sizes.min() <= 1     # even split
+    # the keep fraction 1 - s, with s taken to parts per million
+    keep = Fraction(1_000_000 - round(s * 1_000_000), 1_000_000)
+    for n, kk in zip(sizes.tolist(), k.tolist()):
+        if n == 0:
+            assert kk == 0
+            continue
+        # the smallest count that keeps at least that fraction of the shard
+        assert kk >= n * keep
+        assert kk - 1 < n * keep
+        assert 1 <= kk <= n
+
+
+@settings(max_examples=150, deadline=None)
+@given(_problem())
+def test_topk_matches_brute_force_on_random_shapes(prob):
+    m, W, s = prob
+    start, k = O.layout(m.size, W, s)
+    bits, idx = O.topk_mask(m, start, k)
+    want = _brute_topk(m, start, k)
+    assert (_bits_to_bool(bits, m.size) == want).all()
+    assert idx.tolist() == np.flatnonzero(want).tolist()
+    if m.size % 32:
+        assert bits[-1] >> np.uint32(m.size % 32) == 0
