@@ -66,3 +66,45 @@ def test_topk_matches_brute_force_on_random_shapes(prob):
     assert idx.tolist() == np.flatnonzero(want).tolist()
     if m.size % 32:
         assert bits[-1] >> np.uint32(m.size % 32) == 0
+
+
+@st.composite
+def _trajectory(draw):
+    P = draw(st.integers(1, 300))
+    W = draw(st.integers(1, 6))
+    s = draw(st.sampled_from([0.0, 0.5, 0.9, 0.99]))
+    bf16 = draw(st.booleans())
+    quant = draw(st.booleans())
+    seed = draw(st.integers(0, 2**31 - 1))
+    return P, W, s, bf16, quant, seed
+
+
+@settings(max_examples=60, deadline=None)
+@given(_trajectory())
+def test_step_invariants_on_random_trajectories(case):
+    """Error-feedback conservation bit for bit, compaction order, the one-step
+    lag and off-mask invariance, on random shapes and data."""
+    from tests.test_oracle_pins import HP, _grads, _widen
+    P, W, s, bf16, quant, seed = case
+    rng = np.random.default_rng(seed)
+    w0 = (rng.standard_normal(P) * 0.02).astype(np.float32)
+    st_ = O.new_state(w0, W, s, HP)
+    prev_bits = None
+    for gs in _grads(rng, P, W, 4, bf16=bf16, quant=quant):
+        e_before = [x.copy() for x in st_.e]
+        w_before, m_before = st_.w.copy(), st_.m.copy()
+        rec = O.advance(st_, gs)
+        used = _bits_to_bool(rec["used_bits"], P)
+        if prev_bits is not None:
+            assert (rec["used_bits"] == prev_bits).all()
+        idx = rec["used_idx"]
+        assert idx.tolist() == np.flatnonzero(used).tolist()
+        for w in range(W):
+            a = (_widen(gs[w]) + e_before[w]).astype(np.float32)
+            assert (rec["pack"][w].view(np.uint32) == a[idx].view(np.uint32)).all()
+            sent = np.zeros(P, np.float32)
+            sent[idx] = rec["pack"][w]
+            assert ((sent + st_.e[w]).view(np.uint32) == (a + np.float32(0)).view(np.uint32)).all()
+        assert (st_.w[~used].view(np.uint32) == w_before[~used].view(np.uint32)).all()
+        assert (st_.m[~used].view(np.uint32) == m_before[~used].view(np.uint32)).all()
+        prev_bits = rec["bits"]
