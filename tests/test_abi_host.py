@@ -157,3 +157,22 @@ def test_mask_churn_counts_changed_coordinates():
     assert bench.mask_churn(a, b, 35) == 2 / 70
     c = torch.tensor([0, -1, 0], dtype=torch.int32)          # disjoint, 32 set
     assert abs(bench.mask_churn(torch.tensor([0, 0, -1], dtype=torch.int32), c, 32) - 1.0) < 1e-12
+
+
+def test_algorithmic_bytes_per_step():
+    """The per-step byte counts the roofline uses: the sum of each kernel's
+    algorithmic bytes; level "none" adds the packed buffers' re-read."""
+    import bench
+    from sparse_communication_sharded_gb300 import synth
+    want = {"gpt345m": (32.21, 33.35), "llama500m": (185.67, 186.40), "llama1p8b": (115.99, 116.43)}
+    for name, (gb_sum, gb_none) in want.items():
+        wl = synth.WORKLOADS[name]
+        _, ks = O.layout(wl.P, wl.W, wl.sparsity)
+        k = int(ks.sum())
+        a = bench.algorithmic_bytes(wl, k, "sum")
+        b = bench.algorithmic_bytes(wl, k, "none")
+        assert abs(a["total"] / 1e9 - gb_sum) < 0.01, name
+        assert abs(b["total"] / 1e9 - gb_none) < 0.01, name
+        assert abs((b["total"] - a["total"]) - 4 * k * wl.W) < 1e-3
+        # the compaction dominates: at least 96% of the step's bytes
+        assert a["ef_compact"] / a["total"] > 0.96
