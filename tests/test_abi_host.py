@@ -174,5 +174,6 @@ def test_algorithmic_bytes_per_step():
         assert abs(a["total"] / 1e9 - gb_sum) < 0.01, name
         assert abs(b["total"] / 1e9 - gb_none) < 0.01, name
         assert abs((b["total"] - a["total"]) - 4 * k * wl.W) < 1e-3
-        # the compaction dominates: at least 96% of the step's bytes
-        assert a["ef_compact"] / a["total"] > 0.96
+        # the compaction dominates the step's bytes (92% at GPT-345M's 10%
+        # density, 98.6% at Llama-500M's 1%)
+        assert a["ef_compact"] / a["total"] > 0.9
