@@ -346,8 +346,10 @@ int64_t scape_launch_count(const scape_t *h);
  * device or host memory.  All calls share that array and it keeps the last
  * call's contents: calls that overlap on the GPU race and must be ordered by
  * the caller.  The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.
+ * (cudaGetSymbolAddress) with that device current and keeps it for the life
+ * of the process; make that first call before any stream capture.  The kept
+ * address belongs to the device's current context: after cudaDeviceReset()
+ * on that device, do not call this entry point again in the same process.
  * Limits: 1 <= P <= SCAPE_STATIC_MAX_P, 1 <= W <= SCAPE_STATIC_MAX_WORKERS;
  * larger sizes, NULL pointers, a misaligned m or sparsity outside [0, 1)
  * return SCAPE_EINVAL without touching the GPU; CUDA failures return

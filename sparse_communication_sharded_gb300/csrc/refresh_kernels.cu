@@ -575,15 +575,7 @@ cudaError_t launch_remark(const float* m, int64_t P, int W, const int64_t* shard
                           cudaStream_t st) {
   // enough 128-thread blocks to fill the GPU when every shard is re-marked;
   // in the common case all but one block per shard return at once
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
-      sms = n;
-    else
-      sms = 148;
-  }
+  const int sms = sm_count();
   const int64_t ntiles = (P + kTile - 1) / kTile;
   const int64_t per_shard = (ntiles + W - 1) / W + 1;
   int64_t gx = ((int64_t)sms * 16 + W - 1) / W;
@@ -622,15 +614,7 @@ cudaError_t launch_scan(const uint32_t* tile_cnt, int64_t ntiles, uint32_t* tile
 cudaError_t launch_index(const uint32_t* bits, int64_t P, const uint32_t* tile_base,
                          uint32_t* idx, int64_t k, cudaStream_t st) {
   const int64_t ntiles = (P + kTile - 1) / kTile;
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
-      sms = n;
-    else
-      sms = 148;
-  }
+  const int sms = sm_count();
   // measured on GB300: direct stores win at 1% density, staged stores at 10%
   const bool staged = !(k >= 0 && k * 20 < P);
   // persistent: staged blocks (4 warps, 32 KB) 6 per SM, direct ones (8 warps) 8 per SM

@@ -5,6 +5,7 @@
 // step_kernels.cu, topk_kernels.cu, refresh_kernels.cu and union_kernels.cu on
 // the caller's stream (plus internal copy streams for the host-memory paths).
 // Never allocates device memory.
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -16,6 +17,28 @@
 #include "scape_internal.cuh"
 
 using namespace scapek;
+
+namespace scapek {
+
+int sm_count() {
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    (void)cudaGetLastError();
+    return 152;
+  }
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    (void)cudaGetLastError();
+    return 152;
+  }
+  cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+}  // namespace scapek
 
 namespace {
 

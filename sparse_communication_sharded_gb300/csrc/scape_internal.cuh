@@ -199,6 +199,11 @@ struct EfFuse {
   int flags;
 };
 
+// Streaming multiprocessors of the current device (persistent grids are sized
+// from it).  Looked up once per device and cached; safe to call from any host
+// thread.
+int sm_count();
+
 // ---------------------------------------------------------------- launchers
 // Each returns cudaGetLastError() after enqueueing on `st`.
 // moment: step 1 under the first-moment buffer reading.

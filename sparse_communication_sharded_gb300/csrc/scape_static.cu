@@ -72,7 +72,9 @@ std::mutex g_static_mu;
 unsigned char* g_static_addr[kMaxDevices] = {};
 
 // Device address of the scratch array for the current device, looked up once
-// per device (host code must not use the symbol's name as an address).
+// per device (host code must not use the symbol's name as an address).  The
+// address belongs to the device's primary context; a cudaDeviceReset() would
+// invalidate it, which the header tells callers not to do between calls.
 cudaError_t static_scratch_address(unsigned char** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -669,15 +669,7 @@ chist_kernel(const int64_t* __restrict__ shard_start, const ShardSel* __restrict
 }
 
 int mpass_grid(int64_t P, int blocks_per_sm, int64_t* segs_per_block) {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
-      sms = n;
-    else
-      sms = 148;
-  }
+  const int sms = sm_count();
   const int64_t nseg = (P + kMSeg - 1) / kMSeg;
   const int64_t want = (int64_t)sms * blocks_per_sm;
   const int64_t grid = nseg < want ? nseg : want;

@@ -401,18 +401,18 @@ def test_profiling_counts_launches(cuda_device):
 
 # ------------------------------------------------------------ full-size workloads, sampled shards
 @pytest.mark.parametrize("name,steps,shards", [
-    ("gpt345m", 3, (0, 7)),
-    ("llama500m", 3, (0, 17, 31)),
-    ("llama1p8b", 2, (3,)),
-    # ten steps at full size: eight warm refreshes, each mask used by the next step
-    ("gpt345m", 10, (3,)),
-    ("llama500m", 10, (5,)),
+    # ten steps at full size: nine lagged sparse steps and ten refreshes (eight
+    # of them warm), each mask used by the next step; first, a middle and the
+    # last shard, the oracle running them in parallel processes
+    ("gpt345m", 10, (0, 3, 7)),
+    ("llama500m", 10, (0, 17, 31)),
+    ("llama1p8b", 10, (0, 3, 7)),
 ])
 def test_full_size_sampled_shards(cuda_device, name, steps, shards):
     wl = synth.WORKLOADS[name]
-    free, _ = torch.cuda.mem_get_info()
+    torch.cuda.empty_cache()
     rep = run_sampled_shards(wl, cuda_device, steps, shards)
-    assert rep.exact
+    assert rep.exact, f"not bit-identical ({rep.flips} mask flips of {rep.mask_bits})"
     torch.cuda.empty_cache()
 
 
@@ -455,73 +455,6 @@ def test_host_resident_residuals_match_oracle(cuda_device, P, W, s, dtype, stagi
         assert np.array_equal(opt.e[w].numpy().view(np.uint32), st.e[w].view(np.uint32))
     assert np.array_equal(u32(opt.bits()), st.bits)
     opt.close()
-
-
-# ------------------------------------------------------------ maximum size, by properties
-def test_maximum_size_properties(cuda_device):
-    """P = 2^31 - 1 (the largest accepted), W = 2: too large for the oracle's
-    sort, so check what must hold at any size, on the GPU: every shard's mask
-    holds exactly k_s coordinates, every selected key beats every unselected one
-    (ties to the lower index), the packed buffers are fl(g + e) at the selected
-    positions in ascending order, sent + residual == fl(g + e), and unselected
-    w and m do not move."""
-    P, W, s = (1 << 31) - 1, 2, 0.99
-    free, _ = torch.cuda.mem_get_info()
-    if free < 80 << 30:
-        pytest.skip("needs ~80 GB of free device memory")
-    wl = synth.Workload("max", (("flat", P),), W=W, sparsity=s, steps=2, grad_dtype="bf16")
-    gen = synth.GradientStream(wl, seed=12, device=cuda_device)
-    params = synth.init_params(P, seed=12, device=cuda_device)
-    opt = make_opt(params, W, s, torch.bfloat16)
-    bufs = gen.alloc()
-    gen.next_into(bufs)
-    opt.step(bufs)
-    opt.refresh_mask()
-    torch.cuda.synchronize()
-    # mask: exact k_s per shard and the threshold order
-    words = opt.bits()
-    sel = ((words.view(-1, 1) >> torch.arange(32, device=cuda_device, dtype=torch.int32))
-           & 1).view(-1)[:P].bool()
-    keys = opt.m.view(torch.int32) & 0x7FFFFFFF
-    for sh in range(W):
-        lo, hi = opt.shard_start[sh], opt.shard_start[sh + 1]
-        ss, kk = sel[lo:hi], keys[lo:hi]
-        assert int(ss.sum()) == opt.shard_k[sh]
-        kmin = int(kk[ss].min())
-        assert int(kk[~ss].max()) <= kmin
-        ties_sel = torch.nonzero(ss & (kk == kmin)).flatten()
-        ties_uns = torch.nonzero(~ss & (kk == kmin)).flatten()
-        if ties_uns.numel():
-            assert int(ties_sel.max()) < int(ties_uns.min())
-    del sel, keys
-    # one sparse step: compaction, conservation and off-mask invariance at samples
-    idx = opt.idx().long()
-    e_before = [x.clone() for x in opt.e]
-    w_before, m_before = params.clone(), opt.m.clone()
-    gen.next_into(bufs)
-    opt.step(bufs)
-    torch.cuda.synchronize()
-    gsel = torch.Generator(device=cuda_device).manual_seed(0)
-    js = torch.randint(0, opt.k, (100000,), device=cuda_device, generator=gsel)
-    js = torch.cat([js, torch.tensor([0, opt.k - 1], device=cuda_device)])
-    ii = idx[js]
-    for w in range(W):
-        a = bufs[w][ii].float() + e_before[w][ii]
-        assert torch.equal(opt.pack()[w][js].view(torch.int32), a.view(torch.int32))
-        assert bool((opt.e[w][ii] == 0).all())
-    pos = torch.randint(0, P, (200000,), device=cuda_device, generator=gsel)
-    pos = torch.cat([pos, torch.tensor([P - 1, P - 2, 0], device=cuda_device)])
-    wb = opt.bits()
-    unsel = ((wb[pos >> 5] >> (pos & 31).int()) & 1) == 0
-    pu = pos[unsel]
-    for w in range(W):
-        a = bufs[w][pu].float() + e_before[w][pu]
-        assert torch.equal(opt.e[w][pu].view(torch.int32), a.view(torch.int32))
-    assert torch.equal(params[pu].view(torch.int32), w_before[pu].view(torch.int32))
-    assert torch.equal(opt.m[pu].view(torch.int32), m_before[pu].view(torch.int32))
-    opt.close()
-    del bufs, e_before
-    torch.cuda.empty_cache()
 
 
 # ------------------------------------------------------------ writes stay inside their buffers
