@@ -217,44 +217,158 @@ def _dist():
     return ws, rank, local
 
 
-# --------------------------------------------------------------------- oracle sample
-def run_oracle_sample(wl, steps, seed=0, device=None):
-    """Time the CPU oracle (single thread) on one optimizer shard of the
-    workload: a dense first step (untimed), then `steps` lagged sparse steps
-    with their mask refreshes (timed).  Gradients are drawn on `device` (GPU if
-    given) and copied to host memory.  Returns (params/s, seconds, n_shard)."""
+# --------------------------------------------------------------------- config
+READING = ("paper: only selected coordinates update w and m; the synchronised buffer holds "
+           "the mean of the masked error-fed gradients (the first-moment form is "
+           "SCAPE_VARIANT_MOMENT_SYNC)")
+
+
+def k_of(wl):
+    """k = sum over shards of ceil(n_s (1 - sparsity)), sparsity in ppm."""
+    ppm = round(wl.sparsity * 1e6)
+    starts = [s * wl.P // wl.W for s in range(wl.W + 1)]
+    return sum(((starts[s + 1] - starts[s]) * (1000000 - ppm) + 999999) // 1000000
+               for s in range(wl.W))
+
+
+def workload_config(wl, args, ws=1):
+    """The `config` object of the JSON line; both arms print the same one."""
+    return {"workload": wl.name, "P": wl.P, "W": wl.W, "sparsity": wl.sparsity, "k": k_of(wl),
+            "grad_dtype": wl.grad_dtype, "state_dtype": "f32", "reading": READING,
+            "residuals": args.residuals, "fusion": args.fusion,
+            "staging_rows": (0 if args.residuals == "device" else
+                             min(wl.W, 12) if args.staging_rows is None else
+                             (max(args.staging_rows, 3) if args.staging_rows else 0)),
+            "l2": "inputs larger than L2 (gradients + residuals far beyond 129 MB)",
+            "parallelism": f"{ws} independent problems (weak)" if ws > 1 else "1 GPU"}
+
+
+# --------------------------------------------------------------------- oracle leg
+def _local_cores():
+    """Host cores this process may run on (those local to the GPU when the
+    process was bound to them)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _sample_shards(W, n):
+    """n shard indices spread evenly over 0..W-1 (first and last included)."""
+    if n >= W:
+        return list(range(W))
+    if n == 1:
+        return [W // 2]
+    return sorted({round(j * (W - 1) / (n - 1)) for j in range(n)})
+
+
+def run_oracle_leg(wl, steps, n_shards, device=None, compare=False, seed=0):
+    """The CPU oracle, one process per optimizer shard, on `n_shards` shards of
+    the workload: a dense first step, then `steps` lagged sparse steps with
+    their mask refreshes.  Shards are independent sub-problems, so each worker
+    runs its shard as a one-shard problem of its own (oracle.pool).  Inputs are
+    drawn on `device` (the GPU when there is one) with the bench's seed and
+    copied into the workers' shared buffers.  With compare, the GPU runs the
+    same whole problem from the same inputs and every refresh's mask is
+    compared with the oracle's on the sampled shards.
+
+    Returns a dict: params/s of the sampled shards over the sparse steps (the
+    sum of their sizes times the steps, over the sum of the per-step times of
+    the slowest worker), the per-step wall time of that sample, and, with
+    compare, the mask bits compared and flipped."""
     import numpy as np
     import torch
 
     from oracle import oracle as O
+    from oracle.pool import ShardOracles
     from sparse_communication_sharded_gb300 import synth
 
-    start, ks = O.layout(wl.P, wl.W, wl.sparsity)
-    sh = wl.W // 2
-    lo, hi = int(start[sh]), int(start[sh + 1])
-    n = hi - lo
+    P, W = wl.P, wl.W
+    hp = O.Hyper()
+    start, ks = O.layout(P, W, wl.sparsity)
+    shards = _sample_shards(W, n_shards)
+    spec = [(int(start[s]), int(start[s + 1]), int(ks[s])) for s in shards]
     gdev = device if device is not None else "cpu"
-    gen = synth.GradientStream(wl, seed=seed, device=gdev, P=n, offset=lo)
-    w0 = synth.init_params(n, seed=seed, device=gdev).cpu().numpy()
-    st = O.new_state(w0, wl.W, wl.sparsity, O.Hyper(),
-                     shard_start=np.array([0, n], np.int64), shard_k=np.array([ks[sh]], np.int64))
-    bufs = gen.alloc()
+    w0 = synth.init_params(P, seed=seed, device=gdev)
+    if device is not None:
+        gen = synth.GradientStream(wl, seed=seed, device=gdev)
+        slices = None
+    else:
+        # no GPU: draw each sampled shard's slices on its own (same recipe)
+        gen = None
+        slices = [synth.GradientStream(wl, seed=seed + 1 + j, device="cpu", P=hi - lo, offset=lo)
+                  for j, (lo, hi, _) in enumerate(spec)]
+    opt = None
+    if compare:
+        import sparse_communication_sharded_gb300 as pkg
 
-    def host_grads():
-        gen.next_into(bufs)
-        return [synth.to_numpy_grad(b) for b in bufs]
-
-    O.advance(st, host_grads(), keep=())          # dense first step, untimed
-    total = 0.0
-    for _ in range(steps):
-        g = host_grads()
-        t0 = time.perf_counter()
-        O.advance(st, g, keep=())
-        total += time.perf_counter() - t0
-    del bufs
+        params = w0.clone()
+        gdt = torch.bfloat16 if wl.grad_dtype == "bf16" else torch.float32
+        opt = pkg.Scape(params, W, wl.sparsity, layer_numel=[n for _, n in wl.layers],
+                        lr=hp.lr, beta1=hp.beta1, beta2=hp.beta2, eps=hp.eps,
+                        weight_decay=hp.weight_decay, grad_dtype=gdt)
+    popc = np.array([bin(v).count("1") for v in range(256)], np.int64)
+    flips = bits = 0
+    step_s = []
+    bf16 = wl.grad_dtype == "bf16"
+    with ShardOracles(spec, W, wl.grad_dtype, hp, lambda lo, hi: w0[lo:hi].cpu().numpy(),
+                      pin=device is not None) as pool:
+        del w0
+        bufs = gen.alloc() if gen is not None else None
+        for t in range(1, steps + 2):
+            if gen is not None:
+                gen.next_into(bufs)
+            for j, (lo, hi, _) in enumerate(spec):
+                host = torch.from_numpy(pool.grads(j).view(np.int16 if bf16 else np.float32))
+                src_rows = bufs if gen is not None else slices[j].next()
+                for w in range(W):
+                    src = src_rows[w][lo:hi] if gen is not None else src_rows[w]
+                    host[w].copy_(src.view(torch.int16) if bf16 else src, non_blocking=True)
+            if opt is not None:
+                opt.step(bufs)
+                opt.refresh_mask()
+            if device is not None:
+                torch.cuda.synchronize()
+            times = pool.step()
+            if t >= 2:
+                step_s.append(max(times))
+            if opt is not None:
+                g = opt.bits().cpu().numpy().view(np.uint32)
+                for j, (lo, hi, _) in enumerate(spec):
+                    n = hi - lo
+                    nw = (n + 31) // 32
+                    w0i, sh = lo // 32, lo % 32
+                    a = g[w0i:w0i + nw].astype(np.uint64)
+                    b = np.zeros(nw, np.uint64)
+                    nxt = g[w0i + 1:w0i + 1 + nw].astype(np.uint64)
+                    b[:nxt.size] = nxt
+                    loc = (((a >> np.uint64(sh)) | (b << np.uint64(32 - sh)))
+                           & np.uint64(0xFFFFFFFF)).astype(np.uint32)
+                    if n % 32:
+                        loc[-1] &= np.uint32((1 << (n % 32)) - 1)
+                    x = (loc ^ pool.out(j)["bits"]).view(np.uint8)
+                    flips += int(popc[x].sum())
+                    bits += n
+        del bufs
+    if opt is not None:
+        opt.close()
+        del params
     if device is not None:
         torch.cuda.empty_cache()
-    return n * steps / total, total, n
+    n_sample = sum(hi - lo for lo, hi, _ in spec)
+    secs = sum(step_s)
+    return {"params_per_s": n_sample * len(step_s) / secs if secs else None,
+            "ms_per_step": 1000.0 * secs / max(len(step_s), 1), "steps": len(step_s),
+            "shards": shards, "n_sample": n_sample, "processes": len(spec),
+            "mask_bits": bits, "mask_flips": flips,
+            "mask_flip_fraction": flips / bits if bits else None}
+
+
+def oracle_sample_text(res, wl):
+    return (f"{len(res['shards'])} of {wl.W} optimizer shards ({res['n_sample']} of {wl.P} "
+            f"params, {wl.W} workers each), one oracle process per shard in parallel, "
+            f"{res['steps']} lagged sparse steps + refreshes after an untimed dense step; "
+            f"value = sampled params x steps / sum over steps of the slowest process's time")
 
 
 # --------------------------------------------------------------------- reference arm
@@ -264,26 +378,123 @@ def bench_reference(args, wl):
         return 0
     import torch
     dev = torch.device("cuda:0") if torch.cuda.is_available() else None
+    cores = _local_cores()
+    if dev is not None:
+        near = _bind_near_gpu(dev)
+        cores = len(near) if near else cores
     steps = max(1, args.steps)
-    rate, secs, n = run_oracle_sample(wl, steps, device=dev)
+    t0 = time.perf_counter()
+    res = run_oracle_leg(wl, steps, min(cores, wl.W), device=dev)
+    wall = time.perf_counter() - t0
     line = {
-        "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": ws,
-        "steps": steps, "warmup": args.warmup, "ms_per_step": 1000.0 * secs / steps * wl.P / n,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic",
-        "config": {"workload": wl.name, "P": wl.P, "W": wl.W, "sparsity": wl.sparsity,
-                   "grad_dtype": wl.grad_dtype},
-        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"one optimizer shard ({n} params x {wl.W} workers), "
-                                   f"{steps} lagged sparse steps + refreshes after an untimed "
-                                   f"dense step; ms_per_step scaled to the full P"},
-        "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "impl": "reference", "metric": METRIC, "value": res["params_per_s"], "unit": UNIT,
+        "n_gpus": ws, "steps": res["steps"], "warmup": args.warmup,
+        "ms_per_step": res["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(wl, args),
+        "cpu_baseline": {"value": res["params_per_s"], "unit": UNIT, "cores": res["processes"],
+                         "kind": "oracle", "sample": oracle_sample_text(res, wl)},
+        "extrapolated": {"sample_is_whole_problem": res["n_sample"] == wl.P,
+                         "shards_timed": len(res["shards"]), "shards_total": wl.W,
+                         "ms_per_step_of_sample": res["ms_per_step"],
+                         "full_problem_ms_per_step_estimate":
+                             res["ms_per_step"] * wl.P / res["n_sample"],
+                         "note": "ms_per_step is the measured time of the sampled shards; "
+                                 "the full-problem figure scales it by P / sampled params "
+                                 "(shards are independent) and is not measured"},
+        "wall_s": wall,
+        "e2e": {"value": res["params_per_s"], "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
 
 
 # --------------------------------------------------------------------- GPU arm
+def time_steps(opt, gen, grads, steps, barrier=lambda: None):
+    """Time `steps` whole steps (scape_step + scape_refresh_mask) with CUDA
+    events on the current stream; fresh gradients before each, outside the
+    timed window.  Returns the per-step milliseconds and wall seconds."""
+    import torch
+
+    step_ms, wall = [], []
+    st = torch.cuda.current_stream()
+    for _ in range(steps):
+        gen.next_into(grads)
+        barrier()
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        ev0.record(st)
+        opt.step(grads)
+        opt.refresh_mask()
+        ev1.record(st)
+        torch.cuda.synchronize()
+        wall.append(time.perf_counter() - t0)
+        barrier()
+        step_ms.append(ev0.elapsed_time(ev1))
+    return step_ms, wall
+
+
+def bench_other_workload(name, args, dev, peak):
+    """One more shape, timed like the headline one (fewer extras)."""
+    import torch
+
+    import sparse_communication_sharded_gb300 as pkg
+    from sparse_communication_sharded_gb300 import synth
+
+    wl = synth.WORKLOADS[name]
+    gdt = torch.bfloat16 if wl.grad_dtype == "bf16" else torch.float32
+    params = synth.init_params(wl.P, seed=0, device=dev)
+    opt = pkg.Scape(params, wl.W, wl.sparsity, layer_numel=[n for _, n in wl.layers],
+                    grad_dtype=gdt)
+    opt.set_fusion(FUSION[args.fusion])
+    gen = synth.GradientStream(wl, seed=0, device=dev)
+    grads = gen.alloc()
+    for _ in range(args.warmup):
+        gen.next_into(grads)
+        opt.step(grads)
+        opt.refresh_mask()
+    torch.cuda.synchronize()
+    opt.profile(True)
+    opt.profile_select(["ef_compact"])
+    opt.profile_reset()
+    step_ms, _ = time_steps(opt, gen, grads, args.other_steps)
+    opt.profile_collect()
+    ef_ms, ef_n = opt.profile_read()["ef_compact"]
+    # per-kernel split from two profiled steps after the timed ones
+    opt.profile_select(0xFFFFFFFF)
+    opt.profile_reset()
+    for _ in range(2):
+        gen.next_into(grads)
+        opt.step(grads)
+        opt.refresh_mask()
+    torch.cuda.synchronize()
+    opt.profile_collect()
+    prof = opt.profile_read()
+    opt.profile(False)
+    k = opt.k
+    opt.close()
+    del grads, params, opt
+    torch.cuda.empty_cache()
+    ms = sum(step_ms) / len(step_ms)
+    alg = algorithmic_bytes(wl, k, fusion=args.fusion)
+    ef_avg = ef_ms / max(ef_n, 1)
+    step_kernels = ("dense_step", "ef_compact", "reduce", "adams_sparse")
+    return {"P": wl.P, "W": wl.W, "sparsity": wl.sparsity, "k": k, "grad_dtype": wl.grad_dtype,
+            "steps": args.other_steps, "warmup": args.warmup, "ms_per_step": ms,
+            "ms_each": step_ms, "params_per_s": wl.P / (ms / 1000.0),
+            "hbm_gbs": alg["total"] / (ms / 1000.0) / 1e9,
+            "hbm_frac": alg["total"] / (ms / 1000.0) / 1e9 / peak,
+            "alg_bytes_per_step": alg["total"],
+            "ef_compact": {"ms_per_launch": ef_avg,
+                           "gbs": alg["ef_compact"] / (ef_avg / 1000.0) / 1e9,
+                           "frac": alg["ef_compact"] / (ef_avg / 1000.0) / 1e9 / peak},
+            "kernels_ms_per_step": {n: m / 2 for n, (m, c) in prof.items() if c},
+            "refresh_ms_per_step": sum(m for n, (m, _) in prof.items()
+                                       if n not in step_kernels) / 2}
+
+
 def bench_gpu(args, wl):
     import torch
     import torch.distributed as dist
@@ -328,23 +539,8 @@ def bench_gpu(args, wl):
     opt.profile_select(["ef_compact"])
     opt.profile_reset()
     n_launch0 = opt.launch_count()
-    step_ms, wall = [], []
-    st = torch.cuda.current_stream()
     with ClockSampler(local) as clk:
-        for _ in range(args.steps):
-            gen.next_into(grads)
-            barrier()
-            torch.cuda.synchronize()
-            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            t0 = time.perf_counter()
-            ev0.record(st)
-            opt.step(grads)
-            opt.refresh_mask()
-            ev1.record(st)
-            torch.cuda.synchronize()
-            wall.append(time.perf_counter() - t0)
-            barrier()
-            step_ms.append(ev0.elapsed_time(ev1))
+        step_ms, wall = time_steps(opt, gen, grads, args.steps, barrier=barrier)
     launches = opt.launch_count() - n_launch0
     opt.profile_collect()
     prof_timed = opt.profile_read()
@@ -405,27 +601,39 @@ def bench_gpu(args, wl):
             e2e["value"] = ws * P / (t_e2e / 1000.0)
             e2e["h2d_bytes_per_step"] *= ws
             e2e["d2h_bytes_per_step"] *= ws
+    opt.close()
+    del grads, params, opt, gen
+    torch.cuda.empty_cache()
 
+    # the other two shapes of the pages' workloads, timed the same way
+    others = {}
+    if ws == 1 and args.other_steps > 0:
+        for name in ("gpt345m", "llama500m", "llama1p8b"):
+            if name != wl.name and args.workload in synth.WORKLOADS:
+                others[name] = bench_other_workload(name, args, dev, peak)
+
+    # the CPU oracle on the host cores local to the GPU, one process per
+    # shard, on the same inputs as a fresh GPU run of the workload: its rate
+    # (the CPU baseline) and the mask bits that differ from the GPU's
     cpu = None
+    oracle_leg = None
     if rank == 0 and ws == 1 and args.cpu_steps > 0:
-        rate, secs, n = run_oracle_sample(wl, args.cpu_steps, device=dev)
-        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"one optimizer shard ({n} of {P} params, {W} workers), "
-                         f"{args.cpu_steps} lagged sparse steps + refreshes after an untimed "
-                         f"dense step, single-threaded C, {secs:.1f} s"}
+        near = _bind_near_gpu(dev)
+        cores = len(near) if near else _local_cores()
+        oracle_leg = run_oracle_leg(wl, args.cpu_steps, min(cores, W), device=dev, compare=True)
+        cpu = {"value": oracle_leg["params_per_s"], "unit": UNIT,
+               "cores": oracle_leg["processes"], "kind": "oracle",
+               "sample": oracle_sample_text(oracle_leg, wl),
+               "ms_per_step_of_sample": oracle_leg["ms_per_step"],
+               "extrapolated": False}
 
     if rank == 0:
+        config = workload_config(wl, args, ws)
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t_max, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": wl.name, "P": P, "W": W, "sparsity": wl.sparsity,
-                       "k": opt.k, "grad_dtype": wl.grad_dtype, "state_dtype": "f32",
-                       "residuals": args.residuals, "fusion": args.fusion,
-                       "staging_rows": (opt.staging.numel() // (4 * ((P + 63) // 64 * 64))
-                                        if opt.staging is not None else 0),
-                       "l2": "inputs larger than L2 (gradients + residuals far beyond 129 MB)",
-                       "parallelism": f"{ws} independent problems (weak)"},
+            "config": config,
             "hbm_gbs": alg["total"] / (t_max / 1000.0) / 1e9,
             "hbm_frac": alg["total"] / (t_max / 1000.0) / 1e9 / peak,
             "alg_bytes_per_step": alg["total"],
@@ -437,18 +645,106 @@ def bench_gpu(args, wl):
             "kernels_measured_over": f"{n_break} profiled steps after the timed ones",
             "refresh_ms_per_step": refresh_ms,
             "mask_churn_per_refresh": churn,
+            "mask_flip_fraction": oracle_leg["mask_flip_fraction"] if oracle_leg else None,
+            "mask_flips": ({"flipped": oracle_leg["mask_flips"], "compared": oracle_leg["mask_bits"],
+                            "over": f"{oracle_leg['steps'] + 1} refreshes of shards "
+                                    f"{oracle_leg['shards']} against the oracle on the same "
+                                    f"inputs"} if oracle_leg else None),
             "wall_ms_per_step": 1000.0 * sum(wall) / len(wall),
             "gpu_launches": launches,
             "clocks": clocks,
             "e2e": e2e,
             "baselines": baselines,
+            "other_workloads": others or None,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.barrier()
         dist.destroy_process_group()
-    opt.close()
+    return 0
+
+
+# --------------------------------------------------------------------- flat sweep
+SWEEP_W = (1, 8, 32)
+SWEEP_S = (0.0, 0.9, 0.99, 0.999)
+
+
+def sweep_device_bytes(P, W, k, stride=64):
+    """Device memory one flat-sweep point needs: f32 gradients and residuals of
+    every worker, w and m, and the library's workspace (the candidate buffer
+    of 8 bytes per parameter dominates it), plus the generator's scratch."""
+    rows = (P + stride - 1) // stride * stride
+    ws = P * 8 + W * k * 4 + 2 * k * 4 + P // 8 + W * 8192 * 4 + (64 << 20)
+    return W * P * 4 + W * rows * 4 + 8 * P + ws + 5 * 4 * min(P, 1 << 26) + 4 * P
+
+
+def bench_sweep(args):
+    """The flat sweep: P = 2^e fp32 parameters for the exponents given, W in
+    {1, 8, 32}, sparsity in {0, 90, 99, 99.9}%, gradients quantised to 256
+    levels (many ties in |m|).  Each point: the dense first step and
+    warm-up - 1 lagged steps untimed, then `steps` timed steps (scape_step +
+    scape_refresh_mask, CUDA events).  Points whose footprint exceeds 90% of
+    the free device memory are reported as skipped."""
+    import torch
+
+    import sparse_communication_sharded_gb300 as pkg
+    from sparse_communication_sharded_gb300 import synth
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda:0")
+    pkg.load()
+    peak, peak_kind = _peaks()
+    points = []
+    with ClockSampler(0) as clk:
+        for e in args.sweep_exps:
+            P = 1 << e
+            for W in SWEEP_W:
+                for sp in SWEEP_S:
+                    wl = synth.flat_workload(P, W, sp, steps=args.steps)
+                    k = k_of(wl)
+                    need = sweep_device_bytes(P, W, k)
+                    torch.cuda.empty_cache()
+                    free, _ = torch.cuda.mem_get_info()
+                    pt = {"P": P, "log2P": e, "W": W, "sparsity": sp, "k": k,
+                          "device_bytes": need}
+                    if need > 0.9 * free:
+                        pt["skipped"] = f"needs {need / 2**30:.0f} GiB, {free / 2**30:.0f} GiB free"
+                        points.append(pt)
+                        continue
+                    params = synth.init_params(P, seed=0, device=dev)
+                    opt = pkg.Scape(params, W, sp, grad_dtype=torch.float32)
+                    opt.set_fusion(FUSION[args.fusion])
+                    gen = synth.GradientStream(wl, seed=0, device=dev)
+                    grads = gen.alloc()
+                    for _ in range(args.warmup):
+                        gen.next_into(grads)
+                        opt.step(grads)
+                        opt.refresh_mask()
+                    torch.cuda.synchronize()
+                    step_ms, _ = time_steps(opt, gen, grads, args.steps)
+                    opt.close()
+                    del grads, params, opt, gen
+                    ms = sorted(step_ms)[len(step_ms) // 2]
+                    alg = algorithmic_bytes(wl, k, fusion=args.fusion)["total"]
+                    pt.update({"ms_per_step": ms, "ms_each": step_ms,
+                               "params_per_s": P / (ms / 1000.0),
+                               "hbm_gbs": alg / (ms / 1000.0) / 1e9,
+                               "hbm_frac": alg / (ms / 1000.0) / 1e9 / peak})
+                    points.append(pt)
+    torch.cuda.empty_cache()
+    done = [p for p in points if "ms_per_step" in p]
+    big = [p for p in done if p["log2P"] == max(q["log2P"] for q in done)] if done else []
+    line = {"metric": METRIC, "value": (max(p["params_per_s"] for p in big) if big else None),
+            "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "flat sweep", "exponents": list(args.sweep_exps),
+                       "W": list(SWEEP_W), "sparsity": list(SWEEP_S), "grad_dtype": "f32",
+                       "quantum": 2.0 ** -15, "fusion": args.fusion,
+                       "value_is": "best params/s at the largest P that fits"},
+            "peak": peak, "peak_kind": peak_kind, "clocks": clk.summary(), "sweep": points}
+    print(json.dumps(line), flush=True)
     return 0
 
 
@@ -570,7 +866,10 @@ def main(argv=None):
     ap.add_argument("--workload", default="llama500m")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=6)
-    ap.add_argument("--cpu-steps", type=int, default=2)
+    ap.add_argument("--cpu-steps", type=int, default=5,
+                    help="lagged sparse steps of the CPU oracle leg (0 to skip)")
+    ap.add_argument("--other-steps", type=int, default=10,
+                    help="timed steps of each of the two other workload shapes (0 to skip)")
     ap.add_argument("--residuals", default="device", choices=["device", "host"],
                     help="error-feedback buffers in HBM or in pinned host memory")
     ap.add_argument("--staging-rows", type=int, default=None,
@@ -581,6 +880,11 @@ def main(argv=None):
                          "adams_sparse), sum (writes g_bar), update (also AdamS)")
     ap.add_argument("--baselines", type=int, default=1,
                     help="also time the dense AdamS and AdamW baselines (0 to skip)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="run the flat sweep (2^e fp32 parameters, W in {1, 8, 32}, sparsity "
+                         "in {0, 90, 99, 99.9}%%, 256-level gradients) instead")
+    ap.add_argument("--sweep-exps", type=int, nargs="+", default=[20, 22, 24, 26, 28, 30],
+                    help="exponents e of the flat sweep's P = 2^e")
     ap.add_argument("--P", type=int, default=None,
                     help="with --workload custom: flat parameter count")
     ap.add_argument("--workers", type=int, default=8, help="with --workload custom: W")
@@ -591,6 +895,10 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     from sparse_communication_sharded_gb300 import synth
+    if args.sweep:
+        if args.impl == "reference":
+            ap.error("--sweep times the GPU path only")
+        return bench_sweep(args)
     if args.workload == "custom":
         if not args.P:
             ap.error("--workload custom needs --P")
