@@ -7,10 +7,12 @@ plus scape_refresh_mask (the partitioned top-k that the next step uses).
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload llama500m]
     python bench.py --impl reference ...     # the CPU oracle, same metric
 
-Rank 0 prints one JSON line.  With N > 1 (torchrun) every rank runs its own
-independent problem of the same shape (optimizer shards are independent), no
-data-path collective runs, and the value is the sum over ranks of the
-parameters stepped divided by the slowest rank's time (weak scaling).
+Rank 0 prints one JSON line.  With N > 1 (torchrun) the workload's W optimizer
+shards are split into N contiguous blocks, one per GPU: each rank holds a
+shard-range handle over its parameter slice and steps the slices of all W
+workers' gradients (optimizer shards are independent, so no data-path
+collective runs), and the value is P over the slowest rank's time (strong
+scaling: one problem of fixed size).
 """
 from __future__ import annotations
 
@@ -61,12 +63,13 @@ def mask_churn(prev_bits, bits, k):
 FUSION = {"none": 0, "sum": 1, "update": 2}  # scape_set_fusion levels
 
 
-def algorithmic_bytes(wl, k, fusion="sum"):
+def algorithmic_bytes(wl, k, fusion="sum", P=None):
     """Bytes the method must move per step, by kernel (see the design notes).
     fusion "sum": the compaction also writes g_bar, so the packed buffers are
     written but never re-read; "update": it also updates w and m at the k
-    selected coordinates (no index list or g_bar to read back)."""
-    P, W, G = wl.P, wl.W, _grad_bytes(wl)
+    selected coordinates (no index list or g_bar to read back).  P: the
+    parameters one rank's handle covers, when the shards are split."""
+    P, W, G = (wl.P if P is None else P), wl.W, _grad_bytes(wl)
     ntiles = (P + 2047) // 2048
     ef = W * P * (G + 8) + P / 8 + 4 * ntiles + 4 * k * W
     refresh = 4 * P + P / 8 + P / 8 + 4 * k
@@ -240,7 +243,8 @@ def workload_config(wl, args, ws=1):
                              min(wl.W, 12) if args.staging_rows is None else
                              (max(args.staging_rows, 3) if args.staging_rows else 0)),
             "l2": "inputs larger than L2 (gradients + residuals far beyond 129 MB)",
-            "parallelism": f"{ws} independent problems (weak)" if ws > 1 else "1 GPU"}
+            "parallelism": (f"one problem, its {wl.W} optimizer shards split over {ws} GPUs "
+                            f"(contiguous blocks; strong scaling)" if ws > 1 else "1 GPU")}
 
 
 # --------------------------------------------------------------------- oracle leg
@@ -389,7 +393,7 @@ def bench_reference(args, wl):
     line = {
         "impl": "reference", "metric": METRIC, "value": res["params_per_s"], "unit": UNIT,
         "n_gpus": ws, "steps": res["steps"], "warmup": args.warmup,
-        "ms_per_step": res["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": res["ms_per_step"], "higher_is_better": True, "scaling": "strong",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": workload_config(wl, args),
         "cpu_baseline": {"value": res["params_per_s"], "unit": UNIT, "cores": res["processes"],
@@ -515,12 +519,19 @@ def bench_gpu(args, wl):
 
     P, W = wl.P, wl.W
     gdt = torch.bfloat16 if wl.grad_dtype == "bf16" else torch.float32
-    seed = 1000 * rank
-    params = synth.init_params(P, seed=seed, device=dev)
+    seed = 0
+    # this rank's block of optimizer shards (all of them on one GPU)
+    if W < ws:
+        raise SystemExit(f"{W} optimizer shards cannot be split over {ws} GPUs")
+    shards = multirank.rank_shards(W, ws, rank)
+    lo, hi = multirank.shard_slice(P, W, shards)
+    params = synth.init_params(hi - lo, seed=seed + lo, device=dev)
     opt = pkg.Scape(params, W, wl.sparsity, layer_numel=[n for _, n in wl.layers],
-                    grad_dtype=gdt, residuals=args.residuals, staging_rows=args.staging_rows)
+                    grad_dtype=gdt, residuals=args.residuals, staging_rows=args.staging_rows,
+                    shard_range=(shards.start, shards.stop) if ws > 1 else None)
     opt.set_fusion(FUSION[args.fusion])
-    gen = synth.GradientStream(wl, seed=seed, device=dev)
+    # the slices [lo, hi) of the W workers' gradients
+    gen = synth.GradientStream(wl, seed=seed, device=dev, P=hi - lo, offset=lo)
     grads = gen.alloc()
 
     # warm-up: the dense first step and W - 1 lagged steps
@@ -569,8 +580,9 @@ def bench_gpu(args, wl):
         tt = torch.tensor([my_ms], device=dev, dtype=torch.float64)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         t_max = float(tt.item())
-    value = ws * P / (t_max / 1000.0)
-    alg = algorithmic_bytes(wl, opt.k, fusion=args.fusion)
+    value = multirank.strong_scaling_value(P, t_max / 1000.0)
+    alg = algorithmic_bytes(wl, opt.k, fusion=args.fusion, P=hi - lo)
+    alg_total = multirank.sum_over_ranks(alg["total"], device=dev)
     peak, peak_kind = _peaks()
 
     ef_ms, ef_n = prof_timed["ef_compact"]
@@ -595,12 +607,15 @@ def bench_gpu(args, wl):
     if args.e2e_steps > 0:
         e2e = bench_e2e(opt, wl, grads, args.e2e_steps, dev, shared_source=ws > 1)
         if ws > 1:
-            # whole job: every rank stepped P parameters; the slowest rank sets the time
+            # whole job: the ranks' slices make up the P parameters; the
+            # slowest rank sets the time
             t_e2e = multirank.max_over_ranks(e2e["ms_per_step"], device=dev)
             e2e["ms_per_step"] = t_e2e
-            e2e["value"] = ws * P / (t_e2e / 1000.0)
-            e2e["h2d_bytes_per_step"] *= ws
-            e2e["d2h_bytes_per_step"] *= ws
+            e2e["value"] = P / (t_e2e / 1000.0)
+            e2e["h2d_bytes_per_step"] = int(multirank.sum_over_ranks(e2e["h2d_bytes_per_step"],
+                                                                     device=dev))
+            e2e["d2h_bytes_per_step"] = int(multirank.sum_over_ranks(e2e["d2h_bytes_per_step"],
+                                                                     device=dev))
     opt.close()
     del grads, params, opt, gen
     torch.cuda.empty_cache()
@@ -632,11 +647,12 @@ def bench_gpu(args, wl):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t_max, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "scaling": "strong", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": config,
-            "hbm_gbs": alg["total"] / (t_max / 1000.0) / 1e9,
-            "hbm_frac": alg["total"] / (t_max / 1000.0) / 1e9 / peak,
-            "alg_bytes_per_step": alg["total"],
+            "hbm_gbs": alg_total / (t_max / 1000.0) / 1e9,
+            "hbm_frac": alg_total / (t_max / 1000.0) / 1e9 / (peak * ws),
+            "alg_bytes_per_step": alg_total,
+            "rank0_shards": [shards.start, shards.stop],
             "roofline": {"kernel": "ef_compact", "bound": "hbm", "achieved": ef_gbs,
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": ef_gbs / peak, "traffic": traffic,
@@ -802,7 +818,7 @@ def bench_e2e(opt, wl, dev_grads, steps, dev, shared_source=False):
     from pinned host memory, the step and refresh run, and w[P] is copied back."""
     import torch
 
-    P, W = wl.P, wl.W
+    P, W = opt.P, wl.W  # the parameters this rank's handle covers
     gdt = dev_grads[0].dtype
     esz = dev_grads[0].element_size()
     need = W * P * esz + 4 * P

@@ -80,6 +80,36 @@ int scape_create(scape_t **out, int n_layers, const int64_t *host_layer_numel, i
                  double sparsity, float beta1, float beta2, float lr, float eps,
                  float weight_decay, int grad_dtype);
 
+/*
+ * Create a handle for the optimizer shards [shard_begin, shard_end) of the
+ * problem scape_create() would lay out for these layers and W: one rank's
+ * share of the sharded optimizer ("SCAPE" Sec. II-A: the distributed optimizer
+ * partitions parameters and states evenly over the workers; "Sintesi Tecnica:
+ * SCAPE" Sec. 2: each worker computes the mask only for its own partition).
+ * The handle covers the contiguous parameters [lo, hi), lo = floor(shard_begin
+ * * P_global / W), hi = floor(shard_end * P_global / W), with the global shard
+ * boundaries and per-shard k_s; every buffer bound to it and every gradient
+ * passed to it is the [lo, hi) slice (local index 0 = global index lo).  Each
+ * step still takes W gradient slices (all workers) and averages over W.
+ * Because shards are independent, running every range of a partition of
+ * [0, W) gives, slice by slice, exactly the whole problem's results.  Bitmap,
+ * index list and packed buffers are in local coordinates (bit i of the
+ * handle's bitmap is global parameter lo + i).  scape_get_range() gives the
+ * range; scape_get_geometry() reports P = hi - lo and the shard_end -
+ * shard_begin local shards.
+ * Errors: as scape_create(), plus SCAPE_EINVAL unless 0 <= shard_begin <
+ * shard_end <= W and the range holds at least one parameter.
+ */
+int scape_create_range(scape_t **out, int n_layers, const int64_t *host_layer_numel, int W,
+                       int shard_begin, int shard_end, double sparsity, float beta1,
+                       float beta2, float lr, float eps, float weight_decay, int grad_dtype);
+
+/* Global size, offset of the first covered parameter and the covered shard
+ * range [shard_begin, shard_end) of a handle (0 and [0, W) for scape_create()
+ * handles).  Any output pointer may be NULL. */
+int scape_get_range(const scape_t *h, int64_t *P_global, int64_t *offset, int *shard_begin,
+                    int *shard_end);
+
 /* Release a handle (NULL is a no-op).  Does not free caller-owned memory. */
 void scape_destroy(scape_t *h);
 
@@ -87,10 +117,12 @@ void scape_destroy(scape_t *h);
 const char *scape_last_error(const scape_t *h);
 
 /*
- * Geometry of a handle: P, W, k and, when the host_ arrays are non-NULL, the
- * W + 1 shard boundaries and the W per-shard k_s (partitioned mask: each
- * worker selects only within its own optimizer shard, "Sintesi Tecnica:
- * SCAPE" Sec. 2).  Any output pointer may be NULL.
+ * Geometry of a handle: P (parameters covered), W (workers), k and, when the
+ * host_ arrays are non-NULL, the S + 1 local shard boundaries and the S
+ * per-shard k_s, S = W for scape_create() handles and shard_end - shard_begin
+ * for scape_create_range() ones (partitioned mask: each worker selects only
+ * within its own optimizer shard, "Sintesi Tecnica: SCAPE" Sec. 2).  Any
+ * output pointer may be NULL.
  */
 int scape_get_geometry(const scape_t *h, int64_t *P, int *W, int64_t *k,
                        int64_t *host_shard_start, int64_t *host_shard_k);

@@ -37,6 +37,9 @@ _vp, _i64, _i32, _f32, _f64 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ct
 _PROTOS = {
     "scape_create": (_i32, [ctypes.POINTER(_vp), _i32, _vp, _i32, _f64, _f32, _f32, _f32, _f32,
                             _f32, _i32]),
+    "scape_create_range": (_i32, [ctypes.POINTER(_vp), _i32, _vp, _i32, _i32, _i32, _f64, _f32,
+                                  _f32, _f32, _f32, _f32, _i32]),
+    "scape_get_range": (_i32, [_vp, _vp, _vp, _vp, _vp]),
     "scape_destroy": (None, [_vp]),
     "scape_last_error": (ctypes.c_char_p, [_vp]),
     "scape_get_geometry": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp]),
@@ -112,6 +115,28 @@ def scape_create(layer_numel, W, sparsity, beta1, beta2, lr, eps, weight_decay, 
     return h
 
 
+def scape_create_range(layer_numel, W, shard_begin, shard_end, sparsity, beta1, beta2, lr, eps,
+                       weight_decay, grad_dtype):
+    lib = load()
+    sizes = (ctypes.c_int64 * len(layer_numel))(*[int(n) for n in layer_numel])
+    h = ctypes.c_void_p()
+    rc = lib.scape_create_range(ctypes.byref(h), len(layer_numel), ctypes.addressof(sizes), int(W),
+                                int(shard_begin), int(shard_end), float(sparsity), beta1, beta2,
+                                lr, eps, weight_decay, int(grad_dtype))
+    if rc != SCAPE_OK:
+        raise ScapeError(rc, lib.scape_last_error(None).decode())
+    return h
+
+
+def scape_get_range(h):
+    Pg, off = ctypes.c_int64(), ctypes.c_int64()
+    a, b = ctypes.c_int(), ctypes.c_int()
+    _check(h, load().scape_get_range(h, ctypes.byref(Pg), ctypes.byref(off), ctypes.byref(a),
+                                     ctypes.byref(b)))
+    return {"P_global": Pg.value, "offset": off.value, "shard_begin": a.value,
+            "shard_end": b.value}
+
+
 def scape_destroy(h):
     load().scape_destroy(h)
 
@@ -124,8 +149,9 @@ def scape_get_geometry(h):
     P, W, k = ctypes.c_int64(), ctypes.c_int(), ctypes.c_int64()
     _check(h, load().scape_get_geometry(h, ctypes.byref(P), ctypes.byref(W), ctypes.byref(k),
                                         None, None))
-    start = (ctypes.c_int64 * (W.value + 1))()
-    ks = (ctypes.c_int64 * W.value)()
+    S = scape_get_range(h)["shard_end"] - scape_get_range(h)["shard_begin"]
+    start = (ctypes.c_int64 * (S + 1))()
+    ks = (ctypes.c_int64 * S)()
     _check(h, load().scape_get_geometry(h, None, None, None, ctypes.addressof(start),
                                         ctypes.addressof(ks)))
     return {"P": P.value, "W": W.value, "k": k.value, "shard_start": list(start),

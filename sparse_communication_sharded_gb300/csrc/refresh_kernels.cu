@@ -34,14 +34,15 @@ namespace {
 // straddles shard boundaries is processed one shard piece at a time.
 template <int PASS>
 __global__ void __launch_bounds__(256)
-radix_hist_kernel(const float* __restrict__ m, int64_t P, int W,
+radix_hist_kernel(const float* __restrict__ m, int64_t P, ShardMap sm,
                   const int64_t* __restrict__ shard_start, const ShardSel* __restrict__ sel,
                   uint32_t* __restrict__ hist) {
   constexpr int NB = (PASS == 2) ? 512 : kBins;
   __shared__ uint32_t sh[NB];
   const int64_t seg0 = (int64_t)blockIdx.x * kSeg;
   const int64_t seg1 = min(seg0 + (int64_t)kSeg, P);
-  int s = shard_of(seg0, P, W);
+  const int W = sm.S;
+  int s = sm.of(seg0);
   for (;;) {
     const int64_t s_lo = __ldg(shard_start + s), s_hi = __ldg(shard_start + s + 1);
     const int64_t lo = max(seg0, s_lo), hi = min(seg1, s_hi);
@@ -267,7 +268,8 @@ tie_select_kernel(const float* __restrict__ m, const int64_t* __restrict__ shard
 // parameters of one 16-byte load, the 4-bit pieces of 8 neighbouring lanes are
 // OR-ed into one 32-bit word by shuffles, and lane 8g writes word g of the round.
 __device__ __forceinline__ void mark_tile(int64_t tile, const float* __restrict__ m, int64_t P,
-                                          int W, const int64_t* __restrict__ shard_start,
+                                          const ShardMap& sm,
+                                          const int64_t* __restrict__ shard_start,
                                           const ShardSel* __restrict__ sel,
                                           uint32_t* __restrict__ bits,
                                           uint32_t* __restrict__ tile_cnt, bool accumulate) {
@@ -294,7 +296,7 @@ __device__ __forceinline__ void mark_tile(int64_t tile, const float* __restrict_
     }
   }
   if (threadIdx.x == 0) {
-    const int s0 = shard_of(t0, P, W);
+    const int s0 = sm.of(t0);
     const int64_t t1 = min(t0 + (int64_t)kTile, P);
     const int64_t ist = sel[s0].istar;
     const int64_t rel64 = ist - t0;
@@ -329,7 +331,7 @@ __device__ __forceinline__ void mark_tile(int64_t tile, const float* __restrict_
         const int64_t i = i0 + q;
         if (i < P) {
           int si = s;
-          while (si < W - 1 && i >= __ldg(shard_start + si + 1)) ++si;
+          while (si < sm.S - 1 && i >= __ldg(shard_start + si + 1)) ++si;
           const uint32_t kstar = sel[si].kstar;
           const int64_t istar = sel[si].istar;
           const uint32_t key = magnitude_key(x[q]);
@@ -355,10 +357,11 @@ __device__ __forceinline__ void mark_tile(int64_t tile, const float* __restrict_
 }
 
 __global__ void __launch_bounds__(128)
-mark_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __restrict__ shard_start,
+mark_kernel(const float* __restrict__ m, int64_t P, ShardMap sm,
+            const int64_t* __restrict__ shard_start,
             const ShardSel* __restrict__ sel, uint32_t* __restrict__ bits,
             uint32_t* __restrict__ tile_cnt, bool accumulate) {
-  mark_tile(blockIdx.x, m, P, W, shard_start, sel, bits, tile_cnt, accumulate);
+  mark_tile(blockIdx.x, m, P, sm, shard_start, sel, bits, tile_cnt, accumulate);
 }
 
 // Warm refresh, grid (G, W): the tiles starting in shard s that the
@@ -366,7 +369,7 @@ mark_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __rest
 // kSelRemark, else only its last one when it crosses the shard's end (or the
 // end of the vector).  Each tile is owned by the shard it starts in.
 __global__ void __launch_bounds__(128)
-remark_kernel(const float* __restrict__ m, int64_t P, int W,
+remark_kernel(const float* __restrict__ m, int64_t P, ShardMap sm,
               const int64_t* __restrict__ shard_start, const ShardSel* __restrict__ sel,
               uint32_t* __restrict__ bits, uint32_t* __restrict__ tile_cnt) {
   const int s = blockIdx.y;
@@ -379,7 +382,7 @@ remark_kernel(const float* __restrict__ m, int64_t P, int W,
     t_begin = t_end - 1;
   }
   for (int64_t t = t_begin + blockIdx.x; t < t_end; t += gridDim.x)
-    mark_tile(t, m, P, W, shard_start, sel, bits, tile_cnt, false);
+    mark_tile(t, m, P, sm, shard_start, sel, bits, tile_cnt, false);
 }
 
 // Per-tile popcount of an existing bitmap (checkpoint resume).
@@ -514,7 +517,7 @@ index_kernel(const uint32_t* __restrict__ bits, int64_t P, int64_t ntiles,
 // Per-shard popcount of a bitmap plus the count of bits set past P (in
 // counts[W]); used to validate a restored mask.
 __global__ void __launch_bounds__(256)
-shard_count_kernel(const uint32_t* __restrict__ bits, int64_t P, int64_t nwords, int W,
+shard_count_kernel(const uint32_t* __restrict__ bits, int64_t P, int64_t nwords, ShardMap sm,
                    uint32_t* __restrict__ counts) {
   const int64_t wi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (wi >= nwords) return;
@@ -523,20 +526,21 @@ shard_count_kernel(const uint32_t* __restrict__ bits, int64_t P, int64_t nwords,
     const int b = __ffs(word) - 1;
     word &= word - 1;
     const int64_t i = wi * 32 + b;
-    if (i >= P) atomicAdd(counts + W, 1u);
-    else atomicAdd(counts + shard_of(i, P, W), 1u);
+    if (i >= P) atomicAdd(counts + sm.S, 1u);
+    else atomicAdd(counts + sm.of(i), 1u);
   }
 }
 
 }  // namespace
 
 // ------------------------------------------------------------------ launchers
-cudaError_t launch_hist(int pass, const float* m, int64_t P, int W, const int64_t* shard_start,
-                        const ShardSel* sel, uint32_t* hist, cudaStream_t st) {
+cudaError_t launch_hist(int pass, const float* m, int64_t P, const ShardMap& sm,
+                        const int64_t* shard_start, const ShardSel* sel, uint32_t* hist,
+                        cudaStream_t st) {
   const unsigned grid = (unsigned)((P + kSeg - 1) / kSeg);
-  if (pass == 0) radix_hist_kernel<0><<<grid, 256, 0, st>>>(m, P, W, shard_start, sel, hist);
-  else if (pass == 1) radix_hist_kernel<1><<<grid, 256, 0, st>>>(m, P, W, shard_start, sel, hist);
-  else radix_hist_kernel<2><<<grid, 256, 0, st>>>(m, P, W, shard_start, sel, hist);
+  if (pass == 0) radix_hist_kernel<0><<<grid, 256, 0, st>>>(m, P, sm, shard_start, sel, hist);
+  else if (pass == 1) radix_hist_kernel<1><<<grid, 256, 0, st>>>(m, P, sm, shard_start, sel, hist);
+  else radix_hist_kernel<2><<<grid, 256, 0, st>>>(m, P, sm, shard_start, sel, hist);
   return cudaGetLastError();
 }
 
@@ -562,26 +566,27 @@ cudaError_t launch_tie_select(const float* m, int W, const int64_t* shard_start,
   return cudaGetLastError();
 }
 
-cudaError_t launch_mark(const float* m, int64_t P, int W, const int64_t* shard_start,
+cudaError_t launch_mark(const float* m, int64_t P, const ShardMap& sm, const int64_t* shard_start,
                         const ShardSel* sel, uint32_t* bits, uint32_t* tile_cnt,
                         cudaStream_t st, bool accumulate) {
   const unsigned grid = (unsigned)((P + kTile - 1) / kTile);
-  mark_kernel<<<grid, 128, 0, st>>>(m, P, W, shard_start, sel, bits, tile_cnt, accumulate);
+  mark_kernel<<<grid, 128, 0, st>>>(m, P, sm, shard_start, sel, bits, tile_cnt, accumulate);
   return cudaGetLastError();
 }
 
-cudaError_t launch_remark(const float* m, int64_t P, int W, const int64_t* shard_start,
+cudaError_t launch_remark(const float* m, int64_t P, const ShardMap& sm, const int64_t* shard_start,
                           const ShardSel* sel, uint32_t* bits, uint32_t* tile_cnt,
                           cudaStream_t st) {
   // enough 128-thread blocks to fill the GPU when every shard is re-marked;
   // in the common case all but one block per shard return at once
   const int sms = sm_count();
+  const int W = sm.S;
   const int64_t ntiles = (P + kTile - 1) / kTile;
   const int64_t per_shard = (ntiles + W - 1) / W + 1;
   int64_t gx = ((int64_t)sms * 16 + W - 1) / W;
   if (gx > per_shard) gx = per_shard;
   if (gx < 1) gx = 1;
-  remark_kernel<<<dim3((unsigned)gx, (unsigned)W), 128, 0, st>>>(m, P, W, shard_start, sel, bits,
+  remark_kernel<<<dim3((unsigned)gx, (unsigned)W), 128, 0, st>>>(m, P, sm, shard_start, sel, bits,
                                                                  tile_cnt);
   return cudaGetLastError();
 }
@@ -629,9 +634,9 @@ cudaError_t launch_index(const uint32_t* bits, int64_t P, const uint32_t* tile_b
   return cudaGetLastError();
 }
 
-cudaError_t launch_shard_count(const uint32_t* bits, int64_t P, int64_t nwords, int W,
+cudaError_t launch_shard_count(const uint32_t* bits, int64_t P, int64_t nwords, const ShardMap& sm,
                                uint32_t* counts, cudaStream_t st) {
-  shard_count_kernel<<<(unsigned)((nwords + 255) / 256), 256, 0, st>>>(bits, P, nwords, W, counts);
+  shard_count_kernel<<<(unsigned)((nwords + 255) / 256), 256, 0, st>>>(bits, P, nwords, sm, counts);
   return cudaGetLastError();
 }
 

@@ -64,9 +64,15 @@ struct ProfRec {
 
 struct scape {
   // configuration
-  int64_t P = 0;
-  int W = 0;
+  int64_t P = 0;       // parameters this handle covers
+  int W = 0;           // workers (gradient slices per step)
+  int S = 0;           // optimizer shards this handle covers
   int64_t ppm = 0;
+  // global layout: shards [shard_begin, shard_begin + S) of an even W-way split
+  // of P_global parameters, the first at global index offset
+  int64_t P_global = 0, offset = 0;
+  int shard_begin = 0;
+  ShardMap map{};
   float beta1 = 0, beta2 = 0, lr = 0, eps = 0, wd = 0;
   int dtype = SCAPE_BF16;
   std::vector<int64_t> shard_start, shard_k;
@@ -128,8 +134,8 @@ struct scape {
   ShardSel* sel() const { return at<ShardSel>(off_sel); }
   uint2* cand() const { return at<uint2>(off_cand); }
   uint32_t* cand_cnt() const { return at<uint32_t>(off_ccnt); }
-  uint32_t* above_cnt() const { return at<uint32_t>(off_ccnt) + W; }
-  uint32_t* nar_cnt() const { return at<uint32_t>(off_ccnt) + 2 * W; }
+  uint32_t* above_cnt() const { return at<uint32_t>(off_ccnt) + S; }
+  uint32_t* nar_cnt() const { return at<uint32_t>(off_ccnt) + 2 * S; }
   uint2* nar() const { return at<uint2>(off_nar); }
   uint32_t* scan_scratch() const { return at<uint32_t>(off_scan); }
   int64_t* d_shard_start() const { return at<int64_t>(off_sstart); }
@@ -333,11 +339,13 @@ int step_staged(scape_t* h, const WorkerPtrs& grads, bool vec, const AdamsConst&
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-int scape_create(scape_t** out, int n_layers, const int64_t* host_layer_numel, int W,
-                 double sparsity, float beta1, float beta2, float lr, float eps,
-                 float weight_decay, int grad_dtype) {
+// Handle for shards [a, b) of the even W-way split of the layers' P_global
+// parameters (a = 0, b = W: the whole problem).
+int create_handle(scape_t** out, int n_layers, const int64_t* host_layer_numel, int W, int a,
+                  int b, double sparsity, float beta1, float beta2, float lr, float eps,
+                  float weight_decay, int grad_dtype) {
   g_create_error.clear();
   auto bad = [&](const char* msg) {
     g_create_error = msg;
@@ -354,6 +362,9 @@ int scape_create(scape_t** out, int n_layers, const int64_t* host_layer_numel, i
   }
   if (P < 1) return bad("P must be >= 1");
   if (W < 1 || W > SCAPE_MAX_WORKERS) return bad("W out of range [1, SCAPE_MAX_WORKERS]");
+  if (a < 0 || b > W || a >= b) return bad("shard range must satisfy 0 <= begin < end <= W");
+  const int64_t lo = ((int64_t)a * P) / W, hi = ((int64_t)b * P) / W;
+  if (hi <= lo) return bad("the shard range holds no parameter");
   if (!(sparsity >= 0.0 && sparsity < 1.0)) return bad("sparsity must be in [0, 1)");
   const int64_t ppm = std::llround(sparsity * 1e6);
   if (ppm >= 1000000) return bad("sparsity rounds to 1 (nothing would be sent)");
@@ -367,8 +378,13 @@ int scape_create(scape_t** out, int n_layers, const int64_t* host_layer_numel, i
 
   scape_t* h = new (std::nothrow) scape_t();
   if (!h) return bad("out of host memory");
-  h->P = P;
+  h->P = hi - lo;
   h->W = W;
+  h->S = b - a;
+  h->P_global = P;
+  h->offset = lo;
+  h->shard_begin = a;
+  h->map = ShardMap{P, lo, W, a, b - a};
   h->ppm = ppm;
   h->beta1 = beta1;
   h->beta2 = beta2;
@@ -376,23 +392,26 @@ int scape_create(scape_t** out, int n_layers, const int64_t* host_layer_numel, i
   h->eps = eps;
   h->wd = weight_decay;
   h->dtype = grad_dtype;
-  h->shard_start.resize(W + 1);
-  h->shard_k.resize(W);
+  const int S = b - a;
+  h->shard_start.resize(S + 1);
+  h->shard_k.resize(S);
   int64_t nmax = 0;
   h->all_dense = true;
-  for (int s = 0; s <= W; ++s) h->shard_start[s] = ((int64_t)s * P) / W;
-  for (int s = 0; s < W; ++s) {
+  // local boundaries: the global ones of shards a..b, less the range's start
+  for (int s = 0; s <= S; ++s) h->shard_start[s] = ((int64_t)(a + s) * P) / W - lo;
+  for (int s = 0; s < S; ++s) {
     const int64_t n = h->shard_start[s + 1] - h->shard_start[s];
     h->shard_k[s] = (n * (1000000 - ppm) + 999999) / 1000000;
     h->k += h->shard_k[s];
     nmax = n > nmax ? n : nmax;
     if (h->shard_k[s] != n) h->all_dense = false;
   }
+  P = h->P;  // from here on: the parameters this handle covers
   h->ntiles = (P + kTile - 1) / kTile;
   h->nwords = (P + 31) / 32;
   h->kstride = (int64_t)align_up((size_t)(h->k > 0 ? h->k : 1), 64);
   // candidate passes: about 1200 blocks in total, at least one per shard
-  h->cand_blocks = W >= 1200 ? 1 : 1200 / W;
+  h->cand_blocks = S >= 1200 ? 1 : 1200 / S;
   (void)nmax;
 
   size_t off = 0;
@@ -407,19 +426,37 @@ int scape_create(scape_t** out, int n_layers, const int64_t* host_layer_numel, i
   h->off_tcnt = carve((size_t)h->ntiles * 4);
   h->off_pack = carve((size_t)W * h->kstride * 4);
   h->off_gbar = carve((size_t)h->kstride * 4);
-  h->off_hist = carve((size_t)W * kCandBins0 * 4);
-  h->off_sel = carve((size_t)W * sizeof(ShardSel));
+  h->off_hist = carve((size_t)S * kCandBins0 * 4);
+  h->off_sel = carve((size_t)S * sizeof(ShardSel));
   // candidates of shard s live in [shard_start[s], shard_start[s+1]): capacity = shard size
   h->off_cand = carve((size_t)P * sizeof(uint2));
-  h->off_ccnt = carve((size_t)W * 3 * 4);  // candidate, above-window and narrow-row counts
-  h->off_nar = carve((size_t)W * kNarrowCap * sizeof(uint2));
+  h->off_ccnt = carve((size_t)S * 3 * 4);  // candidate, above-window and narrow-row counts
+  h->off_nar = carve((size_t)S * kNarrowCap * sizeof(uint2));
   h->off_scan = carve((size_t)scan_scratch_words(h->ntiles) * 4);
-  h->off_sstart = carve((size_t)(W + 1) * 8);
-  h->off_sk = carve((size_t)W * 8);
-  h->off_counts = carve((size_t)(W + 1) * 4);
+  h->off_sstart = carve((size_t)(S + 1) * 8);
+  h->off_sk = carve((size_t)S * 8);
+  h->off_counts = carve((size_t)(S + 1) * 4);
   h->ws_need = off;
   *out = h;
   return SCAPE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int scape_create(scape_t** out, int n_layers, const int64_t* host_layer_numel, int W,
+                 double sparsity, float beta1, float beta2, float lr, float eps,
+                 float weight_decay, int grad_dtype) {
+  return create_handle(out, n_layers, host_layer_numel, W, 0, W, sparsity, beta1, beta2, lr, eps,
+                       weight_decay, grad_dtype);
+}
+
+int scape_create_range(scape_t** out, int n_layers, const int64_t* host_layer_numel, int W,
+                       int shard_begin, int shard_end, double sparsity, float beta1, float beta2,
+                       float lr, float eps, float weight_decay, int grad_dtype) {
+  return create_handle(out, n_layers, host_layer_numel, W, shard_begin, shard_end, sparsity,
+                       beta1, beta2, lr, eps, weight_decay, grad_dtype);
 }
 
 void scape_destroy(scape_t* h) {
@@ -454,8 +491,18 @@ int scape_get_geometry(const scape_t* h, int64_t* P, int* W, int64_t* k, int64_t
   if (W) *W = h->W;
   if (k) *k = h->k;
   if (host_shard_start)
-    std::memcpy(host_shard_start, h->shard_start.data(), sizeof(int64_t) * (h->W + 1));
-  if (host_shard_k) std::memcpy(host_shard_k, h->shard_k.data(), sizeof(int64_t) * h->W);
+    std::memcpy(host_shard_start, h->shard_start.data(), sizeof(int64_t) * (h->S + 1));
+  if (host_shard_k) std::memcpy(host_shard_k, h->shard_k.data(), sizeof(int64_t) * h->S);
+  return SCAPE_OK;
+}
+
+int scape_get_range(const scape_t* h, int64_t* P_global, int64_t* offset, int* shard_begin,
+                    int* shard_end) {
+  if (!h) return SCAPE_EINVAL;
+  if (P_global) *P_global = h->P_global;
+  if (offset) *offset = h->offset;
+  if (shard_begin) *shard_begin = h->shard_begin;
+  if (shard_end) *shard_end = h->shard_begin + h->S;
   return SCAPE_OK;
 }
 
@@ -497,13 +544,13 @@ int scape_bind(scape_t* h, float* params, float* m, float* const* host_e_ptrs, v
   h->m = m;
   h->ws = static_cast<char*>(workspace);
   // the small shard table lives in the workspace for the kernels
-  cudaError_t e = cudaMemcpy(h->d_shard_start(), h->shard_start.data(), 8 * (h->W + 1),
+  cudaError_t e = cudaMemcpy(h->d_shard_start(), h->shard_start.data(), 8 * (h->S + 1),
                              cudaMemcpyHostToDevice);
   if (e == cudaSuccess)
-    e = cudaMemcpy(h->d_shard_k(), h->shard_k.data(), 8 * h->W, cudaMemcpyHostToDevice);
+    e = cudaMemcpy(h->d_shard_k(), h->shard_k.data(), 8 * h->S, cudaMemcpyHostToDevice);
   if (e != cudaSuccess) return cuda_fail(h, e, "scape_bind: shard table upload");
   // no previous mask: every shard starts without a bucket guess
-  e = cudaMemset(h->sel(), 0xFF, sizeof(ShardSel) * h->W);
+  e = cudaMemset(h->sel(), 0xFF, sizeof(ShardSel) * h->S);
   if (e != cudaSuccess) return cuda_fail(h, e, "scape_bind: select state reset");
   h->bound = true;
   h->t = 0;
@@ -560,12 +607,12 @@ namespace {
 int enqueue_radix(scape_t* h, cudaStream_t st) {
   for (int pass = 1; pass <= 5; ++pass) {
     int rc = run_kernel(h, kKCandHist, st, [&] {
-      return launch_chist(pass, h->W, h->cand_blocks, h->d_shard_start(), h->sel(), h->cand(),
+      return launch_chist(pass, h->S, h->cand_blocks, h->d_shard_start(), h->sel(), h->cand(),
                           h->cand_cnt(), h->hist(), h->nar(), h->nar_cnt(), kNarrowCap, st);
     });
     if (rc) return rc;
     rc = run_kernel(h, kKCandSelect, st, [&] {
-      return launch_cselect(pass, h->W, h->d_shard_start(), h->d_shard_k(), h->sel(), h->hist(),
+      return launch_cselect(pass, h->S, h->d_shard_start(), h->d_shard_k(), h->sel(), h->hist(),
                             h->cand_cnt(), kSelFormCold, st);
     });
     if (rc) return rc;
@@ -578,23 +625,23 @@ int enqueue_radix(scape_t* h, cudaStream_t st) {
 int refresh_cold(scape_t* h, cudaStream_t st) {
   int rc;
   if (!h->all_dense) {
-    cudaError_t e = cudaMemsetAsync(h->hist(), 0, (size_t)h->W * kCandBins0 * 4, st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(h->cand_cnt(), 0, (size_t)h->W * 3 * 4, st);
+    cudaError_t e = cudaMemsetAsync(h->hist(), 0, (size_t)h->S * kCandBins0 * 4, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->cand_cnt(), 0, (size_t)h->S * 3 * 4, st);
     if (e != cudaSuccess) return cuda_fail(h, e, "scape_refresh_mask: histogram clear");
     rc = run_kernel(h, kKCandHist0, st, [&] {
-      return launch_chist0(h->m, h->P, h->W, h->d_shard_start(), h->sel(), h->hist(), h->cand(),
+      return launch_chist0(h->m, h->P, h->map, h->d_shard_start(), h->sel(), h->hist(), h->cand(),
                            h->cand_cnt(), false, st);
     });
     if (rc) return rc;
   }
   rc = run_kernel(h, kKCandSelect, st, [&] {
-    return launch_cselect(0, h->W, h->d_shard_start(), h->d_shard_k(), h->sel(), h->hist(),
+    return launch_cselect(0, h->S, h->d_shard_start(), h->d_shard_k(), h->sel(), h->hist(),
                           h->cand_cnt(), kSelFormCold, st);
   });
   if (rc) return rc;
   if (!h->all_dense) {
     rc = run_kernel(h, kKCandCollect, st, [&] {
-      return launch_collect(h->m, h->P, h->W, h->d_shard_start(), h->sel(), h->cand(),
+      return launch_collect(h->m, h->P, h->map, h->d_shard_start(), h->sel(), h->cand(),
                             h->cand_cnt(), st);
     });
     if (rc) return rc;
@@ -602,7 +649,7 @@ int refresh_cold(scape_t* h, cudaStream_t st) {
     if (rc) return rc;
   }
   return run_kernel(h, kKMark, st, [&] {
-    return launch_mark(h->m, h->P, h->W, h->d_shard_start(), h->sel(), h->bits(), h->tile_cnt(),
+    return launch_mark(h->m, h->P, h->map, h->d_shard_start(), h->sel(), h->bits(), h->tile_cnt(),
                        st);
   });
 }
@@ -616,48 +663,48 @@ int refresh_warm(scape_t* h, cudaStream_t st) {
   // the histogram rows need no clearing: every refresh leaves them zero (each
   // select pass clears the rows it read, and rows of shards no pass reads are
   // never written); the cold refresh after a bind clears them once
-  cudaError_t e = cudaMemsetAsync(h->cand_cnt(), 0, (size_t)h->W * 3 * 4, st);
+  cudaError_t e = cudaMemsetAsync(h->cand_cnt(), 0, (size_t)h->S * 3 * 4, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(h->tile_cnt(), 0, (size_t)h->ntiles * 4, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "scape_refresh_mask: count clear");
   int rc = run_kernel(h, kKSpecMark, st, [&] {
-    return launch_spec(h->m, h->P, h->W, h->d_shard_start(), h->sel(), h->cand(), h->cand_cnt(),
+    return launch_spec(h->m, h->P, h->map, h->d_shard_start(), h->sel(), h->cand(), h->cand_cnt(),
                        h->above_cnt(), h->bits(), h->tile_cnt(), st);
   });
   if (rc) return rc;
   rc = run_kernel(h, kKCandHist, st, [&] {
-    return launch_whist(h->W, h->cand_blocks, h->d_shard_start(), h->sel(), h->cand(),
+    return launch_whist(h->S, h->cand_blocks, h->d_shard_start(), h->sel(), h->cand(),
                         h->cand_cnt(), h->above_cnt(), h->hist(), st);
   });
   if (rc) return rc;
   rc = run_kernel(h, kKCandSelect, st, [&] {
-    return launch_cselect(0, h->W, h->d_shard_start(), h->d_shard_k(), h->sel(), h->hist(),
+    return launch_cselect(0, h->S, h->d_shard_start(), h->d_shard_k(), h->sel(), h->hist(),
                           h->cand_cnt(), kSelFormWarm, st);
   });
   if (rc) return rc;
   rc = run_kernel(h, kKCandHist0, st, [&] {
-    return launch_chist0(h->m, h->P, h->W, h->d_shard_start(), h->sel(), h->hist(), h->cand(),
+    return launch_chist0(h->m, h->P, h->map, h->d_shard_start(), h->sel(), h->hist(), h->cand(),
                          h->cand_cnt(), true, st);
   });
   if (rc) return rc;
   rc = run_kernel(h, kKCandSelect, st, [&] {
-    return launch_cselect(0, h->W, h->d_shard_start(), h->d_shard_k(), h->sel(), h->hist(),
+    return launch_cselect(0, h->S, h->d_shard_start(), h->d_shard_k(), h->sel(), h->hist(),
                           h->cand_cnt(), kSelFormRerun, st);
   });
   if (rc) return rc;
   rc = run_kernel(h, kKCandCollect, st, [&] {
-    return launch_collect(h->m, h->P, h->W, h->d_shard_start(), h->sel(), h->cand(),
+    return launch_collect(h->m, h->P, h->map, h->d_shard_start(), h->sel(), h->cand(),
                           h->cand_cnt(), st);
   });
   if (rc) return rc;
   rc = enqueue_radix(h, st);
   if (rc) return rc;
   rc = run_kernel(h, kKFixup, st, [&] {
-    return launch_fixup(h->d_shard_start(), h->sel(), h->cand(), h->cand_cnt(), h->W,
+    return launch_fixup(h->d_shard_start(), h->sel(), h->cand(), h->cand_cnt(), h->S,
                         h->cand_blocks, h->bits(), h->tile_cnt(), st);
   });
   if (rc) return rc;
   return run_kernel(h, kKRemark, st, [&] {
-    return launch_remark(h->m, h->P, h->W, h->d_shard_start(), h->sel(), h->bits(),
+    return launch_remark(h->m, h->P, h->map, h->d_shard_start(), h->sel(), h->bits(),
                          h->tile_cnt(), st);
   });
 }
@@ -863,7 +910,7 @@ int scape_union_step(scape_t* h, const void* const* host_grad_ptrs, void* worksp
       if (e == cudaSuccess) e = cudaMemsetAsync(ucnt, 0, 4, st);
       if (e != cudaSuccess) return cuda_fail(h, e, "scape_union_step: histogram clear");
       rc = run_kernel(h, kKCandHist0, st, [&] {
-        return launch_chist0(a, h->P, 1, ustart, sw, uhist, ucand, ucnt, false, st);
+        return launch_chist0(a, h->P, whole_map(h->P, 1), ustart, sw, uhist, ucand, ucnt, false, st);
       });
       if (rc) return rc;
     }
@@ -872,7 +919,7 @@ int scape_union_step(scape_t* h, const void* const* host_grad_ptrs, void* worksp
     if (rc) return rc;
     if (kw < h->P) {
       rc = run_kernel(h, kKCandCollect, st, [&] {
-        return launch_collect(a, h->P, 1, ustart, sw, ucand, ucnt, st);
+        return launch_collect(a, h->P, whole_map(h->P, 1), ustart, sw, ucand, ucnt, st);
       });
       if (rc) return rc;
       for (int pass = 1; pass <= 5; ++pass) {
@@ -887,7 +934,7 @@ int scape_union_step(scape_t* h, const void* const* host_grad_ptrs, void* worksp
       }
     }
     rc = run_kernel(h, kKMark, st, [&] {
-      return launch_mark(a, h->P, 1, ustart, sw, ubits, utcnt, st, /*accumulate=*/true);
+      return launch_mark(a, h->P, whole_map(h->P, 1), ustart, sw, ubits, utcnt, st, /*accumulate=*/true);
     });
     if (rc) return rc;
   }
@@ -959,21 +1006,21 @@ int scape_set_state(scape_t* h, int64_t t, const uint32_t* bits, void* stream) {
   if (t < 1 || !bits) return fail(h, SCAPE_EINVAL, "scape_set_state: need t >= 1 and a bitmap");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemcpyAsync(h->bits(), bits, (size_t)h->nwords * 4, cudaMemcpyDeviceToDevice, st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(h->counts(), 0, (size_t)(h->W + 1) * 4, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(h->counts(), 0, (size_t)(h->S + 1) * 4, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "scape_set_state: copy");
   int rc = run_kernel(h, kKShardCount, st, [&] {
-    return launch_shard_count(h->bits(), h->P, h->nwords, h->W, h->counts(), st);
+    return launch_shard_count(h->bits(), h->P, h->nwords, h->map, h->counts(), st);
   });
   if (rc) return rc;
-  std::vector<uint32_t> cnt(h->W + 1);
-  e = cudaMemcpyAsync(cnt.data(), h->counts(), (size_t)(h->W + 1) * 4, cudaMemcpyDeviceToHost, st);
+  std::vector<uint32_t> cnt(h->S + 1);
+  e = cudaMemcpyAsync(cnt.data(), h->counts(), (size_t)(h->S + 1) * 4, cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(h, e, "scape_set_state: count readback");
-  if (cnt[h->W] != 0) {
+  if (cnt[h->S] != 0) {
     h->mask_ready = false;
     return fail(h, SCAPE_EINVAL, "scape_set_state: bitmap has bits set past P");
   }
-  for (int s = 0; s < h->W; ++s) {
+  for (int s = 0; s < h->S; ++s) {
     if ((int64_t)cnt[s] != h->shard_k[s]) {
       h->mask_ready = false;
       char buf[160];

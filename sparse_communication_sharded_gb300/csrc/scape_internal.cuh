@@ -98,10 +98,25 @@ __device__ __forceinline__ uint32_t magnitude_key(float x) {
   return __float_as_uint(x) & 0x7FFFFFFFu;
 }
 
-// Shard owning parameter i (0 <= i < P): the largest s with floor(s*P/W) <= i.
-__device__ __forceinline__ int shard_of(int64_t i, int64_t P, int W) {
-  return (int)(((i + 1) * (int64_t)W - 1) / P);
-}
+// The shards a handle covers: S consecutive optimizer shards a .. a + S - 1 of
+// an even Wg-way split of Pg parameters ("SCAPE" Sec. II-A: the distributed
+// optimizer partitions the states evenly), whose first parameter is global
+// index `off`; local parameter i is global parameter off + i.  A whole-problem
+// handle has Pg = P, off = 0, Wg = S, a = 0.
+struct ShardMap {
+  int64_t Pg;
+  int64_t off;
+  int Wg;
+  int a;
+  int S;
+  // local shard holding local parameter i: the largest global s with
+  // floor(s * Pg / Wg) <= off + i, minus a
+  __device__ __forceinline__ int of(int64_t i) const {
+    return (int)(((i + off + 1) * (int64_t)Wg - 1) / Pg) - a;
+  }
+};
+
+inline ShardMap whole_map(int64_t P, int S) { return ShardMap{P, 0, S, 0, S}; }
 
 // Exclusive prefix sum over a block of NT threads (NT a multiple of 32).
 // `warp_tot` holds NT/32 words of shared memory; callers __syncthreads()
@@ -228,7 +243,8 @@ cudaError_t launch_reduce(const float* pack, int64_t pack_stride, int W, int64_t
 cudaError_t launch_adams_sparse(const uint32_t* idx, const float* gbar, int64_t k, float* w,
                                 float* m, const AdamsConst& c, bool msync, cudaStream_t st);
 
-cudaError_t launch_hist(int pass, const float* m, int64_t P, int W, const int64_t* shard_start,
+cudaError_t launch_hist(int pass, const float* m, int64_t P, const ShardMap& sm,
+                        const int64_t* shard_start,
                         const ShardSel* sel, uint32_t* hist, cudaStream_t st);
 cudaError_t launch_select(int pass, int W, const int64_t* shard_start, const int64_t* shard_k,
                           ShardSel* sel, uint32_t* hist, cudaStream_t st);
@@ -238,7 +254,7 @@ cudaError_t launch_tie_count(const float* m, int W, const int64_t* shard_start,
 cudaError_t launch_tie_select(const float* m, int W, const int64_t* shard_start, ShardSel* sel,
                               const uint32_t* eqcnt, int64_t nchunk, cudaStream_t st);
 // accumulate: OR the new bits into `bits` instead of overwriting them.
-cudaError_t launch_mark(const float* m, int64_t P, int W, const int64_t* shard_start,
+cudaError_t launch_mark(const float* m, int64_t P, const ShardMap& sm, const int64_t* shard_start,
                         const ShardSel* sel, uint32_t* bits, uint32_t* tile_cnt,
                         cudaStream_t st, bool accumulate = false);
 // union-mask baseline (union_kernels.cu)
@@ -264,14 +280,14 @@ constexpr int kDigit0 = 13;
 constexpr int kKeyShift0 = 31 - kDigit0;
 constexpr int kCandBins0 = 1 << kDigit0;
 // selective: only shards flagged kSelNeedHist, and nothing staged.
-cudaError_t launch_chist0(const float* m, int64_t P, int W, const int64_t* shard_start,
+cudaError_t launch_chist0(const float* m, int64_t P, const ShardMap& sm, const int64_t* shard_start,
                           const ShardSel* sel, uint32_t* hist, uint2* cand, uint32_t* cand_cnt,
                           bool selective, cudaStream_t st);
 // Warm refresh: one read of m that writes the bitmap words and popcounts of
 // every whole single-shard tile from the shard's previous threshold (tile_cnt
 // zeroed first), stages the candidates of the previous bucket window and counts
 // the parameters above it (above_cnt zeroed first).
-cudaError_t launch_spec(const float* m, int64_t P, int W, const int64_t* shard_start,
+cudaError_t launch_spec(const float* m, int64_t P, const ShardMap& sm, const int64_t* shard_start,
                         const ShardSel* sel, uint2* cand, uint32_t* cand_cnt, uint32_t* above_cnt,
                         uint32_t* bits, uint32_t* tile_cnt, cudaStream_t st);
 // Window histogram of the staged candidates with the outside counts lumped.
@@ -286,7 +302,7 @@ cudaError_t launch_fixup(const int64_t* shard_start, const ShardSel* sel, const 
 // Mark the tiles the speculative bitmap does not cover: every tile starting in
 // a kSelRemark shard, and each shard's last tile when it crosses the shard end
 // or the end of the vector.
-cudaError_t launch_remark(const float* m, int64_t P, int W, const int64_t* shard_start,
+cudaError_t launch_remark(const float* m, int64_t P, const ShardMap& sm, const int64_t* shard_start,
                           const ShardSel* sel, uint32_t* bits, uint32_t* tile_cnt,
                           cudaStream_t st);
 // form (pass 0): kSelFormCold on a full histogram, kSelFormWarm on the window
@@ -295,7 +311,7 @@ constexpr int kSelFormCold = 0, kSelFormWarm = 1, kSelFormRerun = 2;
 cudaError_t launch_cselect(int pass, int W, const int64_t* shard_start, const int64_t* shard_k,
                            ShardSel* sel, uint32_t* hist, uint32_t* cand_cnt, int form,
                            cudaStream_t st);
-cudaError_t launch_collect(const float* m, int64_t P, int W, const int64_t* shard_start,
+cudaError_t launch_collect(const float* m, int64_t P, const ShardMap& sm, const int64_t* shard_start,
                            const ShardSel* sel, uint2* cand, uint32_t* cand_cnt, cudaStream_t st);
 // nar (optional): per-shard rows of nar_cap candidates, counts in nar_cnt
 // (zeroed before pass 2): pass 2 narrows the list there for passes 3 to 5.
@@ -304,7 +320,7 @@ cudaError_t launch_chist(int pass, int W, int blocks_per_shard, const int64_t* s
                          const ShardSel* sel, const uint2* cand, const uint32_t* cand_cnt,
                          uint32_t* hist, uint2* nar, uint32_t* nar_cnt, uint32_t nar_cap,
                          cudaStream_t st);
-cudaError_t launch_shard_count(const uint32_t* bits, int64_t P, int64_t nwords, int W,
+cudaError_t launch_shard_count(const uint32_t* bits, int64_t P, int64_t nwords, const ShardMap& sm,
                                uint32_t* counts, cudaStream_t st);
 
 }  // namespace scapek

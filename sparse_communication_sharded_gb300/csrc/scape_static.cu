@@ -137,12 +137,12 @@ extern "C" int scape_topk_mask_static(const float* m, int64_t P, int W, double s
   if (e != cudaSuccess) return SCAPE_ECUDA;
   static_layout_kernel<<<1, 128, 0, st>>>(P, W, ppm);
   if ((e = cudaGetLastError()) != cudaSuccess) return SCAPE_ECUDA;
-  if (!all_dense && (e = launch_hist(0, m, P, W, start, sel, hist, st)) != cudaSuccess)
+  if (!all_dense && (e = launch_hist(0, m, P, whole_map(P, W), start, sel, hist, st)) != cudaSuccess)
     return SCAPE_ECUDA;
   if ((e = launch_select(0, W, start, ks, sel, hist, st)) != cudaSuccess) return SCAPE_ECUDA;
   if (!all_dense) {
     for (int pass = 1; pass <= 2; ++pass) {
-      if ((e = launch_hist(pass, m, P, W, start, sel, hist, st)) != cudaSuccess) return SCAPE_ECUDA;
+      if ((e = launch_hist(pass, m, P, whole_map(P, W), start, sel, hist, st)) != cudaSuccess) return SCAPE_ECUDA;
       if ((e = launch_select(pass, W, start, ks, sel, hist, st)) != cudaSuccess) return SCAPE_ECUDA;
     }
     if ((e = launch_tie_count(m, W, start, sel, eqcnt, nchunk, st)) != cudaSuccess)
@@ -150,7 +150,7 @@ extern "C" int scape_topk_mask_static(const float* m, int64_t P, int W, double s
     if ((e = launch_tie_select(m, W, start, sel, eqcnt, nchunk, st)) != cudaSuccess)
       return SCAPE_ECUDA;
   }
-  if ((e = launch_mark(m, P, W, start, sel, bits, tile_cnt, st)) != cudaSuccess) return SCAPE_ECUDA;
+  if ((e = launch_mark(m, P, whole_map(P, W), start, sel, bits, tile_cnt, st)) != cudaSuccess) return SCAPE_ECUDA;
   if ((e = launch_scan(tile_cnt, ntiles, tile_base, scan_scratch, st)) != cudaSuccess)
     return SCAPE_ECUDA;
   if ((e = launch_index(bits, P, tile_base, idx, ktot, st)) != cudaSuccess) return SCAPE_ECUDA;

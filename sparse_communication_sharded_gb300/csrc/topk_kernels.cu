@@ -89,7 +89,8 @@ static_assert(kMSeg == kTile, "a segment is one mark tile");
 
 template <int MODE>
 __global__ void __launch_bounds__(256)
-mpass_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __restrict__ shard_start,
+mpass_kernel(const float* __restrict__ m, int64_t P, ShardMap sm,
+             const int64_t* __restrict__ shard_start,
              const ShardSel* __restrict__ sel, uint32_t* __restrict__ hist,
              uint2* __restrict__ cand, uint32_t* __restrict__ cand_cnt, int64_t segs_per_block,
              int selective) {
@@ -102,7 +103,8 @@ mpass_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __res
   const int64_t g1 = min(g0 + segs_per_block, nseg);
   if (g0 >= g1) return;
   const int64_t r0 = g0 * kMSeg, r1 = min(g1 * kMSeg, P);
-  int s = shard_of(r0, P, W);
+  const int W = sm.S;
+  int s = sm.of(r0);
   // shards this mode works on
   auto wanted = [&](const ShardSel& q) -> bool {
     if (!HIST) return q.mode == kSelSearch && (q.flags & kSelNeedCollect);
@@ -258,7 +260,8 @@ constexpr int kSpecBlocksPerSm = 4;
 constexpr int kLaneSlots = 16;  // staged candidates per lane
 
 __global__ void __launch_bounds__(256, kSpecBlocksPerSm)
-spec_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __restrict__ shard_start,
+spec_kernel(const float* __restrict__ m, int64_t P, ShardMap sm,
+            const int64_t* __restrict__ shard_start,
             const ShardSel* __restrict__ sel, uint2* __restrict__ cand,
             uint32_t* __restrict__ cand_cnt, uint32_t* __restrict__ above_cnt,
             uint32_t* __restrict__ bits, uint32_t* __restrict__ tile_cnt, int64_t segs_per_block) {
@@ -270,7 +273,8 @@ spec_kernel(const float* __restrict__ m, int64_t P, int W, const int64_t* __rest
   if (g0 >= g1) return;
   // P < 2^31: every index below fits 32 bits
   const uint32_t r0 = (uint32_t)(g0 * kMSeg), r1 = (uint32_t)min(g1 * kMSeg, P);
-  int s = shard_of(r0, P, W);
+  const int W = sm.S;
+  int s = sm.of(r0);
   {
     bool any = false;
     for (int q = s; q < W && (uint32_t)__ldg(shard_start + q) < r1; ++q)
@@ -680,31 +684,31 @@ int mpass_grid(int64_t P, int blocks_per_sm, int64_t* segs_per_block) {
 }  // namespace
 
 // ------------------------------------------------------------------ launchers
-cudaError_t launch_chist0(const float* m, int64_t P, int W, const int64_t* shard_start,
+cudaError_t launch_chist0(const float* m, int64_t P, const ShardMap& sm, const int64_t* shard_start,
                           const ShardSel* sel, uint32_t* hist, uint2* cand, uint32_t* cand_cnt,
                           bool selective, cudaStream_t st) {
   int64_t spb = 1;
   const int grid = mpass_grid(P, 4, &spb);  // 48 KB of shared memory per block
-  mpass_kernel<kMHist><<<grid, 256, 0, st>>>(m, P, W, shard_start, sel, hist, cand, cand_cnt, spb,
+  mpass_kernel<kMHist><<<grid, 256, 0, st>>>(m, P, sm, shard_start, sel, hist, cand, cand_cnt, spb,
                                              selective ? 1 : 0);
   return cudaGetLastError();
 }
 
-cudaError_t launch_spec(const float* m, int64_t P, int W, const int64_t* shard_start,
+cudaError_t launch_spec(const float* m, int64_t P, const ShardMap& sm, const int64_t* shard_start,
                         const ShardSel* sel, uint2* cand, uint32_t* cand_cnt, uint32_t* above_cnt,
                         uint32_t* bits, uint32_t* tile_cnt, cudaStream_t st) {
   int64_t spb = 1;
   const int grid = mpass_grid(P, kSpecBlocksPerSm, &spb);
-  spec_kernel<<<grid, 256, 0, st>>>(m, P, W, shard_start, sel, cand, cand_cnt, above_cnt, bits,
+  spec_kernel<<<grid, 256, 0, st>>>(m, P, sm, shard_start, sel, cand, cand_cnt, above_cnt, bits,
                                     tile_cnt, spb);
   return cudaGetLastError();
 }
 
-cudaError_t launch_collect(const float* m, int64_t P, int W, const int64_t* shard_start,
+cudaError_t launch_collect(const float* m, int64_t P, const ShardMap& sm, const int64_t* shard_start,
                            const ShardSel* sel, uint2* cand, uint32_t* cand_cnt, cudaStream_t st) {
   int64_t spb = 1;
   const int grid = mpass_grid(P, 5, &spb);
-  mpass_kernel<kMCollect><<<grid, 256, 0, st>>>(m, P, W, shard_start, sel, nullptr, cand, cand_cnt,
+  mpass_kernel<kMCollect><<<grid, 256, 0, st>>>(m, P, sm, shard_start, sel, nullptr, cand, cand_cnt,
                                                 spb, 0);
   return cudaGetLastError();
 }

@@ -17,25 +17,48 @@ class Scape:
 
     def __init__(self, params: torch.Tensor, W: int, sparsity: float, *, layer_numel=None,
                  lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1,
-                 grad_dtype=torch.bfloat16, residuals: str = "device", staging_rows=None):
+                 grad_dtype=torch.bfloat16, residuals: str = "device", staging_rows=None,
+                 shard_range=None):
         """residuals: "device" (HBM) or "host": the W error-feedback buffers
         live in pinned host memory (keeps W*P*4 bytes out of HBM).  With host
         residuals, staging_rows (default min(W, 12); 0 for none) residual rows
         of device memory stage them: sparse steps copy them in and out in
         worker groups, overlapped with the compaction; without staging the
-        kernels read and write them in place over the host link."""
+        kernels read and write them in place over the host link.
+
+        shard_range=(a, b): this instance covers only the optimizer shards
+        [a, b) of the problem that layer_numel (the global layer sizes, then
+        required) and W define; `params` is the slice [offset, offset + P)
+        of the global parameters that those shards hold (see
+        scape_create_range), and every gradient passed to step() is the same
+        slice of that worker's gradient."""
         if not params.is_cuda or params.dtype != torch.float32 or not params.is_contiguous():
             raise ValueError("params must be a contiguous float32 CUDA tensor")
         P = params.numel()
-        layer_numel = [P] if layer_numel is None else list(layer_numel)
-        if sum(layer_numel) != P:
-            raise ValueError("layer sizes must sum to params.numel()")
         self.grad_dtype = grad_dtype
         dt = C.SCAPE_BF16 if grad_dtype == torch.bfloat16 else C.SCAPE_F32
         if grad_dtype not in (torch.bfloat16, torch.float32):
             raise ValueError("grad_dtype must be torch.bfloat16 or torch.float32")
-        self.h = C.scape_create(layer_numel, W, sparsity, beta1, beta2, lr, eps, weight_decay, dt)
+        if shard_range is None:
+            layer_numel = [P] if layer_numel is None else list(layer_numel)
+            if sum(layer_numel) != P:
+                raise ValueError("layer sizes must sum to params.numel()")
+            self.h = C.scape_create(layer_numel, W, sparsity, beta1, beta2, lr, eps,
+                                    weight_decay, dt)
+        else:
+            if layer_numel is None:
+                raise ValueError("a shard range needs the global layer sizes")
+            a, b = shard_range
+            self.h = C.scape_create_range(list(layer_numel), W, a, b, sparsity, beta1, beta2, lr,
+                                          eps, weight_decay, dt)
+        rng = C.scape_get_range(self.h)
+        self.P_global, self.offset = rng["P_global"], rng["offset"]
+        self.shard_range = (rng["shard_begin"], rng["shard_end"])
         geo = C.scape_get_geometry(self.h)
+        if geo["P"] != P:
+            C.scape_destroy(self.h)
+            self.h = None
+            raise ValueError(f"params holds {P} elements; the shard range covers {geo['P']}")
         self.P, self.W, self.k = geo["P"], geo["W"], geo["k"]
         self.shard_start, self.shard_k = geo["shard_start"], geo["shard_k"]
         dev = params.device

@@ -1,7 +1,16 @@
-"""World-size-2 gloo test of the multi-rank path on CPU: ranks split the
-optimizer shards, each runs its shards as independent problems (the CPU oracle
-stands in for the GPU kernels here), and the gathered result equals the
-single-process run bit for bit; the timing reduction takes the max over ranks."""
+"""World-size-2 (and 3) gloo tests of the multi-rank split on the CPU.
+
+Each rank builds the library handle of its own block of optimizer shards
+(scape_create_range: host-only, no GPU work) and the ranks gather what their
+handles report.  Together the handles must tile the whole problem exactly as
+the oracle lays it out ("SCAPE" Sec. II-A, even partition; "Sintesi Tecnica:
+SCAPE" Sec. 2, per-partition masks): the parameter slices partition [0, P), the
+local shard boundaries shifted by each slice's offset are the global ones, the
+per-shard k_s are the global k_s and the k sum to the global k.  The same
+gather helper the multi-GPU tests use reassembles a vector from the ranks'
+slices, and the timing reductions take the max and the sum over ranks.  (The
+GPU run of the split, each rank stepping its shards through the CUDA library,
+is tests/test_multirank_gpu.py.)"""
 import os
 import socket
 
@@ -12,17 +21,12 @@ import torch.distributed as dist
 import torch.multiprocessing as mp
 
 from oracle import oracle as O
-from sparse_communication_sharded_gb300 import multirank, synth
+from sparse_communication_sharded_gb300 import _scape as C
+from sparse_communication_sharded_gb300 import build as B
+from sparse_communication_sharded_gb300 import multirank
 
-P, W, S, STEPS = 6000, 4, 0.9, 4
-
-
-def _inputs():
-    wl = synth.Workload("t", (("flat", P),), W=W, sparsity=S, steps=STEPS, grad_dtype="f32")
-    gen = synth.GradientStream(wl, seed=11, device="cpu")
-    grads = [[synth.to_numpy_grad(g) for g in gen.next()] for _ in range(STEPS)]
-    w0 = synth.init_params(P, seed=11).numpy()
-    return w0, grads
+LAYERS = [1000, 70001, 33, 12345]   # P = 83379
+W, S = 8, 0.99
 
 
 def _free_port():
@@ -37,26 +41,27 @@ def _worker(rank, world, port, out_path):
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
     dist.init_process_group("gloo", rank=rank, world_size=world)
-    w0, grads = _inputs()
-    start, ks = O.layout(P, W, S)
     mine = multirank.rank_shards(W, world, rank)
-    w_out = np.zeros(P, np.float32)
-    m_out = np.zeros(P, np.float32)
-    for sh in mine:
-        lo, hi = int(start[sh]), int(start[sh + 1])
-        st = O.new_state(w0[lo:hi], W, S, O.Hyper(), shard_start=np.array([0, hi - lo]),
-                         shard_k=np.array([ks[sh]]))
-        for g in grads:
-            O.advance(st, [x[lo:hi].copy() for x in g], keep=())
-        w_out[lo:hi] = st.w
-        m_out[lo:hi] = st.m
-    # gather the disjoint pieces (result collection only; nothing on the data path)
-    wt, mt = torch.from_numpy(w_out), torch.from_numpy(m_out)
-    dist.all_reduce(wt)
-    dist.all_reduce(mt)
+    h = C.scape_create_range(LAYERS, W, mine.start, mine.stop, S, 0.9, 0.95, 1e-3, 1e-8, 0.1,
+                             C.SCAPE_BF16)
+    geo = C.scape_get_geometry(h)
+    rng = C.scape_get_range(h)
+    C.scape_destroy(h)
+    P = sum(LAYERS)
+    lo, hi = multirank.shard_slice(P, W, mine)
+    assert (rng["offset"], rng["offset"] + geo["P"]) == (lo, hi)
+    # per-shard global start and k, reassembled from every rank's handle
+    starts = torch.tensor([rng["offset"] + x for x in geo["shard_start"][:-1]], dtype=torch.int64)
+    ks = torch.tensor(geo["shard_k"], dtype=torch.int64)
+    all_starts = multirank.gather_slices(starts, mine.start, W)
+    all_k = multirank.gather_slices(ks, mine.start, W)
+    # a parameter vector reassembled from the ranks' slices
+    vec = multirank.gather_slices(torch.arange(lo, hi, dtype=torch.float64), lo, P)
+    k_sum = multirank.sum_over_ranks(geo["k"])
     t_max = multirank.max_over_ranks(1.0 + rank)
     if rank == 0:
-        np.savez(out_path, w=wt.numpy(), m=mt.numpy(), t_max=t_max)
+        np.savez(out_path, starts=all_starts.numpy(), k=all_k.numpy(), vec=vec.numpy(),
+                 k_sum=k_sum, t_max=t_max, P_global=rng["P_global"])
     dist.barrier()
     dist.destroy_process_group()
 
@@ -70,15 +75,33 @@ def test_rank_shards_partition():
         multirank.rank_shards(4, 2, 2)
 
 
-def test_two_gloo_ranks_match_single_process(tmp_path):
+@pytest.mark.parametrize("world", [2, 3])
+def test_rank_handles_tile_the_global_layout(tmp_path, world):
+    B.build()
     out = str(tmp_path / "res.npz")
-    mp.spawn(_worker, args=(2, _free_port(), out), nprocs=2, join=True)
+    mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world, join=True)
     res = np.load(out)
-    w0, grads = _inputs()
-    st = O.new_state(w0, W, S, O.Hyper())
-    for g in grads:
-        O.advance(st, g, keep=())
-    assert np.array_equal(res["w"].view(np.uint32), st.w.view(np.uint32))
-    assert np.array_equal(res["m"].view(np.uint32), st.m.view(np.uint32))
-    assert float(res["t_max"]) == 2.0
+    P = sum(LAYERS)
+    start, ks = O.layout(P, W, S)
+    assert int(res["P_global"]) == P
+    assert np.array_equal(res["starts"], start[:-1])
+    assert np.array_equal(res["k"], ks)
+    assert int(res["k_sum"]) == int(ks.sum())
+    assert np.array_equal(res["vec"], np.arange(P, dtype=np.float64))
+    assert float(res["t_max"]) == float(world)
     assert multirank.weak_scaling_value(100, 2, 0.5) == 400.0
+    assert multirank.strong_scaling_value(100, 0.5) == 200.0
+
+
+def test_range_handle_argument_errors():
+    B.build()
+    for a, b in ((-1, 2), (3, 3), (5, 4), (0, W + 1)):
+        with pytest.raises(C.ScapeError):
+            C.scape_create_range(LAYERS, W, a, b, S, 0.9, 0.95, 1e-3, 1e-8, 0.1, C.SCAPE_F32)
+    # P < W: a range of empty shards holds no parameter
+    with pytest.raises(C.ScapeError):
+        C.scape_create_range([5], 8, 0, 1, 0.5, 0.9, 0.95, 1e-3, 1e-8, 0.1, C.SCAPE_F32)
+    h = C.scape_create_range([5], 8, 0, 2, 0.5, 0.9, 0.95, 1e-3, 1e-8, 0.1, C.SCAPE_F32)
+    geo = C.scape_get_geometry(h)
+    C.scape_destroy(h)
+    assert geo["P"] == 1 and geo["shard_start"] == [0, 0, 1] and geo["shard_k"] == [0, 1]
