@@ -346,7 +346,7 @@ int scape_step_host(scape_t *h, const void *const *host_grads_src,
  * scape_profile_read() copies the totals (milliseconds and launch counts,
  * SCAPE_NUM_KERNELS entries each) and scape_kernel_name() names entry i.
  */
-#define SCAPE_NUM_KERNELS 22
+#define SCAPE_NUM_KERNELS 24
 int scape_profile_enable(scape_t *h, int on);
 /* Which kernels profiling brackets: bit i for kernel i (default: all).  Two
  * event records per launch cost the GPU a few microseconds; a timing run can
@@ -391,6 +391,109 @@ int64_t scape_launch_count(const scape_t *h);
 #define SCAPE_STATIC_MAX_WORKERS 64
 int scape_topk_mask_static(const float *m, int64_t P, int W, double sparsity, uint32_t *bits,
                            uint32_t *idx, void *stream);
+
+/*
+ * ---------------------------------------------------------------------------
+ * Several data-parallel ranks with a real exchange.
+ *
+ * Rank `rank` of G owns the workers and the optimizer shards [a, b),
+ * a = floor(W rank / G), b = floor(W (rank + 1) / G), of the problem
+ * scape_create() would lay out for these layers and W (one optimizer shard
+ * per worker: "SCAPE" Sec. II-A, sharded data parallelism with a distributed
+ * optimizer).  The rank holds a full replica of the parameters w[P], the first
+ * moment of its own parameter range [lo, hi) (the shards it owns), and for
+ * each of its b - a workers the full-length gradient and residual.  Every
+ * step is cut around three collectives that the caller runs (NCCL, gloo, ...)
+ * on the buffers scape_xc_buffers() returns, with the element counts of
+ * scape_xc_counts():
+ *   1. scape_xc_pack(): error feedback and compaction of the local workers
+ *      with the lagged global mask ("SCAPE" Sec. II-B), laid out in the send
+ *      buffer as one contiguous block per destination rank q (rows: local
+ *      workers in order; columns: q's selected coordinates, padded to a
+ *      multiple of 4).
+ *   2. caller: all-to-all with those per-rank counts, send -> recv.  recv then
+ *      holds the W workers' rows of the owned columns in worker order: the
+ *      sparse reduce-scatter of "SCAPE" Sec. I, its sum taken by the owner in
+ *      worker order so that every G gives the one-device result bit for bit.
+ *   3. scape_xc_update(): the ordered mean of the W rows and AdamS at the
+ *      owned selected coordinates ("SCAPE" Sec. II-C, Eq. 2; "Sintesi
+ *      Tecnica: SCAPE" Sec. 2, one synchronised buffer), the updated values
+ *      copied to param_send.
+ *   4. caller: all-gather param_send -> param_recv (rank q's values at row q,
+ *      params_per_rank[q] of them, row stride param_stride): the sparse
+ *      parameter all-gather ("SCAPE" Sec. I).
+ *   5. scape_xc_refresh(): the next mask of the owned shards from their first
+ *      moment ("Sintesi Tecnica: SCAPE" Sec. 2, partitioned mask), aligned to
+ *      the global 32-bit word grid in mask_send (words floor(lo/32) ..).
+ *   6. caller: all-gather mask_send -> mask_recv (mask_words_per_rank[q]
+ *      words at row q, stride mask_stride).  Steps 4 and 6 may overlap: the
+ *      mask is only used by the next step (the one-step lag of "Sintesi
+ *      Tecnica: SCAPE" Sec. 2).
+ *   7. scape_xc_finish(): the other ranks' updated parameters written into w,
+ *      the gathered words merged into the global mask and its index list
+ *      rebuilt for the next step.
+ * Step 1 is dense (every coordinate is sent and every parameter gathered).
+ * All work is enqueued on `stream`; the caller orders its collectives after
+ * the previous call's work (e.g. on the same stream, or after synchronising).
+ * Calls out of this order return SCAPE_ESTATE.  The handle never allocates
+ * device memory: the caller binds one workspace of the size scape_xc_layout()
+ * reports, which holds the exchange buffers (the dense first step needs about
+ * 2 (b - a) P + W (hi - lo) floats of them).
+ * ---------------------------------------------------------------------------
+ */
+typedef struct scape_xc scape_xc_t;
+
+/* Host only.  Errors: as scape_create(), and SCAPE_EINVAL unless
+ * 1 <= G <= W and 0 <= rank < G. */
+int scape_xc_create(scape_xc_t **out, int n_layers, const int64_t *host_layer_numel, int W,
+                    int G, int rank, double sparsity, float beta1, float beta2, float lr,
+                    float eps, float weight_decay, int grad_dtype);
+void scape_xc_destroy(scape_xc_t *h);
+const char *scape_xc_last_error(const scape_xc_t *h);
+
+/* P, global k, local workers b - a, the owned range [own_begin, own_end) and
+ * its k, and the workspace bytes.  Any output may be NULL. */
+int scape_xc_layout(const scape_xc_t *h, int64_t *P, int64_t *k, int *local_workers,
+                    int64_t *own_begin, int64_t *own_end, int64_t *own_k, size_t *ws_bytes);
+
+/*
+ * Bind caller memory: params w[P] (the replica, 16-byte aligned), m_own
+ * (own_end - own_begin floats, zeroed, 16-byte aligned), host array of b - a
+ * residual pointers (each P floats, zeroed, 16-byte aligned), the workspace
+ * (256-byte aligned).  Resets the step count.
+ */
+int scape_xc_bind(scape_xc_t *h, float *params, float *m_own, float *const *host_e_ptrs,
+                  void *workspace, size_t ws_bytes);
+
+/* Element counts of the coming (or current) step's collectives, per rank q:
+ * floats sent to q and received from q in the all-to-all; the parameter and
+ * mask-word all-gathers' per-rank counts and row strides.  Any output may be
+ * NULL (arrays have G entries). */
+int scape_xc_counts(const scape_xc_t *h, int64_t *host_send_counts, int64_t *host_recv_counts,
+                    int64_t *params_per_rank, int64_t *param_stride,
+                    int64_t *mask_words_per_rank, int64_t *mask_stride);
+
+/* Device pointers of the exchange buffers inside the bound workspace, and of
+ * the global mask bitmap (ceil(P/32) words) the next step uses.  SCAPE_ESTATE
+ * before scape_xc_bind().  Any output may be NULL. */
+int scape_xc_buffers(const scape_xc_t *h, float **send, float **recv, float **param_send,
+                     float **param_recv, uint32_t **mask_send, uint32_t **mask_recv,
+                     const uint32_t **global_bits);
+
+/* The four phases of a step (see above).  host_grad_ptrs: b - a device
+ * pointers, the local workers' gradients g^w[P] of the handle's dtype. */
+int scape_xc_pack(scape_xc_t *h, const void *const *host_grad_ptrs, void *stream);
+int scape_xc_update(scape_xc_t *h, void *stream);
+int scape_xc_refresh(scape_xc_t *h, void *stream);
+int scape_xc_finish(scape_xc_t *h, void *stream);
+
+/* Steps completed and the owned shards' current mask bitmap and index list
+ * (local coordinates: bit i is parameter own_begin + i). */
+int scape_xc_get_state(const scape_xc_t *h, int64_t *t, const uint32_t **own_bits,
+                       const uint32_t **own_idx);
+
+/* Kernel launches made through this handle. */
+int64_t scape_xc_launch_count(const scape_xc_t *h);
 
 #ifdef __cplusplus
 }

@@ -19,7 +19,7 @@ SCAPE_ESTATE = -4
 SCAPE_F32 = 0
 SCAPE_BF16 = 1
 SCAPE_MAX_WORKERS = 256
-SCAPE_NUM_KERNELS = 22
+SCAPE_NUM_KERNELS = 24
 
 LIB_PATH = _build.LIB
 
@@ -68,6 +68,20 @@ _PROTOS = {
     "scape_kernel_name": (ctypes.c_char_p, [_i32]),
     "scape_launch_count": (_i64, [_vp]),
     "scape_topk_mask_static": (_i32, [_vp, _i64, _i32, _f64, _vp, _vp, _vp]),
+    "scape_xc_create": (_i32, [ctypes.POINTER(_vp), _i32, _vp, _i32, _i32, _i32, _f64, _f32, _f32,
+                               _f32, _f32, _f32, _i32]),
+    "scape_xc_destroy": (None, [_vp]),
+    "scape_xc_last_error": (ctypes.c_char_p, [_vp]),
+    "scape_xc_layout": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "scape_xc_bind": (_i32, [_vp, _vp, _vp, _vp, _vp, ctypes.c_size_t]),
+    "scape_xc_counts": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "scape_xc_buffers": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "scape_xc_pack": (_i32, [_vp, _vp, _vp]),
+    "scape_xc_update": (_i32, [_vp, _vp]),
+    "scape_xc_refresh": (_i32, [_vp, _vp]),
+    "scape_xc_finish": (_i32, [_vp, _vp]),
+    "scape_xc_get_state": (_i32, [_vp, _vp, _vp, _vp]),
+    "scape_xc_launch_count": (_i64, [_vp]),
 }
 
 
@@ -306,3 +320,94 @@ def scape_topk_mask_static(m_ptr, P, W, sparsity, bits_ptr, idx_ptr, stream=0):
     """Allocation-free per-shard top-k mask; returns the status code."""
     return load().scape_topk_mask_static(m_ptr, int(P), int(W), float(sparsity), bits_ptr,
                                          idx_ptr, stream)
+
+
+# ------------------------------------------------------------ several ranks, real exchange
+def _xcheck(h, rc):
+    if rc != SCAPE_OK:
+        msg = load().scape_xc_last_error(h)
+        raise ScapeError(rc, msg.decode() if msg else "")
+    return rc
+
+
+def scape_xc_create(layer_numel, W, G, rank, sparsity, beta1, beta2, lr, eps, weight_decay,
+                    grad_dtype):
+    lib = load()
+    sizes = (ctypes.c_int64 * len(layer_numel))(*[int(n) for n in layer_numel])
+    h = ctypes.c_void_p()
+    rc = lib.scape_xc_create(ctypes.byref(h), len(layer_numel), ctypes.addressof(sizes), int(W),
+                             int(G), int(rank), float(sparsity), beta1, beta2, lr, eps,
+                             weight_decay, int(grad_dtype))
+    if rc != SCAPE_OK:
+        raise ScapeError(rc, lib.scape_xc_last_error(None).decode())
+    return h
+
+
+def scape_xc_destroy(h):
+    load().scape_xc_destroy(h)
+
+
+def scape_xc_layout(h):
+    P, k, own_b, own_e, own_k = (ctypes.c_int64() for _ in range(5))
+    wl = ctypes.c_int()
+    ws = ctypes.c_size_t()
+    _xcheck(h, load().scape_xc_layout(h, ctypes.byref(P), ctypes.byref(k), ctypes.byref(wl),
+                                      ctypes.byref(own_b), ctypes.byref(own_e),
+                                      ctypes.byref(own_k), ctypes.byref(ws)))
+    return {"P": P.value, "k": k.value, "local_workers": wl.value, "own_begin": own_b.value,
+            "own_end": own_e.value, "own_k": own_k.value, "ws_bytes": ws.value}
+
+
+def scape_xc_bind(h, params_ptr, m_ptr, e_ptrs, ws_ptr, ws_bytes):
+    arr = _ptr_array(e_ptrs)
+    _xcheck(h, load().scape_xc_bind(h, params_ptr, m_ptr, ctypes.addressof(arr), ws_ptr,
+                                    ws_bytes))
+
+
+def scape_xc_counts(h, G):
+    sc = (ctypes.c_int64 * G)()
+    rcv = (ctypes.c_int64 * G)()
+    ppr = (ctypes.c_int64 * G)()
+    mwr = (ctypes.c_int64 * G)()
+    ps, ms = ctypes.c_int64(), ctypes.c_int64()
+    _xcheck(h, load().scape_xc_counts(h, ctypes.addressof(sc), ctypes.addressof(rcv),
+                                      ctypes.addressof(ppr), ctypes.byref(ps),
+                                      ctypes.addressof(mwr), ctypes.byref(ms)))
+    return {"send": list(sc), "recv": list(rcv), "params": list(ppr), "param_stride": ps.value,
+            "mask_words": list(mwr), "mask_stride": ms.value}
+
+
+def scape_xc_buffers(h):
+    ptrs = [ctypes.c_void_p() for _ in range(7)]
+    _xcheck(h, load().scape_xc_buffers(h, *[ctypes.byref(p) for p in ptrs]))
+    names = ("send", "recv", "param_send", "param_recv", "mask_send", "mask_recv", "global_bits")
+    return {n: p.value for n, p in zip(names, ptrs)}
+
+
+def scape_xc_pack(h, grad_ptrs, stream=0):
+    arr = _ptr_array(grad_ptrs)
+    _xcheck(h, load().scape_xc_pack(h, ctypes.addressof(arr), stream))
+
+
+def scape_xc_update(h, stream=0):
+    _xcheck(h, load().scape_xc_update(h, stream))
+
+
+def scape_xc_refresh(h, stream=0):
+    _xcheck(h, load().scape_xc_refresh(h, stream))
+
+
+def scape_xc_finish(h, stream=0):
+    _xcheck(h, load().scape_xc_finish(h, stream))
+
+
+def scape_xc_get_state(h):
+    t = ctypes.c_int64()
+    bits, idx = ctypes.c_void_p(), ctypes.c_void_p()
+    _xcheck(h, load().scape_xc_get_state(h, ctypes.byref(t), ctypes.byref(bits),
+                                         ctypes.byref(idx)))
+    return t.value, bits.value, idx.value
+
+
+def scape_xc_launch_count(h):
+    return load().scape_xc_launch_count(h)

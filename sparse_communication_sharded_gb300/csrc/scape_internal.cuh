@@ -89,6 +89,8 @@ enum KernelId {
   kKFixup,
   kKRemark,
   kKParamPatch,
+  kKDenseUpdate,
+  kKXcMove,
   kNumKernels
 };
 static_assert(kNumKernels == SCAPE_NUM_KERNELS, "kernel table size");
@@ -240,6 +242,14 @@ cudaError_t launch_param_patch(const uint32_t* idx, int64_t k, const float* w, f
                                cudaStream_t st);
 cudaError_t launch_reduce(const float* pack, int64_t pack_stride, int W, int64_t k, float* gbar,
                           cudaStream_t st);
+// multi-rank exchange helpers (step_kernels.cu)
+cudaError_t launch_adams_dense(const float* gbar, int64_t n, float* w, float* m,
+                               const AdamsConst& c, cudaStream_t st);
+cudaError_t launch_index_move(bool scatter, const uint32_t* idx, int64_t k, const float* src,
+                              float* dst, cudaStream_t st);
+cudaError_t launch_align_bits(const uint32_t* local, int64_t n, int shift, uint32_t* out,
+                              int64_t nw_out, cudaStream_t st);
+cudaError_t launch_or_words(const uint32_t* src, int64_t nw, uint32_t* dst, cudaStream_t st);
 cudaError_t launch_adams_sparse(const uint32_t* idx, const float* gbar, int64_t k, float* w,
                                 float* m, const AdamsConst& c, bool msync, cudaStream_t st);
 

@@ -431,6 +431,57 @@ param_patch_kernel(const uint32_t* __restrict__ idx, int64_t k, const float* __r
   dst[i] = __ldg(w + i);
 }
 
+// ------------------------------------------------------------------ exchange helpers
+// Used by the multi-rank exchange (scape_xc.cu).
+// AdamS on every coordinate of a range from the synchronised buffer of the
+// dense first step: g_bar[i] is coordinate i's averaged gradient.
+__global__ void __launch_bounds__(256)
+adams_dense_kernel(const float* __restrict__ gbar, int64_t n, float* __restrict__ wts,
+                   float* __restrict__ mom, AdamsConst c) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  float wv = wts[i], mv = mom[i];
+  adams_update(gbar[i], wv, mv, c);
+  wts[i] = wv;
+  mom[i] = mv;
+}
+
+// dst[j] = src[idx[j]] (gather) or dst[idx[j]] = src[j] (scatter), j < k.
+template <bool SCATTER>
+__global__ void __launch_bounds__(256)
+index_move_kernel(const uint32_t* __restrict__ idx, int64_t k, const float* __restrict__ src,
+                  float* __restrict__ dst) {
+  const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= k) return;
+  const uint32_t i = __ldg(idx + j);
+  if (SCATTER) dst[i] = __ldg(src + j);
+  else dst[j] = __ldg(src + i);
+}
+
+// A bitmap whose bit 0 is global parameter lo, re-aligned to the global word
+// grid: out[j] holds global bits 32 (lo / 32 + j) .. + 31 of it (bits of the
+// global word outside [lo, lo + n) are zero).  The source's bits past n are zero.
+__global__ void __launch_bounds__(256)
+align_bits_kernel(const uint32_t* __restrict__ local, int64_t n, int shift,
+                  uint32_t* __restrict__ out, int64_t nw_out) {
+  const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= nw_out) return;
+  const int64_t nl = (n + 31) / 32;
+  uint32_t v = j < nl ? (__ldg(local + j) << shift) : 0u;
+  if (shift && j >= 1 && j - 1 < nl) v |= __ldg(local + j - 1) >> (32 - shift);
+  out[j] = v;
+}
+
+// dst[j] |= src[j]: a rank's aligned mask words merged into the global bitmap
+// (atomic: the first and last words are shared with the neighbouring ranks).
+__global__ void __launch_bounds__(256)
+or_words_kernel(const uint32_t* __restrict__ src, int64_t nw, uint32_t* __restrict__ dst) {
+  const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= nw) return;
+  const uint32_t v = __ldg(src + j);
+  if (v) atomicOr(dst + j, v);
+}
+
 template <typename GT, int KIND>
 void dense_kind(const WorkerPtrs& p, int W, int64_t P, bool vec, float* w, float* m, float* v,
                 const AdamsConst& c, cudaStream_t st) {
@@ -518,6 +569,36 @@ cudaError_t launch_param_patch(const uint32_t* idx, int64_t k, const float* w, f
                                cudaStream_t st) {
   if (k <= 0) return cudaSuccess;
   param_patch_kernel<<<(unsigned)((k + 255) / 256), 256, 0, st>>>(idx, k, w, dst);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_adams_dense(const float* gbar, int64_t n, float* w, float* m,
+                               const AdamsConst& c, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  adams_dense_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(gbar, n, w, m, c);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_index_move(bool scatter, const uint32_t* idx, int64_t k, const float* src,
+                              float* dst, cudaStream_t st) {
+  if (k <= 0) return cudaSuccess;
+  const unsigned grid = (unsigned)((k + 255) / 256);
+  if (scatter) index_move_kernel<true><<<grid, 256, 0, st>>>(idx, k, src, dst);
+  else index_move_kernel<false><<<grid, 256, 0, st>>>(idx, k, src, dst);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_align_bits(const uint32_t* local, int64_t n, int shift, uint32_t* out,
+                              int64_t nw_out, cudaStream_t st) {
+  if (nw_out <= 0) return cudaSuccess;
+  align_bits_kernel<<<(unsigned)((nw_out + 255) / 256), 256, 0, st>>>(local, n, shift, out,
+                                                                      nw_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_or_words(const uint32_t* src, int64_t nw, uint32_t* dst, cudaStream_t st) {
+  if (nw <= 0) return cudaSuccess;
+  or_words_kernel<<<(unsigned)((nw + 255) / 256), 256, 0, st>>>(src, nw, dst);
   return cudaGetLastError();
 }
 
