@@ -681,6 +681,98 @@ def bench_gpu(args, wl):
     return 0
 
 
+# --------------------------------------------------------------------- exchange mode
+def bench_exchange(args, wl):
+    """The exchange-based multi-rank step (exchange.ScapeDP): each of the N
+    ranks owns W/N workers (their full gradients and residuals) and W/N
+    optimizer shards; a step is the compaction, the all-to-all of the packed
+    values, the owners' update, the sparse parameter all-gather, the owners'
+    mask refresh and the mask all-gather (NCCL).  value = P over the slowest
+    rank's step time (one problem of fixed size: strong scaling)."""
+    import dataclasses
+
+    import torch
+    import torch.distributed as dist
+
+    import sparse_communication_sharded_gb300 as pkg
+    from sparse_communication_sharded_gb300 import multirank, synth
+    from sparse_communication_sharded_gb300.exchange import ScapeDP
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    torch.cuda.set_device(local)
+    dev = torch.device(f"cuda:{local}")
+    pkg.load()
+    P, W = wl.P, wl.W
+    mine = multirank.rank_shards(W, ws, rank)
+    lo, hi = multirank.shard_slice(P, W, mine)
+    gsz = _grad_bytes(wl)
+    wl_ = len(mine)
+    need = wl_ * P * (gsz + 4 + 4) + 4 * P + W * (hi - lo) * 4 + 16 * (hi - lo) + (1 << 30)
+    free, _ = torch.cuda.mem_get_info()
+    if need > 0.92 * free:
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "mode": "exchange", "value": None,
+                              "unavailable": f"needs ~{need / 2**30:.0f} GiB per GPU at N={ws}, "
+                                             f"{free / 2**30:.0f} GiB free"}), flush=True)
+        if ws > 1:
+            dist.destroy_process_group()
+        return 0
+    gdt = torch.bfloat16 if wl.grad_dtype == "bf16" else torch.float32
+    params = synth.init_params(P, seed=0, device=dev)
+    opt = ScapeDP(params, W, wl.sparsity, layer_numel=[n for _, n in wl.layers], grad_dtype=gdt)
+    gen = synth.GradientStream(dataclasses.replace(wl, W=wl_), seed=1 + rank, device=dev)
+    grads = gen.alloc()
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        gen.next_into(grads)
+        opt.step(grads)
+    torch.cuda.synchronize()
+    b0, n0 = opt.bytes_sent, opt.launch_count()
+    st = torch.cuda.current_stream()
+    step_ms = []
+    with ClockSampler(local) as clk:
+        for _ in range(args.steps):
+            gen.next_into(grads)
+            barrier()
+            torch.cuda.synchronize()
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ev0.record(st)
+            opt.step(grads)
+            ev1.record(st)
+            torch.cuda.synchronize()
+            barrier()
+            step_ms.append(ev0.elapsed_time(ev1))
+    sent = (opt.bytes_sent - b0) / args.steps
+    launches = opt.launch_count() - n0
+    my_ms = sum(step_ms) / len(step_ms)
+    t_max = multirank.max_over_ranks(my_ms, device=dev)
+    sent_all = multirank.sum_over_ranks(sent, device=dev)
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "mode": "exchange", "value": P / (t_max / 1000.0), "unit": UNIT,
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max,
+            "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": dict(workload_config(wl, args, ws),
+                           parallelism=f"{ws} data-parallel ranks, each owning {W // ws} or "
+                                       f"{(W + ws - 1) // ws} workers and optimizer shards; "
+                                       f"NCCL all-to-all + two all-gathers per step"),
+            "exchange_bytes_per_step": sent_all,
+            "rank0_ms_each": step_ms, "gpu_launches": launches, "clocks": clk.summary()}),
+            flush=True)
+    opt.close()
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
 # --------------------------------------------------------------------- flat sweep
 SWEEP_W = (1, 8, 32)
 SWEEP_S = (0.0, 0.9, 0.99, 0.999)
@@ -896,6 +988,9 @@ def main(argv=None):
                          "adams_sparse), sum (writes g_bar), update (also AdamS)")
     ap.add_argument("--baselines", type=int, default=1,
                     help="also time the dense AdamS and AdamW baselines (0 to skip)")
+    ap.add_argument("--exchange", action="store_true",
+                    help="time the exchange-based multi-rank step instead (each rank owns W/N "
+                         "workers and optimizer shards; NCCL all-to-all + all-gathers)")
     ap.add_argument("--sweep", action="store_true",
                     help="run the flat sweep (2^e fp32 parameters, W in {1, 8, 32}, sparsity "
                          "in {0, 90, 99, 99.9}%%, 256-level gradients) instead")
@@ -925,6 +1020,8 @@ def main(argv=None):
         wl = synth.WORKLOADS[args.workload]
     if args.impl == "reference":
         return bench_reference(args, wl)
+    if args.exchange:
+        return bench_exchange(args, wl)
     return bench_gpu(args, wl)
 
 

@@ -7,6 +7,15 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+# The randomised oracle properties need hypothesis, which not every machine
+# has (the GPU hosts do not); leave the module out there instead of reporting
+# a skip: its tests are CPU tests and run wherever hypothesis is installed.
+try:
+    import hypothesis  # noqa: F401
+    collect_ignore = []
+except ImportError:
+    collect_ignore = ["test_oracle_properties.py"]
+
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
