@@ -292,18 +292,32 @@ constexpr int kCandBins0 = 1 << kDigit0;
 // selective: only shards flagged kSelNeedHist, and nothing staged.
 cudaError_t launch_chist0(const float* m, int64_t P, const ShardMap& sm, const int64_t* shard_start,
                           const ShardSel* sel, uint32_t* hist, uint2* cand, uint32_t* cand_cnt,
-                          bool selective, cudaStream_t st);
+                          bool selective, int growth, cudaStream_t st);
+// The step's sparse AdamS update, applied inside the warm refresh's read of m
+// (launch_spec with a SpecUpdate): tbase is the rank table of the mask the
+// step used (still in `bits` when the refresh starts), gbar its synchronised
+// buffer, w and m the parameters and first moment (m is the array the refresh
+// reads; it is updated in place).
+struct SpecUpdate {
+  const uint32_t* tbase;
+  const float* gbar;
+  float* w;
+  float* m;
+  AdamsConst c;
+};
 // Warm refresh: one read of m that writes the bitmap words and popcounts of
 // every whole single-shard tile from the shard's previous threshold (tile_cnt
 // zeroed first), stages the candidates of the previous bucket window and counts
-// the parameters above it (above_cnt zeroed first).
+// the parameters above it (above_cnt zeroed first); with `up`, it applies the
+// step's update at the coordinates the old bitmap selects first.
 cudaError_t launch_spec(const float* m, int64_t P, const ShardMap& sm, const int64_t* shard_start,
                         const ShardSel* sel, uint2* cand, uint32_t* cand_cnt, uint32_t* above_cnt,
-                        uint32_t* bits, uint32_t* tile_cnt, cudaStream_t st);
+                        uint32_t* bits, uint32_t* tile_cnt, const SpecUpdate* up, int growth,
+                        cudaStream_t st);
 // Window histogram of the staged candidates with the outside counts lumped.
 cudaError_t launch_whist(int W, int blocks_per_shard, const int64_t* shard_start,
                          const ShardSel* sel, const uint2* cand, const uint32_t* cand_cnt,
-                         const uint32_t* above_cnt, uint32_t* hist, cudaStream_t st);
+                         const uint32_t* above_cnt, uint32_t* hist, int growth, cudaStream_t st);
 // Flip the candidates whose selection differs between the previous and the new
 // threshold (shards without kSelRemark).
 cudaError_t launch_fixup(const int64_t* shard_start, const ShardSel* sel, const uint2* cand,
@@ -318,9 +332,12 @@ cudaError_t launch_remark(const float* m, int64_t P, const ShardMap& sm, const i
 // form (pass 0): kSelFormCold on a full histogram, kSelFormWarm on the window
 // histogram, kSelFormRerun for the kSelNeedHist shards after their full count.
 constexpr int kSelFormCold = 0, kSelFormWarm = 1, kSelFormRerun = 2;
+// growth: how many first-digit buckets above the previous threshold's the
+// window of a warm refresh also covers (the expected growth of the first
+// moments since the previous refresh); 0 elsewhere.
 cudaError_t launch_cselect(int pass, int W, const int64_t* shard_start, const int64_t* shard_k,
                            ShardSel* sel, uint32_t* hist, uint32_t* cand_cnt, int form,
-                           cudaStream_t st);
+                           int growth, cudaStream_t st);
 cudaError_t launch_collect(const float* m, int64_t P, const ShardMap& sm, const int64_t* shard_start,
                            const ShardSel* sel, uint2* cand, uint32_t* cand_cnt, cudaStream_t st);
 // nar (optional): per-shard rows of nar_cap candidates, counts in nar_cnt

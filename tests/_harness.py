@@ -140,7 +140,8 @@ def run_full_trajectory(wl: synth.Workload, device, steps: int, seed: int = 0,
     return rep
 
 
-def run_sampled_shards(wl: synth.Workload, device, steps: int, shards, seed: int = 0):
+def run_sampled_shards(wl: synth.Workload, device, steps: int, shards, seed: int = 0,
+                       fusion=None):
     """Full-size problem on the GPU; the oracle runs each sampled shard as an
     independent sub-problem (shards share nothing but the step count), one
     process per shard in parallel (oracle.pool).  Every step compares the
@@ -154,6 +155,8 @@ def run_sampled_shards(wl: synth.Workload, device, steps: int, shards, seed: int
     gen = synth.GradientStream(wl, seed=seed, device=device)
     params = w0.clone()
     opt = make_opt(params, W, s, gdt)
+    if fusion is not None:
+        opt.set_fusion(fusion)
     start, ks = opt.shard_start, opt.shard_k
     kofs = np.concatenate([[0], np.cumsum(ks)])
     spec = [(start[sh], start[sh + 1], ks[sh]) for sh in shards]

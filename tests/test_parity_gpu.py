@@ -48,12 +48,16 @@ def test_trajectory_matches_oracle(cuda_device, P, W, s, dtype, quant):
     assert rep.exact, "trajectory not bit-identical to the oracle"
 
 
-@pytest.mark.parametrize("fusion", [C.FUSE_NONE, C.FUSE_SUM, C.FUSE_UPDATE])
-@pytest.mark.parametrize("P,W,s,dtype,quant", [TRAJ[1], TRAJ[2], TRAJ[4], TRAJ[6], TRAJ[7],
-                                                TRAJ[9]])
+@pytest.mark.parametrize("fusion", [C.FUSE_NONE, C.FUSE_SUM, C.FUSE_UPDATE, C.FUSE_REFRESH])
+@pytest.mark.parametrize("P,W,s,dtype,quant", [TRAJ[1], TRAJ[2], TRAJ[4], TRAJ[5], TRAJ[6],
+                                                TRAJ[7], TRAJ[9], TRAJ[10],
+                                                (11, 8, 0.5, "f32", False),
+                                                (300001, 3, 0.9, "bf16", False)])
 def test_trajectory_every_fusion_level(cuda_device, fusion, P, W, s, dtype, quant):
     """Separate launches (ordered sum, then unpack + AdamS), the sum inside the
-    compaction, and sum + update inside it all give the oracle's bits."""
+    compaction, sum + update inside it, and the update inside the next
+    refresh's read of m all give the oracle's bits.  (11, 8, 0.5) mixes shards
+    that keep every coordinate (no threshold: update only) with searched ones."""
     rep = run_full_trajectory(_wl(P, W, s, dtype, quant=quant), cuda_device, steps=6,
                               fusion=fusion)
     assert rep.exact
@@ -304,7 +308,9 @@ def test_set_state_rejects_wrong_counts(cuda_device):
 
 @pytest.mark.parametrize("P,W,variant,fusion", [(50000, 4, 0, None), (30011, 32, 0, C.FUSE_UPDATE),
                                                 (30011, 32, 0, C.FUSE_SUM),
-                                                (30011, 32, 0, C.FUSE_NONE), (20000, 3, 1, None)])
+                                                (30011, 32, 0, C.FUSE_NONE),
+                                                (30011, 32, 0, C.FUSE_REFRESH),
+                                                (20000, 3, 1, None)])
 def test_host_buffer_path_matches_device_path(cuda_device, P, W, variant, fusion):
     """scape_step_host (uploads in worker groups, the parameter download before
     the update plus a patch of the changed coordinates, or after it under the
@@ -344,6 +350,37 @@ def test_host_buffer_path_matches_device_path(cuda_device, P, W, variant, fusion
         opt.close()
     for a, b in zip(*per_step):
         assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+@pytest.mark.parametrize("fusion", [C.FUSE_SUM, C.FUSE_REFRESH])
+def test_step_without_refresh_reuses_the_older_mask(cuda_device, fusion):
+    """Skipping a refresh reuses the older mask; with the update deferred to
+    the refresh, the next step applies it on its own first.  Pattern: step 1,
+    refresh, steps 2 and 3 on that mask, refresh, step 4, refresh -- against
+    the oracle's steps taken in the same order."""
+    P, W, s = 70001, 4, 0.99
+    wl = _wl(P, W, s, "bf16")
+    gen = synth.GradientStream(wl, seed=31, device="cpu")
+    w0 = synth.init_params(P, seed=31)
+    params = w0.to(cuda_device)
+    opt = make_opt(params, W, s, torch.bfloat16)
+    opt.set_fusion(fusion)
+    st = O.new_state(w0.numpy(), W, s, HP)
+    bits, idx = O.dense_mask(P)
+    for t, refresh in ((1, True), (2, False), (3, True), (4, True)):
+        grads = gen.next()
+        opt.step([g.to(cuda_device) for g in grads])
+        O.step(t, [synth.to_numpy_grad(g) for g in grads], st.e, st.w, st.m, bits, idx, HP)
+        if refresh:
+            opt.refresh_mask()
+            bits, idx = O.topk_mask(st.m, st.shard_start, st.shard_k)
+    torch.cuda.synchronize()
+    assert np.array_equal(u32(opt.bits()), bits)
+    assert np.array_equal(u32(params), st.w.view(np.uint32))
+    assert np.array_equal(u32(opt.m), st.m.view(np.uint32))
+    for w in range(W):
+        assert np.array_equal(u32(opt.e[w]), st.e[w].view(np.uint32))
+    opt.close()
 
 
 def test_state_errors(cuda_device):
@@ -386,7 +423,7 @@ def test_profiling_counts_launches(cuda_device):
         assert prof["ef_compact"][1] == 1
         assert (prof["reduce"][1], prof["adams_sparse"][1]) == (n_red, n_upd), level
     with pytest.raises(ScapeError):
-        opt.set_fusion(3)
+        opt.set_fusion(4)
     # profiling restricted to one kernel brackets only its launches
     opt.profile_select(["ef_compact"])
     opt.profile_reset()
@@ -409,9 +446,10 @@ def test_profiling_counts_launches(cuda_device):
     ("llama1p8b", 10, (0, 3, 7)),
 ])
 def test_full_size_sampled_shards(cuda_device, name, steps, shards):
+    """At the fusion level the benchmark times: the update inside the refresh."""
     wl = synth.WORKLOADS[name]
     torch.cuda.empty_cache()
-    rep = run_sampled_shards(wl, cuda_device, steps, shards)
+    rep = run_sampled_shards(wl, cuda_device, steps, shards, fusion=C.FUSE_REFRESH)
     assert rep.exact, f"not bit-identical ({rep.flips} mask flips of {rep.mask_bits})"
     torch.cuda.empty_cache()
 
