@@ -610,8 +610,9 @@ int scape_refresh_mask(scape_t* h, void* stream) {
   if (h->warm && !h->all_dense) {
     // a deferred update runs inside the warm refresh's read of m
     SpecUpdate up{h->tile_base(), h->gbar(), h->w, h->m, h->upd_c};
-    rc = refresh_warm(h, st, h->upd_pending ? &up : nullptr);
-    if (rc == SCAPE_OK) h->upd_pending = false;
+    const bool fuse = h->upd_pending;
+    h->upd_pending = false;  // the refresh's read of m applies it
+    rc = refresh_warm(h, st, fuse ? &up : nullptr);
   } else {
     rc = flush_pending(h, st);
     if (rc == SCAPE_OK) rc = refresh_cold(h, st);
