@@ -60,7 +60,7 @@ def mask_churn(prev_bits, bits, k):
     return float(lut[x].sum().item()) / (2.0 * k) if k else 0.0
 
 
-FUSION = {"none": 0, "sum": 1, "update": 2, "refresh": 3}  # scape_set_fusion levels
+FUSION = {"none": 0, "sum": 1, "update": 2}  # scape_set_fusion levels
 
 
 def algorithmic_bytes(wl, k, fusion="sum", P=None):
@@ -74,12 +74,7 @@ def algorithmic_bytes(wl, k, fusion="sum", P=None):
     ef = W * P * (G + 8) + P / 8 + 4 * ntiles + 4 * k * W
     refresh = 4 * P + P / 8 + P / 8 + 4 * k
     out = {"refresh": refresh}
-    if fusion == "refresh":
-        # the update runs inside the refresh's read of m: g_bar, and w and
-        # m at the selected coordinates (m is read there anyway)
-        out["ef_compact"] = ef + 4 * k
-        out["refresh"] = refresh + 4 * k + 8 * k + 4 * k
-    elif fusion == "update":
+    if fusion == "update":
         out["ef_compact"] = ef + 4 * k + 16 * k
     elif fusion == "sum":
         out["ef_compact"] = ef + 4 * k

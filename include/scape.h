@@ -216,9 +216,9 @@ enum scape_variant {
 int scape_set_variant(scape_t *h, int flags);
 
 /*
- * Where the steps of a sparse step run (results are bit-identical at every
- * level).  The compaction sees every worker of a tile, so it can form the
- * synchronised buffer while the residuals stream through:
+ * How much of the step the compaction pass does (results are bit-identical
+ * at every level).  The compaction sees every worker of a tile, so it can
+ * form the synchronised buffer while the residuals stream through:
  *   SCAPE_FUSE_NONE    the ordered sum of the W packed buffers and the
  *       unpack + AdamS run as two separate launches after it, the layout of
  *       "Sintesi Tecnica: SCAPE" Sec. 2;
@@ -226,27 +226,11 @@ int scape_set_variant(scape_t *h, int flags);
  *       (worker-ordered sum / W); the unpack + AdamS runs as its own launch;
  *   SCAPE_FUSE_UPDATE  the compaction also applies AdamS at the selected
  *       coordinates (no further launch; its scattered w and m accesses then
- *       interleave with the residual stream, which measured slower);
- *   SCAPE_FUSE_REFRESH the compaction writes g_bar and the unpack + AdamS
- *       is deferred into the next scape_refresh_mask(), whose single read of
- *       m applies it before taking the new keys (the refresh reads every m
- *       anyway, so the step makes no scattered pass over m of its own).  After
- *       scape_step() the selected w and m are then not yet updated; they are
- *       after scape_refresh_mask().  Any other call that needs them (a second
- *       scape_step() without a refresh, the dense and union baselines,
- *       scape_set_state(), scape_step_host()) applies the deferred update
- *       first, as a launch of its own, and so does the first refresh after
- *       scape_bind().  Under a variant reading, or when every shard keeps all
- *       of its coordinates, this level behaves as SCAPE_FUSE_SUM.
+ *       interleave with the residual stream, which measured slower).
  * The packed buffers and g_bar are written at every level.
  * Errors: SCAPE_EINVAL for an unknown level.
  */
-enum scape_fusion {
-    SCAPE_FUSE_NONE = 0,
-    SCAPE_FUSE_SUM = 1,
-    SCAPE_FUSE_UPDATE = 2,
-    SCAPE_FUSE_REFRESH = 3
-};
+enum scape_fusion { SCAPE_FUSE_NONE = 0, SCAPE_FUSE_SUM = 1, SCAPE_FUSE_UPDATE = 2 };
 int scape_set_fusion(scape_t *h, int level);
 
 /*

@@ -201,7 +201,7 @@ def scape_set_variant(h, flags):
     _check(h, load().scape_set_variant(h, int(flags)))
 
 
-FUSE_NONE, FUSE_SUM, FUSE_UPDATE, FUSE_REFRESH = 0, 1, 2, 3
+FUSE_NONE, FUSE_SUM, FUSE_UPDATE = 0, 1, 2
 
 
 def scape_set_fusion(h, level):

@@ -84,28 +84,9 @@ int enqueue_compact(scape_t* h, const WorkerPtrs& all, int w0, int w1, bool vec,
   });
 }
 
-// Whether this handle defers the sparse update into the next refresh: only
-// under the paper's reading (the variants update differently) and when later
-// refreshes take the warm path (a handle whose shards keep every coordinate
-// always refreshes cold).
-bool defers_update(const scape_t* h) {
-  return h->fusion == SCAPE_FUSE_REFRESH && h->variant == SCAPE_VARIANT_PAPER && !h->all_dense;
-}
-
-// Apply a deferred sparse update on its own (a launch of adams_sparse).
-int flush_pending(scape_t* h, cudaStream_t st) {
-  if (!h->upd_pending) return SCAPE_OK;
-  const int rc = run_kernel(h, kKAdamsSparse, st, [&] {
-    return launch_adams_sparse(h->idx(), h->gbar(), h->k, h->w, h->m, h->upd_c, false, st);
-  });
-  if (rc == SCAPE_OK) h->upd_pending = false;
-  return rc;
-}
-
 // The ordered sum of the packed buffers and the sparse AdamS update, unless
 // the compaction already applied them (plus, under the dense off-mask
-// reading, the zero-gradient update elsewhere).  With the update deferred to
-// the refresh, only its constants are kept.
+// reading, the zero-gradient update elsewhere).
 int enqueue_update(scape_t* h, const AdamsConst& c, cudaStream_t st) {
   int rc = SCAPE_OK;
   if (h->fusion == SCAPE_FUSE_NONE) {
@@ -113,11 +94,6 @@ int enqueue_update(scape_t* h, const AdamsConst& c, cudaStream_t st) {
       return launch_reduce(h->pack(), h->kstride, h->W, h->k, h->gbar(), st);
     });
     if (rc) return rc;
-  }
-  if (defers_update(h)) {
-    h->upd_pending = true;
-    h->upd_c = c;
-    return SCAPE_OK;
   }
   if (h->fusion != SCAPE_FUSE_UPDATE) {
     const bool msync = (h->variant & SCAPE_VARIANT_MOMENT_SYNC) != 0;
@@ -434,7 +410,6 @@ int scape_bind(scape_t* h, float* params, float* m, float* const* host_e_ptrs, v
   h->mask_ready = false;
   h->warm = false;
   h->buffers_valid = false;
-  h->upd_pending = false;
   return SCAPE_OK;
 }
 
@@ -454,11 +429,9 @@ int scape_step(scape_t* h, const void* const* host_grad_ptrs, void* stream) {
     p.e[w] = h->e[w];
     vec = vec && aligned16(host_grad_ptrs[w]);
   }
-  // a deferred update of the previous step that no refresh has applied
-  int rc = flush_pending(h, st);
-  if (rc) return rc;
   const int64_t t = h->t + 1;
   const AdamsConst c = make_const(h, t);
+  int rc;
   if (t == 1) {
     rc = run_kernel(h, kKDenseStep, st, [&] {
       return launch_dense_step(p, h->W, h->P, h->dtype, vec, h->w, h->m, c,
@@ -539,7 +512,7 @@ int refresh_cold(scape_t* h, cudaStream_t st) {
 // thresholds only correct it.  Every launch is enqueued whatever the data
 // holds; the kernels for the rare cases (a shard whose threshold left its
 // bucket window) return at once when no shard needs them.
-int refresh_warm(scape_t* h, cudaStream_t st, const SpecUpdate* up) {
+int refresh_warm(scape_t* h, cudaStream_t st) {
   // Expected growth of the selected first moments since the previous refresh
   // (after step t - 1): the ratio of the bias corrections, (1 - b1^t) /
   // (1 - b1^(t-1)), in first-digit buckets (32 per octave); the bucket
@@ -558,7 +531,7 @@ int refresh_warm(scape_t* h, cudaStream_t st, const SpecUpdate* up) {
   if (e != cudaSuccess) return cuda_fail(h, e, "scape_refresh_mask: count clear");
   int rc = run_kernel(h, kKSpecMark, st, [&] {
     return launch_spec(h->m, h->P, h->map, h->d_shard_start(), h->sel(), h->cand(), h->cand_cnt(),
-                       h->above_cnt(), h->bits(), h->tile_cnt(), up, growth, st);
+                       h->above_cnt(), h->bits(), h->tile_cnt(), growth, st);
   });
   if (rc) return rc;
   rc = run_kernel(h, kKCandHist, st, [&] {
@@ -606,17 +579,7 @@ int scape_refresh_mask(scape_t* h, void* stream) {
   if (!h->bound) return fail(h, SCAPE_ESTATE, "scape_refresh_mask: call scape_bind first");
   if (h->t < 1) return fail(h, SCAPE_ESTATE, "scape_refresh_mask: no step taken yet");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  int rc;
-  if (h->warm && !h->all_dense) {
-    // a deferred update runs inside the warm refresh's read of m
-    SpecUpdate up{h->tile_base(), h->gbar(), h->w, h->m, h->upd_c};
-    const bool fuse = h->upd_pending;
-    h->upd_pending = false;  // the refresh's read of m applies it
-    rc = refresh_warm(h, st, fuse ? &up : nullptr);
-  } else {
-    rc = flush_pending(h, st);
-    if (rc == SCAPE_OK) rc = refresh_cold(h, st);
-  }
+  int rc = (h->warm && !h->all_dense) ? refresh_warm(h, st) : refresh_cold(h, st);
   if (rc) {
     h->warm = false;
     return rc;
@@ -657,8 +620,7 @@ int scape_residual_staging_bytes(const scape_t* h, int rows, size_t* bytes) {
 
 int scape_set_fusion(scape_t* h, int level) {
   if (!h) return SCAPE_EINVAL;
-  if (level != SCAPE_FUSE_NONE && level != SCAPE_FUSE_SUM && level != SCAPE_FUSE_UPDATE &&
-      level != SCAPE_FUSE_REFRESH)
+  if (level != SCAPE_FUSE_NONE && level != SCAPE_FUSE_SUM && level != SCAPE_FUSE_UPDATE)
     return fail(h, SCAPE_EINVAL, "scape_set_fusion: unknown level");
   h->fusion = level;
   return SCAPE_OK;
@@ -689,7 +651,6 @@ static int dense_baseline(scape_t* h, const void* const* grads, float* v, bool a
     p.e[w] = h->e[w];
     vec = vec && aligned16(grads[w]);
   }
-  if (const int rf = flush_pending(h, st)) return rf;
   const int64_t t = h->t + 1;
   const AdamsConst c = make_const(h, t);
   const int rc = run_kernel(h, adamw ? kKAdamW : kKDenseAdams, st, [&] {
@@ -777,7 +738,6 @@ int scape_union_step(scape_t* h, const void* const* host_grad_ptrs, void* worksp
   float* ugbar = reinterpret_cast<float*>(ws + L.gbar);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int64_t kw = union_k_worker(h);
-  if (const int rf = flush_pending(h, st)) return rf;
   cudaError_t e = cudaSuccess;
   if (h->union_ws != workspace) {
     // new workspace: one-shard table over the whole vector, no bucket guesses
@@ -909,7 +869,6 @@ int scape_set_state(scape_t* h, int64_t t, const uint32_t* bits, void* stream) {
   if (!h->bound) return fail(h, SCAPE_ESTATE, "scape_set_state: call scape_bind first");
   if (t < 1 || !bits) return fail(h, SCAPE_EINVAL, "scape_set_state: need t >= 1 and a bitmap");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (const int rf = flush_pending(h, st)) return rf;
   cudaError_t e = cudaMemcpyAsync(h->bits(), bits, (size_t)h->nwords * 4, cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(h->counts(), 0, (size_t)(h->S + 1) * 4, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "scape_set_state: copy");
@@ -971,8 +930,7 @@ int scape_step_host(scape_t* h, const void* const* host_grads_src, void* const* 
     return SCAPE_OK;
   }
   {
-    int rc = ensure_aux(h);
-    if (rc == SCAPE_OK) rc = flush_pending(h, st);  // the previous parameters are copied out
+    const int rc = ensure_aux(h);
     if (rc) return rc;
   }
   // Parameters: under the paper's reading a step changes w only at its k
@@ -1025,7 +983,6 @@ int scape_step_host(scape_t* h, const void* const* host_grads_src, void* const* 
     if (rc) return rc;
   }
   int rc = enqueue_update(h, c, st);
-  if (rc == SCAPE_OK) rc = flush_pending(h, st);  // w is copied out below
   if (rc) return rc;
   h->t = t;
   h->buffers_valid = true;

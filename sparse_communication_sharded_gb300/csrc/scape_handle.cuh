@@ -56,10 +56,6 @@ struct scape {
   bool all_dense = false;  // every shard keeps all of its coordinates
   int variant = SCAPE_VARIANT_PAPER;
   int fusion = SCAPE_FUSE_SUM;  // what the compaction pass also does
-  // SCAPE_FUSE_REFRESH: the last step's sparse update, not yet applied (it
-  // runs inside the next refresh's read of m, or on its own when needed)
-  bool upd_pending = false;
-  AdamsConst upd_c{};
   // workspace offsets (bytes)
   size_t off_bits = 0, off_idx = 0, off_tbase = 0, off_tcnt = 0, off_pack = 0, off_gbar = 0,
          off_hist = 0, off_sel = 0, off_cand = 0, off_ccnt = 0, off_scan = 0, off_sstart = 0,

@@ -293,27 +293,13 @@ constexpr int kCandBins0 = 1 << kDigit0;
 cudaError_t launch_chist0(const float* m, int64_t P, const ShardMap& sm, const int64_t* shard_start,
                           const ShardSel* sel, uint32_t* hist, uint2* cand, uint32_t* cand_cnt,
                           bool selective, int growth, cudaStream_t st);
-// The step's sparse AdamS update, applied inside the warm refresh's read of m
-// (launch_spec with a SpecUpdate): tbase is the rank table of the mask the
-// step used (still in `bits` when the refresh starts), gbar its synchronised
-// buffer, w and m the parameters and first moment (m is the array the refresh
-// reads; it is updated in place).
-struct SpecUpdate {
-  const uint32_t* tbase;
-  const float* gbar;
-  float* w;
-  float* m;
-  AdamsConst c;
-};
 // Warm refresh: one read of m that writes the bitmap words and popcounts of
 // every whole single-shard tile from the shard's previous threshold (tile_cnt
 // zeroed first), stages the candidates of the previous bucket window and counts
-// the parameters above it (above_cnt zeroed first); with `up`, it applies the
-// step's update at the coordinates the old bitmap selects first.
+// the parameters above it (above_cnt zeroed first).
 cudaError_t launch_spec(const float* m, int64_t P, const ShardMap& sm, const int64_t* shard_start,
                         const ShardSel* sel, uint2* cand, uint32_t* cand_cnt, uint32_t* above_cnt,
-                        uint32_t* bits, uint32_t* tile_cnt, const SpecUpdate* up, int growth,
-                        cudaStream_t st);
+                        uint32_t* bits, uint32_t* tile_cnt, int growth, cudaStream_t st);
 // Window histogram of the staged candidates with the outside counts lumped.
 cudaError_t launch_whist(int W, int blocks_per_shard, const int64_t* shard_start,
                          const ShardSel* sel, const uint2* cand, const uint32_t* cand_cnt,

@@ -267,39 +267,17 @@ mpass_kernel(const float* __restrict__ m, int64_t P, ShardMap sm,
 //    previous threshold selected in whole tiles.
 // Partial pieces (shard boundaries inside a tile, the ragged end) are only
 // staged and counted; the remark kernel writes their bits.
-//
-// With UPD the kernel also applies the step's AdamS update ("SCAPE" Sec. II-C,
-// Eq. 2) at the coordinates the step's (lagged) mask selected, so that the
-// step needs no scattered pass over m of its own: the refresh reads every m
-// anyway.  The step's mask is the bitmap being overwritten, so each tile's
-// old words are read (by every warp: all 64 words, for the within-tile
-// ranks) before a block barrier, and the new words are stored after it.  For
-// an old-selected coordinate i with rank r (tile base of the step's rank
-// table plus the old bits before i), m_t = b1 m + (1 - b1) g_bar[r] replaces
-// the value in registers -- the key of the new mask is |m_t| -- and is stored;
-// the parameter update, which needs w[i] and more arithmetic, goes to a
-// per-warp queue of (i, g, m_{t-1}) entries that is worked off 32 at a time,
-// one entry per lane.  Shards without a previous threshold (every coordinate
-// kept, or empty) get the update only.  The arithmetic is adams_update's, so
-// the results equal a separate update launch bit for bit.
 constexpr int kSpecBlocksPerSm = 4;
 constexpr int kLaneSlots = 16;  // staged candidates per lane
-constexpr int kUpdQueue = 64;   // queued parameter updates per warp
 
-struct UpdEntry {
-  uint32_t i;
-  float g, m_prev;
-};
-
-template <bool UPD>
 __global__ void __launch_bounds__(256, kSpecBlocksPerSm)
-spec_kernel(const float* m, int64_t P, ShardMap sm, const int64_t* __restrict__ shard_start,
+spec_kernel(const float* __restrict__ m, int64_t P, ShardMap sm,
+            const int64_t* __restrict__ shard_start,
             const ShardSel* __restrict__ sel, uint2* __restrict__ cand,
             uint32_t* __restrict__ cand_cnt, uint32_t* __restrict__ above_cnt,
             uint32_t* __restrict__ bits, uint32_t* __restrict__ tile_cnt, int64_t segs_per_block,
-            SpecUpdate up, int growth) {
+            int growth) {
   __shared__ uint2 lbuf[8][kLaneSlots * 32];
-  __shared__ UpdEntry uq[UPD ? 8 : 1][UPD ? kUpdQueue : 1];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t nseg = (P + kMSeg - 1) / kMSeg;
   const int64_t g0 = (int64_t)blockIdx.x * segs_per_block;
@@ -309,13 +287,12 @@ spec_kernel(const float* m, int64_t P, ShardMap sm, const int64_t* __restrict__ 
   const uint32_t r0 = (uint32_t)(g0 * kMSeg), r1 = (uint32_t)min(g1 * kMSeg, P);
   const int W = sm.S;
   int s = sm.of(r0);
-  if (!UPD) {
+  {
     bool any = false;
     for (int q = s; q < W && (uint32_t)__ldg(shard_start + q) < r1; ++q)
       any |= sel[q].guess != kNoGuess;
     if (!any) return;
   }
-  const uint32_t lt_mask = (1u << lane) - 1u;
   uint2* const col = lbuf[warp] + lane;  // this lane's column: slot j at col[32 * j]
   const uint32_t col_s = (uint32_t)__cvta_generic_to_shared(col);
   uint32_t nl = 0;                       // this lane's staged candidates
@@ -344,55 +321,6 @@ spec_kernel(const float* m, int64_t P, ShardMap sm, const int64_t* __restrict__ 
     nl = 0;
   };
 
-  // ---- the fused update (UPD)
-  uint32_t qn = 0;  // entries in this warp's update queue (the same in every lane)
-  // parameter updates of the queued entries, 32 at a time (all when `all`)
-  auto drain = [&](bool all) {
-    while (qn >= 32u || (all && qn > 0u)) {
-      const uint32_t np = qn < 32u ? qn : 32u;
-      __syncwarp();
-      if ((uint32_t)lane < np) {
-        const UpdEntry e = uq[warp][lane];
-        float wv = up.w[e.i], mv = e.m_prev;
-        adams_update(e.g, wv, mv, up.c);
-        up.w[e.i] = wv;
-      }
-      __syncwarp();
-      if ((uint32_t)lane + 32u < qn) uq[warp][lane] = uq[warp][lane + 32];
-      qn -= np;
-    }
-    __syncwarp();
-  };
-  // old-selected coordinate i (rank r) whose first moment is x: m_t into x
-  // and into m, the parameter update queued at `slot`
-  auto update_m = [&](uint32_t i, uint32_t r, float& x, uint32_t slot) {
-    const float g = __ldg(up.gbar + r);
-    const float mn = __fadd_rn(__fmul_rn(up.c.beta1, x), __fmul_rn(up.c.one_minus_b1, g));
-    uq[warp][slot] = UpdEntry{i, g, x};
-    x = mn;
-    up.m[i] = mn;
-  };
-  // rank of coordinate i in the step's mask: the tile's base plus the old
-  // bits before i in its tile (only for pieces the kernel does not rewrite)
-  auto old_rank = [&](uint32_t i) -> uint32_t {
-    const uint32_t t = i / kMSeg;
-    uint32_t r = __ldg(up.tbase + t);
-    for (uint32_t j = t * (kMSeg / 32); j < i / 32; ++j) r += __popc(bits[j]);
-    return r + __popc(bits[i / 32] & ((1u << (i & 31)) - 1u));
-  };
-  // one round of up to 256 coordinates [b0, b0 + 256) of a piece whose bitmap
-  // words this kernel does not write; returns the (possibly updated) value
-  auto piece_update = [&](uint32_t i, bool in, float x) -> float {
-    const bool sel_old = in && ((bits[i / 32] >> (i & 31)) & 1u);
-    const uint32_t bal = __ballot_sync(0xffffffffu, sel_old);
-    if (bal) {
-      if (sel_old) update_m(i, old_rank(i), x, qn + __popc(bal & lt_mask));
-      qn += __popc(bal);
-      if (qn >= 32u) drain(false);
-    }
-    return x;
-  };
-
   uint32_t pos = r0;
   while (pos < r1) {
     while (s < W - 1 && (uint32_t)__ldg(shard_start + s + 1) <= pos) ++s;
@@ -412,10 +340,8 @@ spec_kernel(const float* m, int64_t P, ShardMap sm, const int64_t* __restrict__ 
       auto piece = [&](uint32_t a, uint32_t b) {
         for (uint32_t b0 = a; b0 < b; b0 += 256) {
           const uint32_t i = b0 + threadIdx.x;
-          float x = i < b ? __ldcs(m + i) : 0.f;
-          if (UPD) x = piece_update(i, i < b, x);
           if (i < b) {
-            const uint32_t key = magnitude_key(x);
+            const uint32_t key = magnitude_key(__ldcs(m + i));
             acount += key >= top_key ? 1u : 0u;
             if (key - wkey_lo < wkey_n) put(key, i);
           }
@@ -435,64 +361,11 @@ spec_kernel(const float* m, int64_t P, ShardMap sm, const int64_t* __restrict__ 
         uint32_t* bw = bits + (size_t)ta * (kMSeg / 32) + 4 * warp;
         float xc[8], xn[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) xc[j] = __ldcs(p + kMSeg * 0 + 1024 * (j >> 2) + 32 * (j & 3));
-        // UPD: the old words 2 lane, 2 lane + 1 of the tile, and its old rank base
-        uint2 oc = make_uint2(0u, 0u), on = make_uint2(0u, 0u);
-        uint32_t obc = 0, obn = 0;
-        if (UPD) {
-          oc = *reinterpret_cast<const uint2*>(bits + (size_t)ta * (kMSeg / 32) + 2 * lane);
-          obc = __ldg(up.tbase + ta);
-        }
+        for (int j = 0; j < 8; ++j) xc[j] = __ldcs(p + 1024 * (j >> 2) + 32 * (j & 3));
         for (uint32_t t = ta; t < tb; ++t) {
           if (t + 1 < tb) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) xn[j] = __ldcs(p + kMSeg + 1024 * (j >> 2) + 32 * (j & 3));
-            if (UPD) {
-              on = *reinterpret_cast<const uint2*>(bits + (size_t)(t + 1) * (kMSeg / 32) +
-                                                   2 * lane);
-              obn = __ldg(up.tbase + t + 1);
-            }
-          }
-          if (UPD) {
-            // ranks of this warp's old-selected coordinates: exclusive prefix
-            // of the old popcounts over the tile's word pairs
-            const uint32_t pc = __popc(oc.x) + __popc(oc.y);
-            uint32_t incl = pc;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-              const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-              if (lane >= o) incl += v;
-            }
-            const uint32_t excl = incl - pc;
-            uint32_t ow[8], pre[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int L = 16 * h + 2 * warp;  // word 32h + 4w + q sits in lane L + q / 2
-              ow[4 * h + 0] = __shfl_sync(0xffffffffu, oc.x, L);
-              ow[4 * h + 1] = __shfl_sync(0xffffffffu, oc.y, L);
-              ow[4 * h + 2] = __shfl_sync(0xffffffffu, oc.x, L + 1);
-              ow[4 * h + 3] = __shfl_sync(0xffffffffu, oc.y, L + 1);
-              pre[h] = __shfl_sync(0xffffffffu, excl, L);
-            }
-            // every warp has read the tile's old words: they may be overwritten
-            __syncthreads();
-            const uint32_t ibase = t * kMSeg + 128 * warp + lane;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              uint32_t run = obc + pre[h];
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const uint32_t wd = ow[4 * h + q];
-                if (wd) {
-                  if ((wd >> lane) & 1u)
-                    update_m(ibase + 1024 * h + 32 * q, run + __popc(wd & lt_mask), xc[4 * h + q],
-                             qn + __popc(wd & lt_mask));
-                  run += __popc(wd);
-                  qn += __popc(wd);
-                  if (qn >= 32u) drain(false);
-                }
-              }
-            }
           }
           // selected: key > kstar, or key == kstar and i <= istar
           const uint32_t thr = kstar + (t > t_is ? 1u : 0u);
@@ -534,10 +407,6 @@ spec_kernel(const float* m, int64_t P, ShardMap sm, const int64_t* __restrict__ 
           if (t + 1 < tb) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) xc[j] = xn[j];
-            if (UPD) {
-              oc = on;
-              obc = obn;
-            }
           }
         }
         piece(tb * kMSeg, end);
@@ -545,18 +414,9 @@ spec_kernel(const float* m, int64_t P, ShardMap sm, const int64_t* __restrict__ 
       flush_lanes(s);
       const uint32_t a = __reduce_add_sync(0xffffffffu, acount);
       if (lane == 0 && a) atomicAdd(above_cnt + s, a);
-    } else if (UPD) {
-      // no previous threshold (every coordinate kept, or an empty shard):
-      // only the update; the remark kernel writes the bits
-      for (uint32_t b0 = pos; b0 < end; b0 += 256) {
-        const uint32_t i = b0 + threadIdx.x;
-        const float x = i < end ? __ldcs(m + i) : 0.f;
-        piece_update(i, i < end, x);
-      }
     }
     pos = end;
   }
-  if (UPD) drain(true);
 }
 
 // ------------------------------------------------------------------ whist
@@ -848,16 +708,11 @@ cudaError_t launch_chist0(const float* m, int64_t P, const ShardMap& sm, const i
 
 cudaError_t launch_spec(const float* m, int64_t P, const ShardMap& sm, const int64_t* shard_start,
                         const ShardSel* sel, uint2* cand, uint32_t* cand_cnt, uint32_t* above_cnt,
-                        uint32_t* bits, uint32_t* tile_cnt, const SpecUpdate* up, int growth,
-                        cudaStream_t st) {
+                        uint32_t* bits, uint32_t* tile_cnt, int growth, cudaStream_t st) {
   int64_t spb = 1;
   const int grid = mpass_grid(P, kSpecBlocksPerSm, &spb);
-  if (up)
-    spec_kernel<true><<<grid, 256, 0, st>>>(m, P, sm, shard_start, sel, cand, cand_cnt, above_cnt,
-                                            bits, tile_cnt, spb, *up, growth);
-  else
-    spec_kernel<false><<<grid, 256, 0, st>>>(m, P, sm, shard_start, sel, cand, cand_cnt,
-                                             above_cnt, bits, tile_cnt, spb, SpecUpdate{}, growth);
+  spec_kernel<<<grid, 256, 0, st>>>(m, P, sm, shard_start, sel, cand, cand_cnt, above_cnt, bits,
+                                    tile_cnt, spb, growth);
   return cudaGetLastError();
 }
 

@@ -113,11 +113,9 @@ class Scape:
         C.scape_set_variant(self.h, flags)
 
     def set_fusion(self, level):
-        """Where the sparse step's work runs: C.FUSE_NONE (separate reduce and
-        adams_sparse launches), C.FUSE_SUM (the compaction writes g_bar),
-        C.FUSE_UPDATE (it also applies AdamS) or C.FUSE_REFRESH (the AdamS
-        update runs inside the next refresh_mask(); params and m are current
-        after it); results are bit-identical."""
+        """How much of the step the compaction pass does: C.FUSE_NONE (separate
+        reduce and adams_sparse launches), C.FUSE_SUM (it writes g_bar) or
+        C.FUSE_UPDATE (it also applies AdamS); results are bit-identical."""
         C.scape_set_fusion(self.h, level)
 
     def dense_adams_step(self, grads):

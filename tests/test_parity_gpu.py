@@ -48,16 +48,15 @@ def test_trajectory_matches_oracle(cuda_device, P, W, s, dtype, quant):
     assert rep.exact, "trajectory not bit-identical to the oracle"
 
 
-@pytest.mark.parametrize("fusion", [C.FUSE_NONE, C.FUSE_SUM, C.FUSE_UPDATE, C.FUSE_REFRESH])
+@pytest.mark.parametrize("fusion", [C.FUSE_NONE, C.FUSE_SUM, C.FUSE_UPDATE])
 @pytest.mark.parametrize("P,W,s,dtype,quant", [TRAJ[1], TRAJ[2], TRAJ[4], TRAJ[5], TRAJ[6],
                                                 TRAJ[7], TRAJ[9], TRAJ[10],
                                                 (11, 8, 0.5, "f32", False),
                                                 (300001, 3, 0.9, "bf16", False)])
 def test_trajectory_every_fusion_level(cuda_device, fusion, P, W, s, dtype, quant):
     """Separate launches (ordered sum, then unpack + AdamS), the sum inside the
-    compaction, sum + update inside it, and the update inside the next
-    refresh's read of m all give the oracle's bits.  (11, 8, 0.5) mixes shards
-    that keep every coordinate (no threshold: update only) with searched ones."""
+    compaction, and sum + update inside it all give the oracle's bits.
+    (11, 8, 0.5) mixes shards that keep every coordinate with searched ones."""
     rep = run_full_trajectory(_wl(P, W, s, dtype, quant=quant), cuda_device, steps=6,
                               fusion=fusion)
     assert rep.exact
@@ -309,7 +308,6 @@ def test_set_state_rejects_wrong_counts(cuda_device):
 @pytest.mark.parametrize("P,W,variant,fusion", [(50000, 4, 0, None), (30011, 32, 0, C.FUSE_UPDATE),
                                                 (30011, 32, 0, C.FUSE_SUM),
                                                 (30011, 32, 0, C.FUSE_NONE),
-                                                (30011, 32, 0, C.FUSE_REFRESH),
                                                 (20000, 3, 1, None)])
 def test_host_buffer_path_matches_device_path(cuda_device, P, W, variant, fusion):
     """scape_step_host (uploads in worker groups, the parameter download before
@@ -352,10 +350,9 @@ def test_host_buffer_path_matches_device_path(cuda_device, P, W, variant, fusion
         assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
 
 
-@pytest.mark.parametrize("fusion", [C.FUSE_SUM, C.FUSE_REFRESH])
+@pytest.mark.parametrize("fusion", [C.FUSE_NONE, C.FUSE_SUM, C.FUSE_UPDATE])
 def test_step_without_refresh_reuses_the_older_mask(cuda_device, fusion):
-    """Skipping a refresh reuses the older mask; with the update deferred to
-    the refresh, the next step applies it on its own first.  Pattern: step 1,
+    """Skipping a refresh reuses the older mask.  Pattern: step 1,
     refresh, steps 2 and 3 on that mask, refresh, step 4, refresh -- against
     the oracle's steps taken in the same order."""
     P, W, s = 70001, 4, 0.99
@@ -423,7 +420,7 @@ def test_profiling_counts_launches(cuda_device):
         assert prof["ef_compact"][1] == 1
         assert (prof["reduce"][1], prof["adams_sparse"][1]) == (n_red, n_upd), level
     with pytest.raises(ScapeError):
-        opt.set_fusion(4)
+        opt.set_fusion(3)
     # profiling restricted to one kernel brackets only its launches
     opt.profile_select(["ef_compact"])
     opt.profile_reset()
@@ -446,10 +443,9 @@ def test_profiling_counts_launches(cuda_device):
     ("llama1p8b", 10, (0, 3, 7)),
 ])
 def test_full_size_sampled_shards(cuda_device, name, steps, shards):
-    """At the fusion level the benchmark times: the update inside the refresh."""
     wl = synth.WORKLOADS[name]
     torch.cuda.empty_cache()
-    rep = run_sampled_shards(wl, cuda_device, steps, shards, fusion=C.FUSE_REFRESH)
+    rep = run_sampled_shards(wl, cuda_device, steps, shards)
     assert rep.exact, f"not bit-identical ({rep.flips} mask flips of {rep.mask_bits})"
     torch.cuda.empty_cache()
 
