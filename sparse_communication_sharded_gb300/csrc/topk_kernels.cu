@@ -40,18 +40,21 @@ __device__ __forceinline__ uint64_t composite(uint32_t key, uint32_t i) {
 
 // The first-digit buckets [lo, hi] a refresh stages candidates from: one
 // either side of the previous threshold's bucket, stretched toward the bucket
-// the last two thresholds extrapolate to (at most kMaxTrend buckets on) and
-// toward `growth` buckets above it.  Early in training the first moments grow
-// from step to step -- the exponential average starts from zero, so a
-// coordinate that keeps being selected grows by about the ratio of the bias
-// corrections, (1 - b1^t) / (1 - b1^(t-1)): x1.9 at the second step with
-// b1 = 0.9, x1.43 at the third -- and the threshold with them; the host
-// passes that ratio in buckets (32 per octave) as `growth` (0 when unknown).
-// hi may be 8192 (no such digit).  With no previous bucket the window is
-// empty (lo > hi).
+// the last two thresholds extrapolate to (at most kMaxTrend buckets on), and
+// widened to `growth` buckets either side while the first moments are still
+// warming up.  The exponential average starts from zero, so in the first
+// steps the selected coordinates grow by about the ratio of the bias
+// corrections, (1 - b1^t) / (1 - b1^(t-1)) -- x1.9 at the second step with
+// b1 = 0.9 -- while the threshold, the k_s-th largest |m| and so the lower
+// tail of the selected group, moves by a fraction of that in either
+// direction (up to about 10 buckets on the Llama-500M-shaped workload in
+// steps 2 to 5, then by 0 or 1); the host passes the ratio in buckets
+// (32 per octave) as `growth` (0 when unknown; below 4, from about the eighth
+// step with b1 = 0.9, the window is not widened).  hi may be 8192 (no such
+// digit).  With no previous bucket the window is empty (lo > hi).
 constexpr int kMaxTrend = 16;
-constexpr int kMaxGrowth = 32;
-constexpr int kMaxWindow = 2 * 1 + kMaxTrend + kMaxGrowth + 1;  // buckets in the widest window
+constexpr int kMaxGrowth = 24;
+constexpr int kMaxWindow = 2 * kMaxGrowth + 3;  // buckets in the widest window
 
 __device__ __forceinline__ void bucket_window(const ShardSel& q, int growth, uint32_t& lo,
                                               uint32_t& hi) {
@@ -64,16 +67,17 @@ __device__ __forceinline__ void bucket_window(const ShardSel& q, int growth, uin
   if (q.guess_prev != kNoGuess) {
     int d = (int)q.guess - (int)q.guess_prev;
     d = d > kMaxTrend ? kMaxTrend : (d < -kMaxTrend ? -kMaxTrend : d);
-    int pred = (int)q.guess + d;
-    pred = pred < 0 ? 0 : (pred > kCBins0 - 1 ? kCBins0 - 1 : pred);
+    const int pred = (int)q.guess + d;
     a = pred < a ? pred : a;
     b = pred > b ? pred : b;
   }
-  if (growth > 0) {
-    int g = (int)q.guess + (growth > kMaxGrowth ? kMaxGrowth : growth);
-    g = g > kCBins0 - 1 ? kCBins0 - 1 : g;
-    b = g > b ? g : b;
+  if (growth >= 4) {  // the warm-up (a few steps); afterwards the +-1 window holds
+    const int h = growth > kMaxGrowth ? kMaxGrowth : growth;
+    a = (int)q.guess - h < a ? (int)q.guess - h : a;
+    b = (int)q.guess + h > b ? (int)q.guess + h : b;
   }
+  a = a < 0 ? 0 : a;
+  b = b > kCBins0 - 1 ? kCBins0 - 1 : b;
   lo = (uint32_t)(a > 0 ? a - 1 : 0);
   hi = (uint32_t)(b + 1);
 }
@@ -295,16 +299,18 @@ spec_kernel(const float* __restrict__ m, int64_t P, ShardMap sm,
   }
   uint2* const col = lbuf[warp] + lane;  // this lane's column: slot j at col[32 * j]
   const uint32_t col_s = (uint32_t)__cvta_generic_to_shared(col);
-  uint32_t nl = 0;                       // this lane's staged candidates
-  // append (key, i) to this lane's column: a 32-bit shared-memory address
+  // the next free slot of this lane's column (a 32-bit shared-memory address,
+  // 256 bytes per slot); its distance from col_s counts the staged candidates
+  uint32_t sa = col_s;
+  const uint32_t sa_full = col_s + 256u * kLaneSlots, sa_tile = col_s + 256u * (kLaneSlots - 8);
   auto put = [&](uint32_t key, uint32_t i) {
-    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(col_s + 256u * nl), "r"(key), "r"(i)
-                 : "memory");
-    ++nl;
+    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(sa), "r"(key), "r"(i) : "memory");
+    sa += 256u;
   };
 
   // place every lane's column in the shard's candidate range
   auto flush_lanes = [&](int shard) {
+    const uint32_t nl = (sa - col_s) >> 8;
     uint32_t incl = nl;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -318,7 +324,7 @@ spec_kernel(const float* __restrict__ m, int64_t P, ShardMap sm,
     base = __shfl_sync(0xffffffffu, base, 0);
     uint2* out = cand + __ldg(shard_start + shard) + base + (incl - nl);
     for (uint32_t j = 0; j < nl; ++j) out[j] = col[32 * j];
-    nl = 0;
+    sa = col_s;
   };
 
   uint32_t pos = r0;
@@ -345,7 +351,7 @@ spec_kernel(const float* __restrict__ m, int64_t P, ShardMap sm,
             acount += key >= top_key ? 1u : 0u;
             if (key - wkey_lo < wkey_n) put(key, i);
           }
-          if (__any_sync(0xffffffffu, nl == kLaneSlots)) flush_lanes(s);
+          if (__any_sync(0xffffffffu, sa == sa_full)) flush_lanes(s);
         }
       };
 
@@ -354,19 +360,13 @@ spec_kernel(const float* __restrict__ m, int64_t P, ShardMap sm,
         piece(pos, end);
       } else {
         piece(pos, ta * kMSeg);
-        if (__any_sync(0xffffffffu, nl > kLaneSlots - 8)) flush_lanes(s);  // a tile adds <= 8
+        if (__any_sync(0xffffffffu, sa > sa_tile)) flush_lanes(s);  // a tile adds <= 8
         const uint32_t t_is = istar / kMSeg;  // the tile holding istar
         const int lim = (int)(istar - t_is * kMSeg);
         const float* p = m + (size_t)ta * kMSeg + 128 * warp + lane;
         uint32_t* bw = bits + (size_t)ta * (kMSeg / 32) + 4 * warp;
-        float xc[8], xn[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) xc[j] = __ldcs(p + 1024 * (j >> 2) + 32 * (j & 3));
-        for (uint32_t t = ta; t < tb; ++t) {
-          if (t + 1 < tb) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) xn[j] = __ldcs(p + kMSeg + 1024 * (j >> 2) + 32 * (j & 3));
-          }
+        // one whole tile t whose values x this warp holds
+        auto tile = [&](uint32_t t, const float (&x)[8]) {
           // selected: key > kstar, or key == kstar and i <= istar
           const uint32_t thr = kstar + (t > t_is ? 1u : 0u);
           const bool mixed = t == t_is;
@@ -378,14 +378,14 @@ spec_kernel(const float* __restrict__ m, int64_t P, ShardMap sm,
             if (!mixed) {
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
-                const uint32_t key = magnitude_key(xc[4 * h + q]);
+                const uint32_t key = magnitude_key(x[4 * h + q]);
                 wd[q] = __ballot_sync(0xffffffffu, key >= thr);
                 if (key - wkey_lo < wkey_n) put(key, ibase + 1024 * h + 32 * q);
               }
             } else {
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
-                const uint32_t key = magnitude_key(xc[4 * h + q]);
+                const uint32_t key = magnitude_key(x[4 * h + q]);
                 wd[q] = __ballot_sync(
                     0xffffffffu,
                     key >= kstar + (uint32_t)(1024 * h + 128 * warp + 32 * q + lane > lim));
@@ -401,13 +401,28 @@ spec_kernel(const float* __restrict__ m, int64_t P, ShardMap sm,
             atomicAdd(tile_cnt + t, tc);
             acount += tc;
           }
-          if (__any_sync(0xffffffffu, nl > kLaneSlots - 8)) flush_lanes(s);
-          p += kMSeg;
+          if (__any_sync(0xffffffffu, sa > sa_tile)) flush_lanes(s);
           bw += kMSeg / 32;
+        };
+        // two tiles per round, so that the next tile's values load into the
+        // other register set while one is marked (no copies between them)
+        float xa[8], xb[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) xa[j] = __ldcs(p + 1024 * (j >> 2) + 32 * (j & 3));
+        for (uint32_t t = ta; t < tb; t += 2) {
           if (t + 1 < tb) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) xc[j] = xn[j];
+            for (int j = 0; j < 8; ++j) xb[j] = __ldcs(p + kMSeg + 1024 * (j >> 2) + 32 * (j & 3));
           }
+          tile(t, xa);
+          if (t + 1 >= tb) break;
+          if (t + 2 < tb) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              xa[j] = __ldcs(p + 2 * kMSeg + 1024 * (j >> 2) + 32 * (j & 3));
+          }
+          tile(t + 1, xb);
+          p += 2 * kMSeg;
         }
         piece(tb * kMSeg, end);
       }
