@@ -72,7 +72,8 @@ def algorithmic_bytes(wl, k, fusion="sum", P=None):
     P, W, G = (wl.P if P is None else P), wl.W, _grad_bytes(wl)
     ntiles = (P + 2047) // 2048
     ef = W * P * (G + 8) + P / 8 + 4 * ntiles + 4 * k * W
-    refresh = 4 * P + P / 8 + P / 8 + 4 * k
+    # a mask that keeps every coordinate never changes: no refresh after the first
+    refresh = 0 if k >= P else 4 * P + P / 8 + P / 8 + 4 * k
     out = {"refresh": refresh}
     if fusion == "update":
         out["ef_compact"] = ef + 4 * k + 16 * k
@@ -572,6 +573,13 @@ def bench_gpu(args, wl):
     torch.cuda.synchronize()
     opt.profile_collect()
     prof = opt.profile_read()
+    # the scattered update's floor on this GPU: its memory accesses alone
+    opt.profile_reset()
+    for _ in range(3):
+        opt.probe_random_access()
+    torch.cuda.synchronize()
+    opt.profile_collect()
+    probe_ms = opt.profile_read()["probe_rmw"][0] / 3
     opt.profile(False)
 
     my_ms = sum(step_ms) / len(step_ms)
@@ -596,6 +604,18 @@ def bench_gpu(args, wl):
                              "share": ms / max(sum(m for m, _ in prof.values()), 1e-9)}
     step_kernels = ("dense_step", "ef_compact", "reduce", "adams_sparse")
     refresh_ms = sum(ms for name, (ms, _) in prof.items() if name not in step_kernels) / n_break
+    upd_ms, upd_n = prof["adams_sparse"]
+    upd_ms = upd_ms / max(upd_n, 1)
+    update_roofline = None
+    if upd_n:
+        update_roofline = {
+            "kernel": "adams_sparse", "bound": "random DRAM accesses",
+            "ms_per_launch": upd_ms, "alg_bytes_per_launch": 24 * opt.k,
+            "achieved_gbs": 24 * opt.k / (upd_ms / 1000.0) / 1e9,
+            "frac_of_hbm_peak": 24 * opt.k / (upd_ms / 1000.0) / 1e9 / peak,
+            "probe_ms": probe_ms, "frac_of_probe": probe_ms / upd_ms,
+            "note": "probe = the same scattered reads and writes of w and m (and in-order idx "
+                    "and g_bar) without the arithmetic, on this GPU: the floor of this kernel"}
 
     # dense baselines on the same workload and buffers (after the SCAPE timing)
     baselines = None
@@ -658,6 +678,7 @@ def bench_gpu(args, wl):
                          "frac": ef_gbs / peak, "traffic": traffic,
                          "alg_bytes_per_launch": alg["ef_compact"], "ms_per_launch": ef_avg},
             "kernels": kernels,
+            "update_roofline": update_roofline,
             "kernels_measured_over": f"{n_break} profiled steps after the timed ones",
             "refresh_ms_per_step": refresh_ms,
             "mask_churn_per_refresh": churn,

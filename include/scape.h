@@ -191,7 +191,9 @@ int scape_step(scape_t *h, const void *const *host_grad_ptrs, void *stream);
  * after scape_bind() reads m two or three times; every later call reads it
  * once, writing the bitmap from the previous threshold and correcting it,
  * as long as each shard's threshold stays near the previous one (a shard
- * whose threshold moved further is counted and re-marked in full).
+ * whose threshold moved further is counted and re-marked in full).  When
+ * every shard keeps all of its coordinates (sparsity 0, or shards of one
+ * parameter) the mask is all ones and only the first call does any work.
  * Errors: SCAPE_ESTATE before the first step.
  */
 int scape_refresh_mask(scape_t *h, void *stream);
@@ -346,7 +348,7 @@ int scape_step_host(scape_t *h, const void *const *host_grads_src,
  * scape_profile_read() copies the totals (milliseconds and launch counts,
  * SCAPE_NUM_KERNELS entries each) and scape_kernel_name() names entry i.
  */
-#define SCAPE_NUM_KERNELS 24
+#define SCAPE_NUM_KERNELS 25
 int scape_profile_enable(scape_t *h, int on);
 /* Which kernels profiling brackets: bit i for kernel i (default: all).  Two
  * event records per launch cost the GPU a few microseconds; a timing run can
@@ -359,6 +361,18 @@ const char *scape_kernel_name(int i);
 
 /* Total kernel launches made through this handle since creation. */
 int64_t scape_launch_count(const scape_t *h);
+
+/*
+ * A timing probe of the GPU, not a step of the method: the memory accesses of
+ * the sparse update -- the index list and the synchronised buffer read in
+ * order, w[i] and m[i] read and written back at the k coordinates of the
+ * current mask -- without its arithmetic.  w and m are left bit for bit as
+ * they were.  Its time is the floor the scattered update can reach on this
+ * GPU (the accesses are scattered 4-byte reads and writes, bound by the rate
+ * of random DRAM accesses rather than by bytes).  Profiled as "probe_rmw".
+ * Errors: SCAPE_ESTATE before a mask exists.
+ */
+int scape_probe_random_access(scape_t *h, void *stream);
 
 /*
  * Per-shard top-k mask that allocates nothing.  The SCAPE pages have no

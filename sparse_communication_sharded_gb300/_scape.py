@@ -19,7 +19,7 @@ SCAPE_ESTATE = -4
 SCAPE_F32 = 0
 SCAPE_BF16 = 1
 SCAPE_MAX_WORKERS = 256
-SCAPE_NUM_KERNELS = 24
+SCAPE_NUM_KERNELS = 25
 
 LIB_PATH = _build.LIB
 
@@ -68,6 +68,7 @@ _PROTOS = {
     "scape_kernel_name": (ctypes.c_char_p, [_i32]),
     "scape_launch_count": (_i64, [_vp]),
     "scape_topk_mask_static": (_i32, [_vp, _i64, _i32, _f64, _vp, _vp, _vp]),
+    "scape_probe_random_access": (_i32, [_vp, _vp]),
     "scape_xc_create": (_i32, [ctypes.POINTER(_vp), _i32, _vp, _i32, _i32, _i32, _f64, _f32, _f32,
                                _f32, _f32, _f32, _i32]),
     "scape_xc_destroy": (None, [_vp]),
@@ -310,6 +311,10 @@ def scape_kernel_name(i):
 
 def scape_launch_count(h):
     return load().scape_launch_count(h)
+
+
+def scape_probe_random_access(h, stream=0):
+    _check(h, load().scape_probe_random_access(h, stream))
 
 
 SCAPE_STATIC_MAX_P = 1 << 26

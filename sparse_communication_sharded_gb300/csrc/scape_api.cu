@@ -47,7 +47,7 @@ const char* const kKernelNames[kNumKernels] = {
     "dense_step",  "ef_compact", "reduce", "adams_sparse", "cand_hist0", "cand_select",
     "cand_collect", "cand_hist",  "mark",   "scan",         "index",      "shard_count",
     "tile_count",  "offmask",    "dense_adams", "adamw", "ef_add", "union_move", "spec_mark",
-    "fixup", "remark", "param_patch", "dense_update", "xc_move"};
+    "fixup", "remark", "param_patch", "dense_update", "xc_move", "probe_rmw"};
 
 }  // namespace host
 }  // namespace scapek
@@ -578,6 +578,9 @@ int scape_refresh_mask(scape_t* h, void* stream) {
   if (!h) return SCAPE_EINVAL;
   if (!h->bound) return fail(h, SCAPE_ESTATE, "scape_refresh_mask: call scape_bind first");
   if (h->t < 1) return fail(h, SCAPE_ESTATE, "scape_refresh_mask: no step taken yet");
+  // every shard keeps all of its coordinates: the mask is all ones whatever m
+  // holds, and the one built already (bitmap, index list, rank table) stands
+  if (h->all_dense && h->mask_ready) return SCAPE_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int rc = (h->warm && !h->all_dense) ? refresh_warm(h, st) : refresh_cold(h, st);
   if (rc) {
@@ -1005,6 +1008,16 @@ int scape_step_host(scape_t* h, const void* const* host_grads_src, void* const* 
   e = cudaStreamWaitEvent(st, h->ev_done, 0);
   if (e != cudaSuccess) return cuda_fail(h, e, "scape_step_host: stream wait");
   return SCAPE_OK;
+}
+
+int scape_probe_random_access(scape_t* h, void* stream) {
+  if (!h) return SCAPE_EINVAL;
+  if (!h->bound || !h->mask_ready)
+    return fail(h, SCAPE_ESTATE, "scape_probe_random_access: needs a bound handle with a mask");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return run_kernel(h, kKProbeRmw, st, [&] {
+    return launch_probe_rmw(h->idx(), h->gbar(), h->k, h->w, h->m, st);
+  });
 }
 
 int scape_profile_enable(scape_t* h, int on) {

@@ -91,6 +91,7 @@ enum KernelId {
   kKParamPatch,
   kKDenseUpdate,
   kKXcMove,
+  kKProbeRmw,
   kNumKernels
 };
 static_assert(kNumKernels == SCAPE_NUM_KERNELS, "kernel table size");
@@ -242,6 +243,10 @@ cudaError_t launch_param_patch(const uint32_t* idx, int64_t k, const float* w, f
                                cudaStream_t st);
 cudaError_t launch_reduce(const float* pack, int64_t pack_stride, int W, int64_t k, float* gbar,
                           cudaStream_t st);
+// Timing probe: adams_sparse's memory accesses without its arithmetic (w and m
+// written back unchanged).
+cudaError_t launch_probe_rmw(const uint32_t* idx, const float* gbar, int64_t k, float* w,
+                             float* m, cudaStream_t st);
 // multi-rank exchange helpers (step_kernels.cu)
 cudaError_t launch_adams_dense(const float* gbar, int64_t n, float* w, float* m,
                                const AdamsConst& c, cudaStream_t st);

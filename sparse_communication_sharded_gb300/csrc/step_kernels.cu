@@ -418,6 +418,49 @@ adams_sparse_kernel(const uint32_t* __restrict__ idx, const float* __restrict__ 
   }
 }
 
+// ------------------------------------------------------------------ probe_rmw
+// A timing probe of the machine, not part of the method: the memory accesses
+// of adams_sparse with none of its arithmetic -- idx and g_bar read in
+// order, w[i] and m[i] read and written back unchanged at the k selected
+// coordinates -- so that its time is the floor the scattered update can
+// reach on this GPU.  The stores are inline PTX so that the compiler keeps
+// them; the values written are the values read (bit for bit).
+__device__ __forceinline__ void st_keep(float* p, float v) {
+  asm volatile("st.global.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
+__global__ void __launch_bounds__(256)
+probe_rmw_kernel(const uint32_t* __restrict__ idx, const float* __restrict__ gbar, int64_t k,
+                 float* __restrict__ wts, float* __restrict__ mom) {
+  const int64_t j0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (j0 >= k) return;
+  if (j0 + 4 <= k) {
+    // the same loads as adams_sparse: 16-byte idx and g_bar, then w and m
+    const uint4 iv = __ldg(reinterpret_cast<const uint4*>(idx + j0));
+    const float4 gv = __ldg(reinterpret_cast<const float4*>(gbar + j0));
+    const uint32_t ii[4] = {iv.x, iv.y, iv.z, iv.w};
+    float wv[4], mv[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      wv[q] = wts[ii[q]];
+      mv[q] = mom[ii[q]];
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      st_keep(wts + ii[q], wv[q]);
+      st_keep(mom + ii[q], mv[q]);
+    }
+    if (gv.x + gv.y + gv.z + gv.w == 1.0e30f) asm volatile("" ::: "memory");  // keep g_bar
+  } else {
+    for (int64_t j = j0; j < k; ++j) {
+      const uint32_t i = idx[j];
+      const float wv = wts[i], mv = mom[i];
+      st_keep(wts + i, wv);
+      st_keep(mom + i, mv);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ param_patch
 // dst[idx[j]] = w[idx[j]] for the k coordinates a step changed; dst is the
 // device address of the caller's page-locked host copy of the parameters,
@@ -562,6 +605,14 @@ cudaError_t launch_adams_sparse(const uint32_t* idx, const float* gbar, int64_t 
   const unsigned grid = (unsigned)(((k + 3) / 4 + 255) / 256);
   if (msync) adams_sparse_kernel<true><<<grid, 256, 0, st>>>(idx, gbar, k, w, m, c);
   else adams_sparse_kernel<false><<<grid, 256, 0, st>>>(idx, gbar, k, w, m, c);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_probe_rmw(const uint32_t* idx, const float* gbar, int64_t k, float* w,
+                             float* m, cudaStream_t st) {
+  if (k <= 0) return cudaSuccess;
+  const unsigned grid = (unsigned)(((k + 3) / 4 + 255) / 256);
+  probe_rmw_kernel<<<grid, 256, 0, st>>>(idx, gbar, k, w, m);
   return cudaGetLastError();
 }
 

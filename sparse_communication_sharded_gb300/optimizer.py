@@ -194,6 +194,11 @@ class Scape:
     def launch_count(self):
         return C.scape_launch_count(self.h)
 
+    def probe_random_access(self):
+        """Timing probe: the sparse update's memory accesses without its
+        arithmetic (w and m are left unchanged)."""
+        C.scape_probe_random_access(self.h, self._stream())
+
     def close(self):
         if getattr(self, "h", None) is not None:
             C.scape_destroy(self.h)

@@ -380,6 +380,29 @@ def test_step_without_refresh_reuses_the_older_mask(cuda_device, fusion):
     opt.close()
 
 
+def test_random_access_probe_changes_nothing(cuda_device):
+    """The timing probe reads and writes back w and m at the mask's
+    coordinates: both stay bit for bit what they were."""
+    P, W, s = 100003, 4, 0.99
+    wl = _wl(P, W, s, "bf16")
+    gen = synth.GradientStream(wl, seed=2, device=cuda_device)
+    params = synth.init_params(P, seed=2, device=cuda_device)
+    opt = make_opt(params, W, s, torch.bfloat16)
+    bufs = gen.alloc()
+    with pytest.raises(ScapeError):
+        opt.probe_random_access()          # no mask yet
+    for _ in range(3):
+        gen.next_into(bufs)
+        opt.step(bufs)
+        opt.refresh_mask()
+    w0, m0 = params.clone(), opt.m.clone()
+    opt.probe_random_access()
+    torch.cuda.synchronize()
+    assert torch.equal(params.view(torch.int32), w0.view(torch.int32))
+    assert torch.equal(opt.m.view(torch.int32), m0.view(torch.int32))
+    opt.close()
+
+
 def test_state_errors(cuda_device):
     P, W = 1000, 2
     params = torch.zeros(P, device=cuda_device)
