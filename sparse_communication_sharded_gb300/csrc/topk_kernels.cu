@@ -48,9 +48,10 @@ __device__ __forceinline__ uint64_t composite(uint32_t key, uint32_t i) {
 // b1 = 0.9 -- while the threshold, the k_s-th largest |m| and so the lower
 // tail of the selected group, moves by a fraction of that in either
 // direction (up to about 10 buckets on the Llama-500M-shaped workload in
-// steps 2 to 5, then by 0 or 1); the host passes the ratio in buckets
-// (32 per octave) as `growth` (0 when unknown; below 4, from about the eighth
-// step with b1 = 0.9, the window is not widened).  hi may be 8192 (no such
+// steps 2 to 4, then by 0 or 1, which the trend follows); the host passes the
+// ratio in buckets (32 per octave) as `growth` (0 when unknown).  Only the
+// refreshes after steps 2 to 4 (growth >= 11 buckets with b1 = 0.9) are
+// widened: a wide window stages many candidates where the mask is dense.  hi may be 8192 (no such
 // digit).  With no previous bucket the window is empty (lo > hi).
 constexpr int kMaxTrend = 16;
 constexpr int kMaxGrowth = 24;
@@ -71,7 +72,7 @@ __device__ __forceinline__ void bucket_window(const ShardSel& q, int growth, uin
     a = pred < a ? pred : a;
     b = pred > b ? pred : b;
   }
-  if (growth >= 4) {  // the warm-up (a few steps); afterwards the +-1 window holds
+  if (growth >= 11) {  // the first three warm refreshes; afterwards the trend suffices
     const int h = growth > kMaxGrowth ? kMaxGrowth : growth;
     a = (int)q.guess - h < a ? (int)q.guess - h : a;
     b = (int)q.guess + h > b ? (int)q.guess + h : b;
