@@ -852,14 +852,30 @@ def bench_sweep(args):
                         opt.refresh_mask()
                     torch.cuda.synchronize()
                     step_ms, _ = time_steps(opt, gen, grads, args.steps)
+                    # per-kernel split of two more steps
+                    opt.profile(True)
+                    opt.profile_reset()
+                    for _ in range(2):
+                        gen.next_into(grads)
+                        opt.step(grads)
+                        opt.refresh_mask()
+                    torch.cuda.synchronize()
+                    opt.profile_collect()
+                    prof = opt.profile_read()
                     opt.close()
                     del grads, params, opt, gen
                     ms = sorted(step_ms)[len(step_ms) // 2]
-                    alg = algorithmic_bytes(wl, k, fusion=args.fusion)["total"]
+                    ab = algorithmic_bytes(wl, k, fusion=args.fusion)
+                    alg = ab["total"]
+                    ef_ms = prof["ef_compact"][0] / max(prof["ef_compact"][1], 1)
                     pt.update({"ms_per_step": ms, "ms_each": step_ms,
                                "params_per_s": P / (ms / 1000.0),
                                "hbm_gbs": alg / (ms / 1000.0) / 1e9,
-                               "hbm_frac": alg / (ms / 1000.0) / 1e9 / peak})
+                               "hbm_frac": alg / (ms / 1000.0) / 1e9 / peak,
+                               "ef_compact_ms": ef_ms,
+                               "ef_compact_frac": ab["ef_compact"] / (ef_ms / 1000.0) / 1e9 / peak,
+                               "kernels_ms_per_step": {n: m / 2 for n, (m, c) in prof.items()
+                                                       if c}})
                     points.append(pt)
     torch.cuda.empty_cache()
     done = [p for p in points if "ms_per_step" in p]
