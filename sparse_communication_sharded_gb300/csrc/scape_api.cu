@@ -97,9 +97,16 @@ int enqueue_update(scape_t* h, const AdamsConst& c, cudaStream_t st) {
   }
   if (h->fusion != SCAPE_FUSE_UPDATE) {
     const bool msync = (h->variant & SCAPE_VARIANT_MOMENT_SYNC) != 0;
-    rc = run_kernel(h, kKAdamsSparse, st, [&] {
-      return launch_adams_sparse(h->idx(), h->gbar(), h->k, h->w, h->m, c, msync, st);
-    });
+    if (h->all_dense && !msync) {
+      // every coordinate kept: slot j is coordinate j, no index list to read
+      rc = run_kernel(h, kKDenseUpdate, st, [&] {
+        return launch_adams_dense(h->gbar(), h->P, h->w, h->m, c, st);
+      });
+    } else {
+      rc = run_kernel(h, kKAdamsSparse, st, [&] {
+        return launch_adams_sparse(h->idx(), h->gbar(), h->k, h->w, h->m, c, msync, st);
+      });
+    }
   }
   if (rc || !(h->variant & SCAPE_VARIANT_DENSE_OFFMASK)) return rc;
   return run_kernel(h, kKOffmask, st,

@@ -115,10 +115,39 @@ constexpr int kEfMinBlocks = 4;
 // Every selected value is also added to its slot's running sum (started at
 // -0.0, the identity of IEEE addition, so the sum equals the worker-ordered
 // sum that begins with worker 0's value).
+// `full`: all eight parameters selected and their slots 16-byte aligned (in
+// the packed row and in the running sums): the same values are then moved by
+// vector loads and stores (the case of masks that keep most coordinates).
 template <bool MSYNC, class G>
-__device__ __forceinline__ void ef_select8(G&& g, const float (&e)[8], uint32_t byte,
+__device__ __forceinline__ void ef_select8(G&& g, const float (&e)[8], uint32_t byte, bool full,
                                            float* __restrict__ prow, float (&out)[8],
                                            const MomentPack& mp, int64_t i0, float* ssum) {
+  if (full) {
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float a = __fadd_rn(g(j), e[j]);  // error-feedback add
+      v[j] = a;
+      if (MSYNC) v[j] = __fadd_rn(__fmul_rn(mp.beta1, mp.m[i0 + j]), __fmul_rn(mp.c1, a));
+      out[j] = __fsub_rn(a, a);  // residual: everything was sent
+    }
+    float4* p4 = reinterpret_cast<float4*>(prow);
+    p4[0] = make_float4(v[0], v[1], v[2], v[3]);
+    p4[1] = make_float4(v[4], v[5], v[6], v[7]);
+    float4* s4 = reinterpret_cast<float4*>(ssum);
+    float4 s0 = s4[0], s1 = s4[1];
+    s0.x = __fadd_rn(s0.x, v[0]);
+    s0.y = __fadd_rn(s0.y, v[1]);
+    s0.z = __fadd_rn(s0.z, v[2]);
+    s0.w = __fadd_rn(s0.w, v[3]);
+    s1.x = __fadd_rn(s1.x, v[4]);
+    s1.y = __fadd_rn(s1.y, v[5]);
+    s1.z = __fadd_rn(s1.z, v[6]);
+    s1.w = __fadd_rn(s1.w, v[7]);
+    s4[0] = s0;
+    s4[1] = s1;
+    return;
+  }
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const float a = __fadd_rn(g(j), e[j]);  // error-feedback add
@@ -155,7 +184,7 @@ ef_compact_kernel(const __grid_constant__ WorkerPtrs ptrs, int W, int64_t P,
                   const uint32_t* __restrict__ bits, const uint32_t* __restrict__ tile_base,
                   float* __restrict__ pack, int64_t pack_stride, MomentPack mp, EfFuse fz) {
   __shared__ uint32_t warp_tot[kTileThreads / 32];
-  __shared__ float tile_sum[kTile];
+  __shared__ __align__(16) float tile_sum[kTile];
   __shared__ float tile_w[kTile], tile_m[kTile];  // w, m at the selected slots (finishing launch)
   const int64_t tile = blockIdx.x;
   const int64_t i0 = tile * kTile + (int64_t)threadIdx.x * 8;
@@ -164,6 +193,11 @@ ef_compact_kernel(const __grid_constant__ WorkerPtrs ptrs, int W, int64_t P,
   uint32_t total;
   const uint32_t excl = block_exclusive_scan<kTileThreads>(__popc(byte), warp_tot, &total);
   const int64_t slot0 = (int64_t)__ldg(tile_base + tile) + excl;
+  // every parameter of this thread selected, slots 16-byte aligned: vector
+  // path (float32 gradients only: with bfloat16 ones two workers are in
+  // flight and the extra registers would spill)
+  const bool full =
+      sizeof(GT) == 4 && byte == 0xFFu && ((slot0 | (int64_t)excl) & 3) == 0;
   float* const pbase = pack + slot0;
   // this thread's selected slots: tile_sum[excl .. excl + popc(byte))
   float* const ssum = tile_sum + excl;
@@ -207,7 +241,7 @@ ef_compact_kernel(const __grid_constant__ WorkerPtrs ptrs, int W, int64_t P,
         if (w0 + u < W) {
           float out[8];
           const auto& gu = g[u];
-          ef_select8<MSYNC>([&](int j) { return GradIO<GT>::at(gu, j); }, e[u], byte,
+          ef_select8<MSYNC>([&](int j) { return GradIO<GT>::at(gu, j); }, e[u], byte, full,
                             pbase + (int64_t)(w0 + u) * pack_stride, out, mp, i0, ssum);
           store8_f32(ptrs.e[w0 + u] + i0, out);
         }
@@ -223,7 +257,8 @@ ef_compact_kernel(const __grid_constant__ WorkerPtrs ptrs, int W, int64_t P,
         g[j] = in ? GradIO<GT>::load1(ptrs.g[wk], i0 + j) : 0.f;
         e[j] = in ? __ldcs(ptrs.e[wk] + i0 + j) : 0.f;
       }
-      ef_select8<MSYNC>([&](int j) { return g[j]; }, e, byte, pbase + (int64_t)wk * pack_stride,
+      ef_select8<MSYNC>([&](int j) { return g[j]; }, e, byte, false,
+                        pbase + (int64_t)wk * pack_stride,
                         out, mp, i0, ssum);
 #pragma unroll
       for (int j = 0; j < 8; ++j)
