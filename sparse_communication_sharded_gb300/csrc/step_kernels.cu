@@ -188,6 +188,25 @@ ef_compact_kernel(const __grid_constant__ WorkerPtrs ptrs, int W, int64_t P,
   __shared__ float tile_w[kTile], tile_m[kTile];  // w, m at the selected slots (finishing launch)
   const int64_t tile = blockIdx.x;
   const int64_t i0 = tile * kTile + (int64_t)threadIdx.x * 8;
+  // full tile with aligned buffers: 16-byte loads and stores, the loads of a
+  // worker group issued before any of it is stored (float32 gradients: one
+  // worker in flight, two would spill at 64 registers)
+  constexpr int U = sizeof(GT) == 2 ? kWorkerUnroll : 1;
+  const bool vec_tile = VEC && (tile + 1) * kTile <= P;
+  typename GradIO<GT>::Raw g[U];
+  float e[U][8];
+  // the first group's values do not depend on the mask: their loads go out
+  // before the block's prologue (bitmap word, block scan, rank-table base),
+  // which then runs under them -- what keeps the few-worker case streaming
+  if (vec_tile) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (u < W) {
+        g[u] = GradIO<GT>::load_raw(ptrs.g[u], i0);
+        load8_f32(ptrs.e[u] + i0, e[u]);
+      }
+    }
+  }
   uint32_t byte = 0;
   if (i0 < P) byte = (__ldg(bits + (i0 >> 5)) >> (uint32_t)(i0 & 31)) & 0xFFu;
   uint32_t total;
@@ -221,19 +240,15 @@ ef_compact_kernel(const __grid_constant__ WorkerPtrs ptrs, int W, int64_t P,
   cp_async_commit();
   cp_async_wait<1>();  // the partial sums have landed
 
-  if (VEC && (tile + 1) * kTile <= P) {
-    // full tile: 16-byte loads and stores; the loads of a worker pair are
-    // issued before either pair member is stored
-    // float32 gradients: one worker in flight (two would spill at 64 registers)
-    constexpr int U = sizeof(GT) == 2 ? kWorkerUnroll : 1;
+  if (vec_tile) {
     for (int w0 = 0; w0 < W; w0 += U) {
-      typename GradIO<GT>::Raw g[U];
-      float e[U][8];
+      if (w0 > 0) {
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if (w0 + u < W) {
-          g[u] = GradIO<GT>::load_raw(ptrs.g[w0 + u], i0);
-          load8_f32(ptrs.e[w0 + u] + i0, e[u]);
+        for (int u = 0; u < U; ++u) {
+          if (w0 + u < W) {
+            g[u] = GradIO<GT>::load_raw(ptrs.g[w0 + u], i0);
+            load8_f32(ptrs.e[w0 + u] + i0, e[u]);
+          }
         }
       }
 #pragma unroll
