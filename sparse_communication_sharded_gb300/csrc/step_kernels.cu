@@ -123,29 +123,27 @@ __device__ __forceinline__ void ef_select8(G&& g, const float (&e)[8], uint32_t 
                                            float* __restrict__ prow, float (&out)[8],
                                            const MomentPack& mp, int64_t i0, float* ssum) {
   if (full) {
-    float v[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float a = __fadd_rn(g(j), e[j]);  // error-feedback add
-      v[j] = a;
-      if (MSYNC) v[j] = __fadd_rn(__fmul_rn(mp.beta1, mp.m[i0 + j]), __fmul_rn(mp.c1, a));
-      out[j] = __fsub_rn(a, a);  // residual: everything was sent
-    }
     float4* p4 = reinterpret_cast<float4*>(prow);
-    p4[0] = make_float4(v[0], v[1], v[2], v[3]);
-    p4[1] = make_float4(v[4], v[5], v[6], v[7]);
     float4* s4 = reinterpret_cast<float4*>(ssum);
-    float4 s0 = s4[0], s1 = s4[1];
-    s0.x = __fadd_rn(s0.x, v[0]);
-    s0.y = __fadd_rn(s0.y, v[1]);
-    s0.z = __fadd_rn(s0.z, v[2]);
-    s0.w = __fadd_rn(s0.w, v[3]);
-    s1.x = __fadd_rn(s1.x, v[4]);
-    s1.y = __fadd_rn(s1.y, v[5]);
-    s1.z = __fadd_rn(s1.z, v[6]);
-    s1.w = __fadd_rn(s1.w, v[7]);
-    s4[0] = s0;
-    s4[1] = s1;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {  // four values at a time: fewer live registers
+      float v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float a = __fadd_rn(g(4 * h + j), e[4 * h + j]);  // error-feedback add
+        v[j] = a;
+        if (MSYNC)
+          v[j] = __fadd_rn(__fmul_rn(mp.beta1, mp.m[i0 + 4 * h + j]), __fmul_rn(mp.c1, a));
+        out[4 * h + j] = __fsub_rn(a, a);  // residual: everything was sent
+      }
+      p4[h] = make_float4(v[0], v[1], v[2], v[3]);
+      float4 sv = s4[h];
+      sv.x = __fadd_rn(sv.x, v[0]);
+      sv.y = __fadd_rn(sv.y, v[1]);
+      sv.z = __fadd_rn(sv.z, v[2]);
+      sv.w = __fadd_rn(sv.w, v[3]);
+      s4[h] = sv;
+    }
     return;
   }
 #pragma unroll
@@ -195,10 +193,12 @@ ef_compact_kernel(const __grid_constant__ WorkerPtrs ptrs, int W, int64_t P,
   const bool vec_tile = VEC && (tile + 1) * kTile <= P;
   typename GradIO<GT>::Raw g[U];
   float e[U][8];
-  // the first group's values do not depend on the mask: their loads go out
-  // before the block's prologue (bitmap word, block scan, rank-table base),
-  // which then runs under them -- what keeps the few-worker case streaming
-  if (vec_tile) {
+  // with one or two workers a block has little else to wait for: the first
+  // group's values, which do not depend on the mask, are loaded before the
+  // block's prologue (bitmap word, block scan, rank-table base), which then
+  // runs under them (with more workers that only lengthens live ranges)
+  const bool hoist = vec_tile && W <= 2;
+  if (hoist) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       if (u < W) {
@@ -242,7 +242,7 @@ ef_compact_kernel(const __grid_constant__ WorkerPtrs ptrs, int W, int64_t P,
 
   if (vec_tile) {
     for (int w0 = 0; w0 < W; w0 += U) {
-      if (w0 > 0) {
+      if (w0 > 0 || !hoist) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           if (w0 + u < W) {
