@@ -291,6 +291,19 @@ int scape_union_workspace_bytes(const scape_t *h, int64_t capacity, size_t *byte
 int scape_union_step(scape_t *h, const void *const *host_grad_ptrs, void *workspace,
                      size_t ws_bytes, int64_t capacity, int64_t *host_k_union, void *stream);
 
+/*
+ * Whether the steady warm refresh is replayed as a CUDA graph (default on).
+ * Once the warm-up widening of the bucket windows is over, every warm
+ * scape_refresh_mask() enqueues the same launches with the same arguments;
+ * the first such call captures them (and the rebuild of the index list) into
+ * a graph on an internal stream and later calls launch that graph on
+ * `stream`, which saves the launch gaps of its ~20 small kernels.  Calls made
+ * while profiling brackets any refresh kernel, or while `stream` is being
+ * captured by the caller, enqueue the launches themselves.  scape_bind()
+ * drops the graph.
+ */
+int scape_set_graphs(scape_t *h, int on);
+
 /* Learning rate for subsequent steps (schedules).  lr must be finite. */
 int scape_set_lr(scape_t *h, float lr);
 

@@ -48,6 +48,7 @@ _PROTOS = {
     "scape_step": (_i32, [_vp, _vp, _vp]),
     "scape_refresh_mask": (_i32, [_vp, _vp]),
     "scape_set_lr": (_i32, [_vp, _f32]),
+    "scape_set_graphs": (_i32, [_vp, _i32]),
     "scape_set_variant": (_i32, [_vp, _i32]),
     "scape_set_fusion": (_i32, [_vp, _i32]),
     "scape_residual_staging_bytes": (_i32, [_vp, _i32, ctypes.POINTER(ctypes.c_size_t)]),
@@ -241,6 +242,10 @@ def scape_union_step(h, grad_ptrs, ws_ptr, ws_bytes, capacity, stream=0):
     _check(h, load().scape_union_step(h, ctypes.addressof(arr), ws_ptr, ws_bytes, int(capacity),
                                       ctypes.byref(ku), stream))
     return ku.value
+
+
+def scape_set_graphs(h, on):
+    _check(h, load().scape_set_graphs(h, 1 if on else 0))
 
 
 def scape_set_lr(h, lr):

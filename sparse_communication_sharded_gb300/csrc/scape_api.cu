@@ -321,6 +321,8 @@ int scape_create_range(scape_t** out, int n_layers, const int64_t* host_layer_nu
 
 void scape_destroy(scape_t* h) {
   if (!h) return;
+  drop_graph(h);
+  if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
   for (auto& r : h->pending) {
     cudaEventDestroy(r.a);
     cudaEventDestroy(r.b);
@@ -412,6 +414,7 @@ int scape_bind(scape_t* h, float* params, float* m, float* const* host_e_ptrs, v
   // no previous mask: every shard starts without a bucket guess
   e = cudaMemset(h->sel(), 0xFF, sizeof(ShardSel) * h->S);
   if (e != cudaSuccess) return cuda_fail(h, e, "scape_bind: select state reset");
+  drop_graph(h);  // its launches point into the previous workspace
   h->bound = true;
   h->t = 0;
   h->mask_ready = false;
@@ -514,22 +517,28 @@ int refresh_cold(scape_t* h, cudaStream_t st) {
   });
 }
 
+// Warm-up widening of the bucket windows for the refresh after step t: the
+// expected growth of the selected first moments since the previous refresh,
+// the ratio of the bias corrections (1 - b1^t) / (1 - b1^(t-1)) in first-digit
+// buckets (32 per octave), while it is at least kWidenFrom buckets -- the
+// refreshes after steps 2 to 4 with b1 = 0.9, whose thresholds move by up to
+// about 10 buckets either way -- and 0 afterwards (the trend then suffices).
+constexpr int kWidenFrom = 11;
+
+int warm_growth(const scape_t* h) {
+  if (h->t < 2 || !(h->beta1 > 0.f)) return 0;
+  const double b1 = h->beta1;
+  const double r = (1.0 - std::pow(b1, (double)h->t)) / (1.0 - std::pow(b1, (double)(h->t - 1)));
+  const int g = (int)std::lround(32.0 * std::log2(r));
+  return g >= kWidenFrom ? g : 0;
+}
+
 // Every later refresh: the bitmap is written speculatively from the previous
 // thresholds in the same read of m that stages the candidates; the new
 // thresholds only correct it.  Every launch is enqueued whatever the data
 // holds; the kernels for the rare cases (a shard whose threshold left its
 // bucket window) return at once when no shard needs them.
-int refresh_warm(scape_t* h, cudaStream_t st) {
-  // Expected growth of the selected first moments since the previous refresh
-  // (after step t - 1): the ratio of the bias corrections, (1 - b1^t) /
-  // (1 - b1^(t-1)), in first-digit buckets (32 per octave); the bucket
-  // windows also cover that much growth above the previous thresholds.
-  int growth = 0;
-  if (h->t >= 2 && h->beta1 > 0.f) {
-    const double b1 = h->beta1;
-    const double r = (1.0 - std::pow(b1, (double)h->t)) / (1.0 - std::pow(b1, (double)(h->t - 1)));
-    growth = (int)std::lround(32.0 * std::log2(r));
-  }
+int refresh_warm(scape_t* h, cudaStream_t st, int growth) {
   // the histogram rows need no clearing: every refresh leaves them zero (each
   // select pass clears the rows it read, and rows of shards no pass reads are
   // never written); the cold refresh after a bind clears them once
@@ -579,6 +588,39 @@ int refresh_warm(scape_t* h, cudaStream_t st) {
   });
 }
 
+// Capture the steady warm refresh (growth 0) and the rebuild of the rank
+// table and index list into a graph, on an internal stream; the captured
+// work does not run.  On any failure the handle stays eager.
+void capture_refresh(scape_t* h) {
+  cudaError_t e = cudaSuccess;
+  if (!h->cap_stream) e = cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    h->graph_failed = true;
+    return;
+  }
+  const int64_t n0 = h->launches;
+  cudaGraph_t graph = nullptr;
+  e = cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal);
+  int rc = SCAPE_ECUDA;
+  if (e == cudaSuccess) {
+    rc = refresh_warm(h, h->cap_stream, 0);
+    if (rc == SCAPE_OK) rc = rebuild_from_bits(h, h->cap_stream, true);
+    e = cudaStreamEndCapture(h->cap_stream, &graph);
+  }
+  h->graph_launches = h->launches - n0;
+  h->launches = n0;  // nothing ran yet
+  if (e == cudaSuccess && rc == SCAPE_OK && graph)
+    e = cudaGraphInstantiate(&h->refresh_exec, graph, 0);
+  if (graph) cudaGraphDestroy(graph);
+  if (e != cudaSuccess || rc != SCAPE_OK || !h->refresh_exec) {
+    (void)cudaGetLastError();
+    h->err.clear();
+    h->refresh_exec = nullptr;
+    h->graph_failed = true;
+  }
+}
+
 }  // namespace
 
 int scape_refresh_mask(scape_t* h, void* stream) {
@@ -589,7 +631,31 @@ int scape_refresh_mask(scape_t* h, void* stream) {
   // holds, and the one built already (bitmap, index list, rank table) stands
   if (h->all_dense && h->mask_ready) return SCAPE_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  int rc = (h->warm && !h->all_dense) ? refresh_warm(h, st) : refresh_cold(h, st);
+  const bool warm = h->warm && !h->all_dense;
+  const int growth = warm ? warm_growth(h) : 0;
+  // The steady warm refresh enqueues the same launches with the same
+  // arguments every time: replay it as one graph (unless profiling brackets
+  // its launches, or the caller is capturing its own stream).
+  constexpr uint32_t kRefreshKernels =
+      (1u << kKCandHist0) | (1u << kKCandSelect) | (1u << kKCandCollect) | (1u << kKCandHist) |
+      (1u << kKScan) | (1u << kKIndex) | (1u << kKSpecMark) | (1u << kKFixup) | (1u << kKRemark);
+  const bool bracketed = h->prof && (h->prof_mask & kRefreshKernels);
+  if (warm && growth == 0 && h->graphs && !h->graph_failed && !bracketed) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusNone) {
+      if (!h->refresh_exec) capture_refresh(h);
+      if (h->refresh_exec) {
+        const cudaError_t e = cudaGraphLaunch(h->refresh_exec, st);
+        if (e != cudaSuccess) return cuda_fail(h, e, "scape_refresh_mask: graph launch");
+        h->launches += h->graph_launches;
+        h->mask_ready = true;
+        return SCAPE_OK;
+      }
+    } else {
+      (void)cudaGetLastError();
+    }
+  }
+  int rc = warm ? refresh_warm(h, st, growth) : refresh_cold(h, st);
   if (rc) {
     h->warm = false;
     return rc;
@@ -598,6 +664,12 @@ int scape_refresh_mask(scape_t* h, void* stream) {
   if (rc) return rc;
   h->warm = true;
   h->mask_ready = true;
+  return SCAPE_OK;
+}
+
+int scape_set_graphs(scape_t* h, int on) {
+  if (!h) return SCAPE_EINVAL;
+  h->graphs = on != 0;
   return SCAPE_OK;
 }
 

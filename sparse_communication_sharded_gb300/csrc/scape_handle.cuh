@@ -87,6 +87,13 @@ struct scape {
   int stage_workers = 0;           // residual rows it holds
   int64_t stage_stride = 0;        // floats per row (P rounded up to 64)
   std::vector<cudaEvent_t> ev_in, ev_comp, ev_out;  // per worker group
+  // CUDA graph of the steady warm refresh (and the rebuild of its index list):
+  // captured once on an internal stream, replayed on the caller's stream
+  bool graphs = true;               // scape_set_graphs
+  bool graph_failed = false;        // capture or instantiation failed: eager from then on
+  cudaStream_t cap_stream = nullptr;
+  cudaGraphExec_t refresh_exec = nullptr;
+  int64_t graph_launches = 0;       // kernel launches one replay makes
   // profiling
   bool prof = false;
   uint32_t prof_mask = 0xFFFFFFFFu;  // kernels whose launches are bracketed by events
@@ -176,6 +183,12 @@ inline AdamsConst make_const(const scape_t* h, int64_t t) {
   c.eps = h->eps;
   c.wd = h->wd;
   return c;
+}
+
+// Free the captured refresh graph (its launches point into the bound workspace).
+inline void drop_graph(scape_t* h) {
+  if (h->refresh_exec) cudaGraphExecDestroy(h->refresh_exec);
+  h->refresh_exec = nullptr;
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -176,7 +176,7 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-template <typename GT, bool VEC, bool MSYNC>
+template <typename GT, bool VEC, bool MSYNC, bool HOIST>
 __global__ void __launch_bounds__(kTileThreads, kEfMinBlocks)
 ef_compact_kernel(const __grid_constant__ WorkerPtrs ptrs, int W, int64_t P,
                   const uint32_t* __restrict__ bits, const uint32_t* __restrict__ tile_base,
@@ -193,11 +193,12 @@ ef_compact_kernel(const __grid_constant__ WorkerPtrs ptrs, int W, int64_t P,
   const bool vec_tile = VEC && (tile + 1) * kTile <= P;
   typename GradIO<GT>::Raw g[U];
   float e[U][8];
-  // with one or two workers a block has little else to wait for: the first
-  // group's values, which do not depend on the mask, are loaded before the
-  // block's prologue (bitmap word, block scan, rank-table base), which then
-  // runs under them (with more workers that only lengthens live ranges)
-  const bool hoist = vec_tile && W <= 2;
+  // HOIST (one or two workers: a block has little else to wait for): the
+  // first group's values, which do not depend on the mask, are loaded before
+  // the block's prologue (bitmap word, block scan, rank-table base), which
+  // then runs under them.  With more workers the host picks the kernel
+  // without it: its longer live ranges cost registers there.
+  const bool hoist = HOIST && vec_tile;
   if (hoist) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -589,11 +590,14 @@ void compact_kind(const WorkerPtrs& p, int W, int64_t P, bool vec, const uint32_
                   const uint32_t* tile_base, float* pack, int64_t pack_stride,
                   const MomentPack& mp, const EfFuse& fz, cudaStream_t st) {
   const unsigned grid = (unsigned)((P + kTile - 1) / kTile);
-  if (vec)
-    ef_compact_kernel<GT, true, MSYNC>
+  if (vec && W <= 2)
+    ef_compact_kernel<GT, true, MSYNC, true>
+        <<<grid, kTileThreads, 0, st>>>(p, W, P, bits, tile_base, pack, pack_stride, mp, fz);
+  else if (vec)
+    ef_compact_kernel<GT, true, MSYNC, false>
         <<<grid, kTileThreads, 0, st>>>(p, W, P, bits, tile_base, pack, pack_stride, mp, fz);
   else
-    ef_compact_kernel<GT, false, MSYNC>
+    ef_compact_kernel<GT, false, MSYNC, false>
         <<<grid, kTileThreads, 0, st>>>(p, W, P, bits, tile_base, pack, pack_stride, mp, fz);
 }
 

@@ -49,9 +49,8 @@ __device__ __forceinline__ uint64_t composite(uint32_t key, uint32_t i) {
 // tail of the selected group, moves by a fraction of that in either
 // direction (up to about 10 buckets on the Llama-500M-shaped workload in
 // steps 2 to 4, then by 0 or 1, which the trend follows); the host passes the
-// ratio in buckets (32 per octave) as `growth` (0 when unknown).  Only the
-// refreshes after steps 2 to 4 (growth >= 11 buckets with b1 = 0.9) are
-// widened: a wide window stages many candidates where the mask is dense.  hi may be 8192 (no such
+// ratio in buckets (32 per octave) as `growth` for the refreshes that need it
+// (0 otherwise: a wide window stages many candidates where the mask is dense).  hi may be 8192 (no such
 // digit).  With no previous bucket the window is empty (lo > hi).
 constexpr int kMaxTrend = 16;
 constexpr int kMaxGrowth = 24;
@@ -72,7 +71,7 @@ __device__ __forceinline__ void bucket_window(const ShardSel& q, int growth, uin
     a = pred < a ? pred : a;
     b = pred > b ? pred : b;
   }
-  if (growth >= 11) {  // the first three warm refreshes; afterwards the trend suffices
+  if (growth > 0) {
     const int h = growth > kMaxGrowth ? kMaxGrowth : growth;
     a = (int)q.guess - h < a ? (int)q.guess - h : a;
     b = (int)q.guess + h > b ? (int)q.guess + h : b;

@@ -144,6 +144,10 @@ class Scape:
     def set_lr(self, lr):
         C.scape_set_lr(self.h, lr)
 
+    def set_graphs(self, on):
+        """Replay the steady warm mask refresh as a CUDA graph (default on)."""
+        C.scape_set_graphs(self.h, on)
+
     # ----------------------------------------------------------- state views
     def _view(self, ptr, n, dtype):
         off = ptr - self.workspace.data_ptr()

@@ -85,7 +85,8 @@ def local_words(g: np.ndarray, lo: int, hi: int) -> np.ndarray:
 
 
 def run_full_trajectory(wl: synth.Workload, device, steps: int, seed: int = 0,
-                        grad_offset_elems: int = 0, variant: int = 0, fusion=None):
+                        grad_offset_elems: int = 0, variant: int = 0, fusion=None,
+                        graphs=None):
     """Whole problem on both sides (small sizes): compare every step."""
     P, W, s = wl.P, wl.W, wl.sparsity
     gdt = torch.bfloat16 if wl.grad_dtype == "bf16" else torch.float32
@@ -97,6 +98,8 @@ def run_full_trajectory(wl: synth.Workload, device, steps: int, seed: int = 0,
         opt.set_variant(variant)
     if fusion is not None:
         opt.set_fusion(fusion)
+    if graphs is not None:
+        opt.set_graphs(graphs)
     st = O.new_state(w0.numpy(), W, s, HP)
     rep = Report(f"{wl.name} W={W} s={s} x {steps} steps")
     # optional misaligned gradient buffers (scalar path)

@@ -62,6 +62,15 @@ def test_trajectory_every_fusion_level(cuda_device, fusion, P, W, s, dtype, quan
     assert rep.exact
 
 
+@pytest.mark.parametrize("P,W,s,dtype,quant", [TRAJ[2], TRAJ[5], TRAJ[6], TRAJ[9]])
+def test_trajectory_refresh_graph_off(cuda_device, P, W, s, dtype, quant):
+    """Every refresh enqueued launch by launch (the steady warm refresh is
+    otherwise replayed from a captured graph): the same oracle bits."""
+    rep = run_full_trajectory(_wl(P, W, s, dtype, quant=quant), cuda_device, steps=10,
+                              graphs=False)
+    assert rep.exact
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_unaligned_gradients_scalar_path(cuda_device, dtype):
     rep = run_full_trajectory(_wl(30001, 4, 0.9, dtype), cuda_device, steps=5, grad_offset_elems=1)
