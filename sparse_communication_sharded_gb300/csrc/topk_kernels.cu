@@ -254,11 +254,12 @@ mpass_kernel(const float* __restrict__ m, int64_t P, ShardMap sm,
 // run of 2048-parameter tiles; each shard piece of the run is split into its
 // whole tiles and at most two partial pieces.
 //  * Whole tiles get their bitmap words and popcount from the previous
-//    threshold.  Lane l of warp w holds parameters 1024h + 128w + 32q + l of
-//    the tile (h = 0..1, q = 0..3; coalesced 4-byte loads at fixed offsets
-//    from one pointer), so the ballot of "selected" for (h, q) is bitmap word
-//    32h + 4w + q and lane 0 stores a warp's four words with one 16-byte store.
-//    The next tile's values are loaded while the current one is processed.
+//    threshold.  Each warp takes whole tiles on its own, in eight chunks of
+//    256: lane l holds parameters 256c + 32q + l of chunk c (q = 0..7;
+//    coalesced 4-byte loads at fixed offsets from one pointer), so the ballot
+//    of "selected" for (c, q) is bitmap word 8c + q and lane 0 stores a
+//    chunk's eight words with two 16-byte stores.  The next chunk's values
+//    are loaded while the current one is processed.
 //  * Candidates whose bucket is within one of `guess` are staged per lane:
 //    lane l appends to its own column of the warp's shared-memory buffer
 //    (slot j at j * 32 + l), one predicated store per hit, with no warp-wide
@@ -272,7 +273,8 @@ mpass_kernel(const float* __restrict__ m, int64_t P, ShardMap sm,
 // Partial pieces (shard boundaries inside a tile, the ragged end) are only
 // staged and counted; the remark kernel writes their bits.
 constexpr int kSpecBlocksPerSm = 4;
-constexpr int kLaneSlots = 16;  // staged candidates per lane
+constexpr int kSpecBufChunks = 1;  // 256-parameter chunks per register set (two sets)
+constexpr int kLaneSlots = 16;     // staged candidates per lane
 
 __global__ void __launch_bounds__(256, kSpecBlocksPerSm)
 spec_kernel(const float* __restrict__ m, int64_t P, ShardMap sm,
@@ -363,66 +365,87 @@ spec_kernel(const float* __restrict__ m, int64_t P, ShardMap sm,
         if (__any_sync(0xffffffffu, sa > sa_tile)) flush_lanes(s);  // a tile adds <= 8
         const uint32_t t_is = istar / kMSeg;  // the tile holding istar
         const int lim = (int)(istar - t_is * kMSeg);
-        const float* p = m + (size_t)ta * kMSeg + 128 * warp + lane;
-        uint32_t* bw = bits + (size_t)ta * (kMSeg / 32) + 4 * warp;
-        // one whole tile t whose values x this warp holds
-        auto tile = [&](uint32_t t, const float (&x)[8]) {
-          // selected: key > kstar, or key == kstar and i <= istar
-          const uint32_t thr = kstar + (t > t_is ? 1u : 0u);
-          const bool mixed = t == t_is;
-          const uint32_t ibase = t * kMSeg + 128 * warp + lane;
-          uint32_t tc = 0;
+        // chunk c (parameters 256c .. 256c + 255) of tile t, whose values x
+        // this warp holds (lane l: parameter 256c + 32q + l in x[q]); tc counts
+        // this lane's selected parameters of the tile
+        auto chunk = [&](uint32_t t, int c, const float (&x)[8 * kSpecBufChunks], int x0,
+                         uint32_t& tc) {
+          const uint32_t ibase = t * kMSeg + 256 * c + lane;
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
+          for (int h = 0; h < 2; ++h) {  // words 8c + 4h .. 8c + 4h + 3
             uint32_t wd[4];
-            if (!mixed) {
+            if (t != t_is) {
+              // selected: key >= kstar before istar's tile, key > kstar after it
+              const uint32_t thr = kstar + (t > t_is ? 1u : 0u);
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
-                const uint32_t key = magnitude_key(x[4 * h + q]);
-                wd[q] = __ballot_sync(0xffffffffu, key >= thr);
-                if (key - wkey_lo < wkey_n) put(key, ibase + 1024 * h + 32 * q);
+                const uint32_t key = magnitude_key(x[x0 + 4 * h + q]);
+                const bool on = key >= thr;
+                wd[q] = __ballot_sync(0xffffffffu, on);
+                tc += on ? 1u : 0u;
+                if (key - wkey_lo < wkey_n) put(key, ibase + 32 * (4 * h + q));
               }
             } else {
+              // key > kstar, or key == kstar and i <= istar
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
-                const uint32_t key = magnitude_key(x[4 * h + q]);
-                wd[q] = __ballot_sync(
-                    0xffffffffu,
-                    key >= kstar + (uint32_t)(1024 * h + 128 * warp + 32 * q + lane > lim));
-                if (key - wkey_lo < wkey_n) put(key, ibase + 1024 * h + 32 * q);
+                const uint32_t key = magnitude_key(x[x0 + 4 * h + q]);
+                const bool on =
+                    key >= kstar + (uint32_t)(256 * c + 32 * (4 * h + q) + lane > lim);
+                wd[q] = __ballot_sync(0xffffffffu, on);
+                tc += on ? 1u : 0u;
+                if (key - wkey_lo < wkey_n) put(key, ibase + 32 * (4 * h + q));
               }
             }
-            if (lane == 0) {
-              *reinterpret_cast<uint4*>(bw + 32 * h) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-              tc += __popc(wd[0]) + __popc(wd[1]) + __popc(wd[2]) + __popc(wd[3]);
+            if (lane == 0)
+              *reinterpret_cast<uint4*>(bits + (size_t)t * (kMSeg / 32) + 8 * c + 4 * h) =
+                  make_uint4(wd[0], wd[1], wd[2], wd[3]);
+          }
+          if (__any_sync(0xffffffffu, sa > sa_tile)) flush_lanes(s);  // a chunk adds <= 8
+        };
+        // Warp w takes the whole tiles ta + w, ta + w + 8, ... on its own, so
+        // the per-tile work (threshold choice, count, its store) is done once
+        // per 2048 parameters.  Values load kSpecBufChunks chunks at a time
+        // into one of two register sets while the other set's chunks are
+        // marked (at a tile's end: the warp's next tile's first chunks).
+        constexpr int D = kSpecBufChunks;
+        uint32_t t = ta + (uint32_t)warp;
+        if (t < tb) {
+          const float* p = m + (size_t)t * kMSeg + lane;
+          float xa[8 * D], xb[8 * D];
+#pragma unroll
+          for (int q = 0; q < 8 * D; ++q) xa[q] = __ldcs(p + 32 * q);
+          uint32_t tc = 0;
+          int c = 0;  // xa holds chunks c .. c + D - 1 of tile t
+#pragma unroll 1
+          for (;;) {
+#pragma unroll
+            for (int q = 0; q < 8 * D; ++q) xb[q] = __ldcs(p + 256 * (c + D) + 32 * q);
+#pragma unroll
+            for (int d = 0; d < D; ++d) chunk(t, c + d, xa, 8 * d, tc);
+            if (c + 2 * D < 8) {
+#pragma unroll
+              for (int q = 0; q < 8 * D; ++q) xa[q] = __ldcs(p + 256 * (c + 2 * D) + 32 * q);
+            } else if (t + 8 < tb) {
+#pragma unroll
+              for (int q = 0; q < 8 * D; ++q) xa[q] = __ldcs(p + 8 * kMSeg + 32 * q);
+            }
+#pragma unroll
+            for (int d = 0; d < D; ++d) chunk(t, c + D + d, xb, 8 * d, tc);
+            c += 2 * D;
+            if (c == 8) {
+              const uint32_t n = __reduce_add_sync(0xffffffffu, tc);
+              if (lane == 0) {
+                tile_cnt[t] = n;  // the tile is this warp's alone
+                acount += n;
+              }
+              if (t + 8 >= tb) break;
+              t += 8;
+              p += 8 * kMSeg;
+              tc = 0;
+              c = 0;
             }
           }
-          if (lane == 0 && tc) {
-            atomicAdd(tile_cnt + t, tc);
-            acount += tc;
-          }
-          if (__any_sync(0xffffffffu, sa > sa_tile)) flush_lanes(s);
-          bw += kMSeg / 32;
-        };
-        // two tiles per round, so that the next tile's values load into the
-        // other register set while one is marked (no copies between them)
-        float xa[8], xb[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) xa[j] = __ldcs(p + 1024 * (j >> 2) + 32 * (j & 3));
-        for (uint32_t t = ta; t < tb; t += 2) {
-          if (t + 1 < tb) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) xb[j] = __ldcs(p + kMSeg + 1024 * (j >> 2) + 32 * (j & 3));
-          }
-          tile(t, xa);
-          if (t + 1 >= tb) break;
-          if (t + 2 < tb) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              xa[j] = __ldcs(p + 2 * kMSeg + 1024 * (j >> 2) + 32 * (j & 3));
-          }
-          tile(t + 1, xb);
-          p += 2 * kMSeg;
         }
         piece(tb * kMSeg, end);
       }
@@ -730,6 +753,7 @@ cudaError_t launch_spec(const float* m, int64_t P, const ShardMap& sm, const int
                                     tile_cnt, spb, growth);
   return cudaGetLastError();
 }
+
 
 cudaError_t launch_collect(const float* m, int64_t P, const ShardMap& sm, const int64_t* shard_start,
                            const ShardSel* sel, uint2* cand, uint32_t* cand_cnt, cudaStream_t st) {
