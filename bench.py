@@ -61,6 +61,15 @@ def mask_churn(prev_bits, bits, k):
 
 
 FUSION = {"none": 0, "sum": 1, "update": 2}  # scape_set_fusion levels
+FUSION_NAME = {v: k for k, v in FUSION.items()}
+
+
+def apply_fusion(opt, choice):
+    """Set the fusion level ("auto": keep the library's default for the
+    handle's density) and return the name of the level in force."""
+    if choice != "auto":
+        opt.set_fusion(FUSION[choice])
+    return FUSION_NAME[opt.fusion()]
 
 
 def algorithmic_bytes(wl, k, fusion="sum", P=None):
@@ -453,7 +462,7 @@ def bench_other_workload(name, args, dev, peak):
     params = synth.init_params(wl.P, seed=0, device=dev)
     opt = pkg.Scape(params, wl.W, wl.sparsity, layer_numel=[n for _, n in wl.layers],
                     grad_dtype=gdt)
-    opt.set_fusion(FUSION[args.fusion])
+    fusion = apply_fusion(opt, args.fusion)
     gen = synth.GradientStream(wl, seed=0, device=dev)
     grads = gen.alloc()
     for _ in range(args.warmup):
@@ -483,11 +492,11 @@ def bench_other_workload(name, args, dev, peak):
     del grads, params, opt
     torch.cuda.empty_cache()
     ms = sum(step_ms) / len(step_ms)
-    alg = algorithmic_bytes(wl, k, fusion=args.fusion)
+    alg = algorithmic_bytes(wl, k, fusion=fusion)
     ef_avg = ef_ms / max(ef_n, 1)
     step_kernels = ("dense_step", "ef_compact", "reduce", "adams_sparse")
     return {"P": wl.P, "W": wl.W, "sparsity": wl.sparsity, "k": k, "grad_dtype": wl.grad_dtype,
-            "steps": args.other_steps, "warmup": args.warmup, "ms_per_step": ms,
+            "fusion": fusion, "steps": args.other_steps, "warmup": args.warmup, "ms_per_step": ms,
             "ms_each": step_ms, "params_per_s": wl.P / (ms / 1000.0),
             "hbm_gbs": alg["total"] / (ms / 1000.0) / 1e9,
             "hbm_frac": alg["total"] / (ms / 1000.0) / 1e9 / peak,
@@ -530,7 +539,7 @@ def bench_gpu(args, wl):
     opt = pkg.Scape(params, W, wl.sparsity, layer_numel=[n for _, n in wl.layers],
                     grad_dtype=gdt, residuals=args.residuals, staging_rows=args.staging_rows,
                     shard_range=(shards.start, shards.stop) if ws > 1 else None)
-    opt.set_fusion(FUSION[args.fusion])
+    fusion = apply_fusion(opt, args.fusion)
     # the slices [lo, hi) of the W workers' gradients
     gen = synth.GradientStream(wl, seed=seed, device=dev, P=hi - lo, offset=lo)
     grads = gen.alloc()
@@ -589,7 +598,7 @@ def bench_gpu(args, wl):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         t_max = float(tt.item())
     value = multirank.strong_scaling_value(P, t_max / 1000.0)
-    alg = algorithmic_bytes(wl, opt.k, fusion=args.fusion, P=hi - lo)
+    alg = algorithmic_bytes(wl, opt.k, fusion=fusion, P=hi - lo)
     alg_total = multirank.sum_over_ranks(alg["total"], device=dev)
     peak, peak_kind = _peaks()
 
@@ -672,6 +681,7 @@ def bench_gpu(args, wl):
             "hbm_gbs": alg_total / (t_max / 1000.0) / 1e9,
             "hbm_frac": alg_total / (t_max / 1000.0) / 1e9 / (peak * ws),
             "alg_bytes_per_step": alg_total,
+            "fusion_level": fusion,
             "rank0_shards": [shards.start, shards.stop],
             "roofline": {"kernel": "ef_compact", "bound": "hbm", "achieved": ef_gbs,
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
@@ -843,7 +853,7 @@ def bench_sweep(args):
                         continue
                     params = synth.init_params(P, seed=0, device=dev)
                     opt = pkg.Scape(params, W, sp, grad_dtype=torch.float32)
-                    opt.set_fusion(FUSION[args.fusion])
+                    fusion = apply_fusion(opt, args.fusion)
                     gen = synth.GradientStream(wl, seed=0, device=dev)
                     grads = gen.alloc()
                     for _ in range(args.warmup):
@@ -865,7 +875,8 @@ def bench_sweep(args):
                     opt.close()
                     del grads, params, opt, gen
                     ms = sorted(step_ms)[len(step_ms) // 2]
-                    ab = algorithmic_bytes(wl, k, fusion=args.fusion)
+                    ab = algorithmic_bytes(wl, k, fusion=fusion)
+                    pt["fusion"] = fusion
                     alg = ab["total"]
                     ef_ms = prof["ef_compact"][0] / max(prof["ef_compact"][1], 1)
                     pt.update({"ms_per_step": ms, "ms_each": step_ms,
@@ -1020,9 +1031,10 @@ def main(argv=None):
     ap.add_argument("--staging-rows", type=int, default=None,
                     help="with --residuals host: device rows staging the residuals "
                          "(default min(W, 12); 0 = kernels access host memory in place)")
-    ap.add_argument("--fusion", default="sum", choices=sorted(FUSION),
+    ap.add_argument("--fusion", default="auto", choices=sorted(FUSION) + ["auto"],
                     help="what the compaction pass also does: none (separate reduce and "
-                         "adams_sparse), sum (writes g_bar), update (also AdamS)")
+                         "adams_sparse), sum (writes g_bar), update (also AdamS); auto: the "
+                         "library's default for the density (update from 5%% selected)")
     ap.add_argument("--baselines", type=int, default=1,
                     help="also time the dense AdamS and AdamW baselines (0 to skip)")
     ap.add_argument("--exchange", action="store_true",

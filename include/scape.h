@@ -224,16 +224,21 @@ int scape_set_variant(scape_t *h, int flags);
  *   SCAPE_FUSE_NONE    the ordered sum of the W packed buffers and the
  *       unpack + AdamS run as two separate launches after it, the layout of
  *       "Sintesi Tecnica: SCAPE" Sec. 2;
- *   SCAPE_FUSE_SUM     (default) the compaction also writes g_bar
- *       (worker-ordered sum / W); the unpack + AdamS runs as its own launch;
+ *   SCAPE_FUSE_SUM     the compaction also writes g_bar (worker-ordered
+ *       sum / W); the unpack + AdamS runs as its own launch;
  *   SCAPE_FUSE_UPDATE  the compaction also applies AdamS at the selected
- *       coordinates (no further launch; its scattered w and m accesses then
- *       interleave with the residual stream, which measured slower).
+ *       coordinates (no further launch; its w and m accesses interleave with
+ *       the residual stream).
+ * Default, set by scape_create / scape_create_range from the handle's own
+ * k and P: SCAPE_FUSE_UPDATE when at least 5% of the coordinates are
+ * selected (20 k >= P) and not all of them, SCAPE_FUSE_SUM otherwise.
  * The packed buffers and g_bar are written at every level.
- * Errors: SCAPE_EINVAL for an unknown level.
+ * scape_get_fusion writes the current level to *level.
+ * Errors: SCAPE_EINVAL for an unknown level or a NULL pointer.
  */
 enum scape_fusion { SCAPE_FUSE_NONE = 0, SCAPE_FUSE_SUM = 1, SCAPE_FUSE_UPDATE = 2 };
 int scape_set_fusion(scape_t *h, int level);
+int scape_get_fusion(const scape_t *h, int *level);
 
 /*
  * Device staging for residuals bound in host memory (the pages keep the

@@ -51,6 +51,7 @@ _PROTOS = {
     "scape_set_graphs": (_i32, [_vp, _i32]),
     "scape_set_variant": (_i32, [_vp, _i32]),
     "scape_set_fusion": (_i32, [_vp, _i32]),
+    "scape_get_fusion": (_i32, [_vp, _vp]),
     "scape_residual_staging_bytes": (_i32, [_vp, _i32, ctypes.POINTER(ctypes.c_size_t)]),
     "scape_set_residual_staging": (_i32, [_vp, _vp, ctypes.c_size_t]),
     "scape_dense_adams_step": (_i32, [_vp, _vp, _vp]),
@@ -208,6 +209,12 @@ FUSE_NONE, FUSE_SUM, FUSE_UPDATE = 0, 1, 2
 
 def scape_set_fusion(h, level):
     _check(h, load().scape_set_fusion(h, int(level)))
+
+
+def scape_get_fusion(h):
+    level = ctypes.c_int(0)
+    _check(h, load().scape_get_fusion(h, ctypes.byref(level)))
+    return level.value
 
 
 def scape_residual_staging_bytes(h, rows):

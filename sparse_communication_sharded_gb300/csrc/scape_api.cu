@@ -266,6 +266,11 @@ int create_handle(scape_t** out, int n_layers, const int64_t* host_layer_numel, 
     nmax = n > nmax ? n : nmax;
     if (h->shard_k[s] != n) h->all_dense = false;
   }
+  // Default fusion level by density: from 5% of coordinates selected the
+  // update inside the compaction pass (its w and m accesses cover much of each
+  // tile's sectors) beats a separate scattered launch; below that, and when
+  // every coordinate is kept (coalesced dense update), the separate launch.
+  h->fusion = (!h->all_dense && h->k * 20 >= h->P) ? SCAPE_FUSE_UPDATE : SCAPE_FUSE_SUM;
   P = h->P;  // from here on: the parameters this handle covers
   h->ntiles = (P + kTile - 1) / kTile;
   h->nwords = (P + 31) / 32;
@@ -697,6 +702,12 @@ int scape_set_residual_staging(scape_t* h, void* device_buffer, size_t bytes) {
 int scape_residual_staging_bytes(const scape_t* h, int rows, size_t* bytes) {
   if (!h || !bytes || rows < 3) return SCAPE_EINVAL;
   *bytes = (size_t)rows * (size_t)((h->P + 63) / 64 * 64) * 4;
+  return SCAPE_OK;
+}
+
+int scape_get_fusion(const scape_t* h, int* level) {
+  if (!h || !level) return SCAPE_EINVAL;
+  *level = h->fusion;
   return SCAPE_OK;
 }
 

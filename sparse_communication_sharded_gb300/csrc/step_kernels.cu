@@ -6,8 +6,8 @@
 //                ("SCAPE" Sec. II-B: sent = TopK(g + e) through the mask,
 //                e <- g + e - sent), one pass over every worker's g and e.
 //                It can also form the ordered sum of the packed values
-//                (g_bar; the default) and apply AdamS at the selected
-//                coordinates (EfFuse flags).
+//                (g_bar; done by default) and apply AdamS at the selected
+//                coordinates (EfFuse flags; by default from 5% density).
 //   reduce       ordered sum of the W packed buffers / W: the single
 //                synchronised sparse buffer ("Sintesi Tecnica: SCAPE" Sec. 2)
 //                (separate-launch form, and the union-mask baseline).

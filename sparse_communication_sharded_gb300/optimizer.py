@@ -115,8 +115,13 @@ class Scape:
     def set_fusion(self, level):
         """How much of the step the compaction pass does: C.FUSE_NONE (separate
         reduce and adams_sparse launches), C.FUSE_SUM (it writes g_bar) or
-        C.FUSE_UPDATE (it also applies AdamS); results are bit-identical."""
+        C.FUSE_UPDATE (it also applies AdamS); results are bit-identical.  The
+        default depends on the density (C.FUSE_UPDATE from 5% selected)."""
         C.scape_set_fusion(self.h, level)
+
+    def fusion(self):
+        """The current fusion level."""
+        return C.scape_get_fusion(self.h)
 
     def dense_adams_step(self, grads):
         """Dense AdamS baseline on the mean gradient (no error feedback, no mask)."""
