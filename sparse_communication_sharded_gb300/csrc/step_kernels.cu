@@ -435,36 +435,38 @@ __device__ __forceinline__ void sparse_update(float b, float& w, float& m, const
   else adams_update(b, w, m, c);
 }
 
+// Slots of a 256-thread block: 1024 consecutive ones; thread t takes slots
+// t, t + 256, t + 512, t + 768 of them, so that each load instruction of a
+// warp covers 32 consecutive slots (neighbouring coordinates).  Measured
+// against thread t taking slots 4t .. 4t + 3 by 16-byte loads of idx and
+// g_bar: 0.49 against 0.55 ms on the Llama-500M shape (its probe 0.51
+// against 0.57 ms), 1.17 against 1.30 ms on Llama-1.8B.
 template <bool MSYNC>
 __global__ void __launch_bounds__(256)
 adams_sparse_kernel(const uint32_t* __restrict__ idx, const float* __restrict__ gbar, int64_t k,
                     float* __restrict__ wts, float* __restrict__ mom, AdamsConst c) {
-  const int64_t j0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
-  if (j0 >= k) return;
-  if (j0 + 4 <= k) {
-    const uint4 iv = __ldg(reinterpret_cast<const uint4*>(idx + j0));
-    const float4 gv = __ldg(reinterpret_cast<const float4*>(gbar + j0));
-    const uint32_t ii[4] = {iv.x, iv.y, iv.z, iv.w};
-    const float gg[4] = {gv.x, gv.y, gv.z, gv.w};
-    float wv[4], mv[4];
+  const int64_t j0 = (int64_t)blockIdx.x * 1024 + threadIdx.x;
+  uint32_t ii[4];
+  float gg[4], wv[4], mv[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < 4; ++q) {
+    const int64_t j = j0 + 256 * q;
+    ii[q] = j < k ? __ldg(idx + j) : 0u;
+    gg[q] = j < k ? __ldg(gbar + j) : 0.f;
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (j0 + 256 * q < k) {
       wv[q] = wts[ii[q]];
       mv[q] = mom[ii[q]];
     }
+  }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < 4; ++q) {
+    if (j0 + 256 * q < k) {
       sparse_update<MSYNC>(gg[q], wv[q], mv[q], c);
       wts[ii[q]] = wv[q];
       mom[ii[q]] = mv[q];
-    }
-  } else {
-    for (int64_t j = j0; j < k; ++j) {
-      const uint32_t i = idx[j];
-      float wv = wts[i], mv = mom[i];
-      sparse_update<MSYNC>(gbar[j], wv, mv, c);
-      wts[i] = wv;
-      mom[i] = mv;
     }
   }
 }
@@ -483,31 +485,29 @@ __device__ __forceinline__ void st_keep(float* p, float v) {
 __global__ void __launch_bounds__(256)
 probe_rmw_kernel(const uint32_t* __restrict__ idx, const float* __restrict__ gbar, int64_t k,
                  float* __restrict__ wts, float* __restrict__ mom) {
-  const int64_t j0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
-  if (j0 >= k) return;
-  if (j0 + 4 <= k) {
-    // the same loads as adams_sparse: 16-byte idx and g_bar, then w and m
-    const uint4 iv = __ldg(reinterpret_cast<const uint4*>(idx + j0));
-    const float4 gv = __ldg(reinterpret_cast<const float4*>(gbar + j0));
-    const uint32_t ii[4] = {iv.x, iv.y, iv.z, iv.w};
-    float wv[4], mv[4];
+  // the same slots per thread and the same loads as adams_sparse
+  const int64_t j0 = (int64_t)blockIdx.x * 1024 + threadIdx.x;
+  uint32_t ii[4];
+  float wv[4], mv[4], gsum = 0.f;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < 4; ++q) {
+    const int64_t j = j0 + 256 * q;
+    ii[q] = j < k ? __ldg(idx + j) : 0u;
+    gsum += j < k ? __ldg(gbar + j) : 0.f;
+  }
+  if (gsum == 1.0e30f) asm volatile("" ::: "memory");  // keep g_bar's loads
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (j0 + 256 * q < k) {
       wv[q] = wts[ii[q]];
       mv[q] = mom[ii[q]];
     }
+  }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < 4; ++q) {
+    if (j0 + 256 * q < k) {
       st_keep(wts + ii[q], wv[q]);
       st_keep(mom + ii[q], mv[q]);
-    }
-    if (gv.x + gv.y + gv.z + gv.w == 1.0e30f) asm volatile("" ::: "memory");  // keep g_bar
-  } else {
-    for (int64_t j = j0; j < k; ++j) {
-      const uint32_t i = idx[j];
-      const float wv = wts[i], mv = mom[i];
-      st_keep(wts + i, wv);
-      st_keep(mom + i, mv);
     }
   }
 }
@@ -656,7 +656,7 @@ cudaError_t launch_reduce(const float* pack, int64_t pack_stride, int W, int64_t
 cudaError_t launch_adams_sparse(const uint32_t* idx, const float* gbar, int64_t k, float* w,
                                 float* m, const AdamsConst& c, bool msync, cudaStream_t st) {
   if (k <= 0) return cudaSuccess;
-  const unsigned grid = (unsigned)(((k + 3) / 4 + 255) / 256);
+  const unsigned grid = (unsigned)((k + 1023) / 1024);  // 1024 slots per block
   if (msync) adams_sparse_kernel<true><<<grid, 256, 0, st>>>(idx, gbar, k, w, m, c);
   else adams_sparse_kernel<false><<<grid, 256, 0, st>>>(idx, gbar, k, w, m, c);
   return cudaGetLastError();
@@ -665,7 +665,7 @@ cudaError_t launch_adams_sparse(const uint32_t* idx, const float* gbar, int64_t 
 cudaError_t launch_probe_rmw(const uint32_t* idx, const float* gbar, int64_t k, float* w,
                              float* m, cudaStream_t st) {
   if (k <= 0) return cudaSuccess;
-  const unsigned grid = (unsigned)(((k + 3) / 4 + 255) / 256);
+  const unsigned grid = (unsigned)((k + 1023) / 1024);
   probe_rmw_kernel<<<grid, 256, 0, st>>>(idx, gbar, k, w, m);
   return cudaGetLastError();
 }
