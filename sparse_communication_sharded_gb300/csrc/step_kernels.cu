@@ -435,34 +435,37 @@ __device__ __forceinline__ void sparse_update(float b, float& w, float& m, const
   else adams_update(b, w, m, c);
 }
 
-// Slots of a 256-thread block: 1024 consecutive ones; thread t takes slots
-// t, t + 256, t + 512, t + 768 of them, so that each load instruction of a
-// warp covers 32 consecutive slots (neighbouring coordinates).  Measured
-// against thread t taking slots 4t .. 4t + 3 by 16-byte loads of idx and
-// g_bar: 0.49 against 0.55 ms on the Llama-500M shape (its probe 0.51
-// against 0.57 ms), 1.17 against 1.30 ms on Llama-1.8B.
+// Slots of a 256-thread block: 256 kUpdSlots consecutive ones; thread t takes
+// slots t, t + 256, ... of them, so that each load instruction of a warp
+// covers 32 consecutive slots (neighbouring coordinates).  Measured on the
+// Llama-500M shape: 4 consecutive slots per thread by 16-byte loads of idx
+// and g_bar 0.55 ms, 4 slots 256 apart 0.49 ms on the same box; on another,
+// 1, 2, 4 and 8 slots 256 apart 0.409, 0.402, 0.421 and 0.432 ms (Llama-1.8B:
+// 0.973, 0.951, 0.996, 1.012 ms).
+constexpr int kUpdSlots = 2;  // slots per thread
+
 template <bool MSYNC>
 __global__ void __launch_bounds__(256)
 adams_sparse_kernel(const uint32_t* __restrict__ idx, const float* __restrict__ gbar, int64_t k,
                     float* __restrict__ wts, float* __restrict__ mom, AdamsConst c) {
-  const int64_t j0 = (int64_t)blockIdx.x * 1024 + threadIdx.x;
-  uint32_t ii[4];
-  float gg[4], wv[4], mv[4];
+  const int64_t j0 = (int64_t)blockIdx.x * (256 * kUpdSlots) + threadIdx.x;
+  uint32_t ii[kUpdSlots];
+  float gg[kUpdSlots], wv[kUpdSlots], mv[kUpdSlots];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < kUpdSlots; ++q) {
     const int64_t j = j0 + 256 * q;
     ii[q] = j < k ? __ldg(idx + j) : 0u;
     gg[q] = j < k ? __ldg(gbar + j) : 0.f;
   }
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < kUpdSlots; ++q) {
     if (j0 + 256 * q < k) {
       wv[q] = wts[ii[q]];
       mv[q] = mom[ii[q]];
     }
   }
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < kUpdSlots; ++q) {
     if (j0 + 256 * q < k) {
       sparse_update<MSYNC>(gg[q], wv[q], mv[q], c);
       wts[ii[q]] = wv[q];
@@ -486,25 +489,25 @@ __global__ void __launch_bounds__(256)
 probe_rmw_kernel(const uint32_t* __restrict__ idx, const float* __restrict__ gbar, int64_t k,
                  float* __restrict__ wts, float* __restrict__ mom) {
   // the same slots per thread and the same loads as adams_sparse
-  const int64_t j0 = (int64_t)blockIdx.x * 1024 + threadIdx.x;
-  uint32_t ii[4];
-  float wv[4], mv[4], gsum = 0.f;
+  const int64_t j0 = (int64_t)blockIdx.x * (256 * kUpdSlots) + threadIdx.x;
+  uint32_t ii[kUpdSlots];
+  float wv[kUpdSlots], mv[kUpdSlots], gsum = 0.f;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < kUpdSlots; ++q) {
     const int64_t j = j0 + 256 * q;
     ii[q] = j < k ? __ldg(idx + j) : 0u;
     gsum += j < k ? __ldg(gbar + j) : 0.f;
   }
   if (gsum == 1.0e30f) asm volatile("" ::: "memory");  // keep g_bar's loads
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < kUpdSlots; ++q) {
     if (j0 + 256 * q < k) {
       wv[q] = wts[ii[q]];
       mv[q] = mom[ii[q]];
     }
   }
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < kUpdSlots; ++q) {
     if (j0 + 256 * q < k) {
       st_keep(wts + ii[q], wv[q]);
       st_keep(mom + ii[q], mv[q]);
@@ -656,7 +659,7 @@ cudaError_t launch_reduce(const float* pack, int64_t pack_stride, int W, int64_t
 cudaError_t launch_adams_sparse(const uint32_t* idx, const float* gbar, int64_t k, float* w,
                                 float* m, const AdamsConst& c, bool msync, cudaStream_t st) {
   if (k <= 0) return cudaSuccess;
-  const unsigned grid = (unsigned)((k + 1023) / 1024);  // 1024 slots per block
+  const unsigned grid = (unsigned)((k + 256 * kUpdSlots - 1) / (256 * kUpdSlots));
   if (msync) adams_sparse_kernel<true><<<grid, 256, 0, st>>>(idx, gbar, k, w, m, c);
   else adams_sparse_kernel<false><<<grid, 256, 0, st>>>(idx, gbar, k, w, m, c);
   return cudaGetLastError();
@@ -665,7 +668,7 @@ cudaError_t launch_adams_sparse(const uint32_t* idx, const float* gbar, int64_t 
 cudaError_t launch_probe_rmw(const uint32_t* idx, const float* gbar, int64_t k, float* w,
                              float* m, cudaStream_t st) {
   if (k <= 0) return cudaSuccess;
-  const unsigned grid = (unsigned)((k + 1023) / 1024);
+  const unsigned grid = (unsigned)((k + 256 * kUpdSlots - 1) / (256 * kUpdSlots));
   probe_rmw_kernel<<<grid, 256, 0, st>>>(idx, gbar, k, w, m);
   return cudaGetLastError();
 }
