@@ -231,7 +231,8 @@ int scape_set_variant(scape_t *h, int flags);
  *       the residual stream).
  * Default, set by scape_create / scape_create_range from the handle's own
  * k and P: SCAPE_FUSE_UPDATE when at least 5% of the coordinates are
- * selected (20 k >= P) and not all of them, SCAPE_FUSE_SUM otherwise.
+ * selected (20 k >= P; with W <= 2 workers 0.5%: 200 k >= P) and not all of
+ * them, SCAPE_FUSE_SUM otherwise.
  * The packed buffers and g_bar are written at every level.
  * scape_get_fusion writes the current level to *level.
  * Errors: SCAPE_EINVAL for an unknown level or a NULL pointer.

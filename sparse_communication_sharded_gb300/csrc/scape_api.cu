@@ -266,11 +266,13 @@ int create_handle(scape_t** out, int n_layers, const int64_t* host_layer_numel, 
     nmax = n > nmax ? n : nmax;
     if (h->shard_k[s] != n) h->all_dense = false;
   }
-  // Default fusion level by density: from 5% of coordinates selected the
-  // update inside the compaction pass (its w and m accesses cover much of each
-  // tile's sectors) beats a separate scattered launch; below that, and when
-  // every coordinate is kept (coalesced dense update), the separate launch.
-  h->fusion = (!h->all_dense && h->k * 20 >= h->P) ? SCAPE_FUSE_UPDATE : SCAPE_FUSE_SUM;
+  // Default fusion level by density: from 5% of coordinates selected (0.5%
+  // with one or two workers, whose compaction streams little per tile) the
+  // update inside the compaction pass beats a separate scattered launch;
+  // below that, and when every coordinate is kept (coalesced dense update),
+  // the separate launch.
+  const bool fuse_update = h->k * 20 >= h->P || (W <= 2 && h->k * 200 >= h->P);
+  h->fusion = (!h->all_dense && fuse_update) ? SCAPE_FUSE_UPDATE : SCAPE_FUSE_SUM;
   P = h->P;  // from here on: the parameters this handle covers
   h->ntiles = (P + kTile - 1) / kTile;
   h->nwords = (P + 31) / 32;

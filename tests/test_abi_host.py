@@ -152,13 +152,17 @@ def test_fusion_and_staging_validate_without_gpu(lib):
                                         (4096, 4, 0.0, C.FUSE_SUM), (354871296, 8, 0.9, C.FUSE_UPDATE),
                                         (569570560, 32, 0.99, C.FUSE_SUM),
                                         (1364297728, 8, 0.99, C.FUSE_SUM), (100000, 3, 0.95, C.FUSE_UPDATE),
-                                        (100000, 3, 0.96, C.FUSE_SUM)])
+                                        (100000, 3, 0.96, C.FUSE_SUM), (4096, 1, 0.99, C.FUSE_UPDATE),
+                                        (4096, 2, 0.999, C.FUSE_SUM), (4096, 3, 0.99, C.FUSE_SUM),
+                                        (1 << 20, 1, 0.0, C.FUSE_SUM)])
 def test_default_fusion_follows_density(lib, P, W, s, want):
     """The update goes into the compaction pass from 5% of the coordinates
-    selected (20 k >= P), except when every coordinate is kept."""
+    selected (20 k >= P; 0.5% with one or two workers), except when every
+    coordinate is kept."""
     h = _create(P=P, W=W, s=s)
     k = C.scape_get_geometry(h)["k"]
-    assert (20 * k >= P and k < P) == (want == C.FUSE_UPDATE)
+    fused = 20 * k >= P or (W <= 2 and 200 * k >= P)
+    assert (fused and k < P) == (want == C.FUSE_UPDATE)
     assert C.scape_get_fusion(h) == want
     C.scape_set_fusion(h, C.FUSE_NONE)
     assert C.scape_get_fusion(h) == C.FUSE_NONE
