@@ -284,13 +284,29 @@ ef_compact_kernel(const __grid_constant__ WorkerPtrs ptrs, int W, int64_t P,
   if (!(fz.flags & kEfAccum)) return;
   // g_bar = (((p_0 + p_1) + ...) + p_{W-1}) / W and AdamS at each selected
   // coordinate ("SCAPE" Sec. II-C, Eq. 2); or the partial sum for the next group
-  if (!(fz.flags & kEfFinish)) {
-    for (int r = 0; r < __popc(byte); ++r) fz.gbar[slot0 + r] = ssum[r];
-    return;
-  }
   const float fw = (float)fz.W_total;
   if (!(fz.flags & kEfUpdate)) {
-    for (int r = 0; r < __popc(byte); ++r) fz.gbar[slot0 + r] = __fdiv_rn(ssum[r], fw);
+    const bool fin = (fz.flags & kEfFinish) != 0;
+    if (full) {
+      // eight consecutive aligned slots: two 16-byte stores (else a warp's
+      // stores would be 4 bytes at a 32-byte stride)
+      const float4* s4 = reinterpret_cast<const float4*>(ssum);
+      float4* g4 = reinterpret_cast<float4*>(fz.gbar + slot0);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float4 v = s4[h];
+        if (fin) {
+          v.x = __fdiv_rn(v.x, fw);
+          v.y = __fdiv_rn(v.y, fw);
+          v.z = __fdiv_rn(v.z, fw);
+          v.w = __fdiv_rn(v.w, fw);
+        }
+        g4[h] = v;
+      }
+    } else {
+      for (int r = 0; r < __popc(byte); ++r)
+        fz.gbar[slot0 + r] = fin ? __fdiv_rn(ssum[r], fw) : ssum[r];
+    }
     return;
   }
   cp_async_wait<0>();
