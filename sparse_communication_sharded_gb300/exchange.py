@@ -24,10 +24,40 @@ live here; every computation is a library kernel.
 """
 from __future__ import annotations
 
+from datetime import timedelta
+
 import torch
 import torch.distributed as dist
 
 from . import _scape as C
+
+
+class PeerLost(RuntimeError):
+    """A rank of the group did not reach a step; the others stop before it,
+    with none of the step's kernels or collectives launched."""
+
+    def __init__(self, missing, step):
+        self.missing = sorted(missing)
+        self.step = step
+        super().__init__(f"ranks {self.missing} did not reach step {step}")
+
+
+def check_peers(store, rank, world, step, timeout=timedelta(seconds=30)):
+    """Host-side liveness check before a step's first launch.  Every rank
+    announces `step` in the store (any torch.distributed Store, e.g. the
+    process group's) and waits at most `timeout` for the announcements of the
+    others; a rank that has left (raised, exited, never joined) is named in
+    the PeerLost raised on the others, before they launch anything."""
+    key = "scape/alive/{}/{}".format
+    store.set(key(step, rank), "1")
+    others = [q for q in range(world) if q != rank]
+    try:
+        store.wait([key(step, q) for q in others], timeout)
+    except RuntimeError as e:  # the store's timeout (DistStoreError is one)
+        missing = [q for q in others if not store.check([key(step, q)])]
+        if not missing:  # the wait failed for another reason
+            raise
+        raise PeerLost(missing, step) from e
 
 
 def _ws_view(workspace, ptr, n, dtype):
@@ -87,11 +117,17 @@ class ScapeDP:
     W            workers = optimizer shards of the whole job
     layer_numel  the layer sizes (sum P); default one layer
     group        torch.distributed process group (default: the world)
+    liveness     optional torch.distributed Store: before each step the ranks
+                 check that all of them reached it (check_peers) and raise
+                 PeerLost on the others if one has left; without it a rank
+                 that has left shows as an error of the next collective once
+                 the process group's timeout expires
     """
 
     def __init__(self, params: torch.Tensor, W: int, sparsity: float, *, layer_numel=None,
                  lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1,
-                 grad_dtype=torch.bfloat16, group=None):
+                 grad_dtype=torch.bfloat16, group=None, liveness=None,
+                 liveness_timeout=timedelta(seconds=30)):
         if not params.is_cuda or params.dtype != torch.float32 or not params.is_contiguous():
             raise ValueError("params must be a contiguous float32 CUDA tensor")
         self.group = group
@@ -122,6 +158,9 @@ class ScapeDP:
                         lay["ws_bytes"])
         self.buf = ExchangeBuffers(self.h, self.workspace, self.G)
         self.bytes_sent = 0
+        # optional store for check_peers before every step
+        self.liveness, self.liveness_timeout = liveness, liveness_timeout
+        self.steps = 0
 
     @staticmethod
     def _stream():
@@ -136,6 +175,8 @@ class ScapeDP:
         for g in grads:
             if g.dtype != self.grad_dtype or g.numel() != self.P or not g.is_cuda:
                 raise ValueError("gradient dtype/size/device mismatch")
+        if self.liveness is not None:
+            check_peers(self.liveness, self.rank, self.G, self.steps, self.liveness_timeout)
         st = self._stream()
         cnt = self.buf.counts()
         G, b = self.G, self.buf
@@ -158,6 +199,7 @@ class ScapeDP:
                 wk.wait()
         C.scape_xc_finish(self.h, st)
         self.bytes_sent += 4 * (sum(cnt["send"]) + ps + ms)
+        self.steps += 1
 
     # ----------------------------------------------------------- state views
     @property

@@ -50,7 +50,12 @@ def _run(c, rank, world, out_path):
     mine = multirank.rank_shards(W, world, rank)
     gdt = torch.bfloat16 if c["dtype"] == "bf16" else torch.float32
     params = synth.init_params(P, seed=23).to(dev)
-    opt = ScapeDP(params, W, c["s"], layer_numel=[n for _, n in wl.layers], grad_dtype=gdt, **HPV)
+    # with several ranks, every step first checks on the host that all of them
+    # reached it (check_peers over a file store)
+    live = (dist.FileStore(os.path.join(os.path.dirname(out_path), "live"), world)
+            if world > 1 else None)
+    opt = ScapeDP(params, W, c["s"], layer_numel=[n for _, n in wl.layers], grad_dtype=gdt,
+                  liveness=live, **HPV)
     assert opt.Wl == len(mine)
     gen = synth.GradientStream(wl, seed=23, device="cpu")
     bits = []
@@ -59,6 +64,7 @@ def _run(c, rank, world, out_path):
         opt.step([grads[w].to(dev) for w in mine])
         torch.cuda.synchronize()
         bits.append(opt.global_bits().cpu().numpy().view(np.uint32).copy())
+    assert opt.steps == c["steps"]
     res = {"w": params.cpu().numpy(), "m": opt.m.cpu().numpy(), "own": np.array(opt.own),
            "bits": np.stack(bits), "launches": opt.launch_count()}
     for j, w in enumerate(mine):
