@@ -525,6 +525,17 @@ int scape_xc_finish(scape_xc_t *h, void *stream);
 int scape_xc_get_state(const scape_xc_t *h, int64_t *t, const uint32_t **own_bits,
                        const uint32_t **own_idx);
 
+/* Resume after t >= 1 completed steps from a checkpoint: `global_bits` (device,
+ * ceil(P/32) words) is the global mask the next step uses -- the bitmap behind
+ * the global_bits buffer of scape_xc_buffers() when the checkpoint was taken,
+ * the same on every rank; w, m_own and the residuals are the caller's
+ * (restored by the caller before the next step).  The owned shards' part is
+ * checked (SCAPE_EINVAL if a shard does not hold exactly k_s set bits); the
+ * next refresh of the owned shards is a cold one.  Call between steps.
+ * Errors: SCAPE_EINVAL (t < 1, NULL bitmap, wrong counts), SCAPE_ESTATE (not
+ * bound, or a step in progress), SCAPE_ECUDA. */
+int scape_xc_set_state(scape_xc_t *h, int64_t t, const uint32_t *global_bits, void *stream);
+
 /* Kernel launches made through this handle. */
 int64_t scape_xc_launch_count(const scape_xc_t *h);
 

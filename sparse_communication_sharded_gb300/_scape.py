@@ -84,6 +84,7 @@ _PROTOS = {
     "scape_xc_refresh": (_i32, [_vp, _vp]),
     "scape_xc_finish": (_i32, [_vp, _vp]),
     "scape_xc_get_state": (_i32, [_vp, _vp, _vp, _vp]),
+    "scape_xc_set_state": (_i32, [_vp, _i64, _vp, _vp]),
     "scape_xc_launch_count": (_i64, [_vp]),
 }
 
@@ -424,6 +425,10 @@ def scape_xc_get_state(h):
     _xcheck(h, load().scape_xc_get_state(h, ctypes.byref(t), ctypes.byref(bits),
                                          ctypes.byref(idx)))
     return t.value, bits.value, idx.value
+
+
+def scape_xc_set_state(h, t, global_bits_ptr, stream=0):
+    _xcheck(h, load().scape_xc_set_state(h, int(t), global_bits_ptr, stream))
 
 
 def scape_xc_launch_count(h):

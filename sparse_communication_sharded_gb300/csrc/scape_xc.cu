@@ -91,6 +91,23 @@ int xcuda(scape_xc_t* h, cudaError_t e, const char* what) {
   return xfail(h, SCAPE_ECUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }
 
+// Bits [lo, lo + n) of a global bitmap moved to bit 0 of `local` (the inverse
+// of the realignment of the owned shards' words in scape_xc_refresh); bits past
+// lo + n are cleared.
+__global__ void __launch_bounds__(256)
+extract_bits_kernel(const uint32_t* __restrict__ global, int64_t nw_global, int64_t lo, int64_t n,
+                    uint32_t* __restrict__ local) {
+  const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= (n + 31) / 32) return;
+  const int64_t w0 = lo / 32 + j;
+  const int s = (int)(lo % 32);
+  uint32_t v = __ldg(global + w0) >> s;
+  if (s && w0 + 1 < nw_global) v |= __ldg(global + w0 + 1) << (32 - s);
+  const int64_t rem = n - 32 * j;  // bits of this word inside [lo, lo + n)
+  if (rem < 32) v &= (1u << rem) - 1u;
+  local[j] = v;
+}
+
 // Rebuild the global rank table and index list from the global bitmap.
 int rebuild_global(scape_xc_t* h, cudaStream_t st) {
   scape_t* o = h->own;
@@ -498,6 +515,40 @@ int scape_xc_get_state(const scape_xc_t* h, int64_t* t, const uint32_t** own_bit
   if (t) *t = h->t;
   if (own_bits) *own_bits = h->bound ? h->own->bits() : nullptr;
   if (own_idx) *own_idx = h->bound ? h->own->idx() : nullptr;
+  return SCAPE_OK;
+}
+
+int scape_xc_set_state(scape_xc_t* h, int64_t t, const uint32_t* global_bits, void* stream) {
+  if (!h) return SCAPE_EINVAL;
+  if (!h->bound) return xfail(h, SCAPE_ESTATE, "scape_xc_set_state: call scape_xc_bind first");
+  if (h->phase != 0) return xfail(h, SCAPE_ESTATE, "scape_xc_set_state: a step is in progress");
+  if (t < 1 || !global_bits)
+    return xfail(h, SCAPE_EINVAL, "scape_xc_set_state: need t >= 1 and a bitmap");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  scape_t* o = h->own;
+  const int r = h->rank;
+  const int64_t n = h->hi[r] - h->lo[r];
+  // the owned shards' words, moved to bit 0, in the (idle) mask-gather buffer
+  uint32_t* local = h->at<uint32_t>(h->off_mrecv);
+  int rc = run_kernel(o, kKXcMove, st, [&] {
+    extract_bits_kernel<<<(unsigned)(((n + 31) / 32 + 255) / 256), 256, 0, st>>>(
+        global_bits, h->nwords, h->lo[r], n, local);
+    return cudaGetLastError();
+  });
+  if (rc) return xfail(h, rc, o->err);
+  // validates the owned shards' counts and rebuilds their rank table
+  rc = scape_set_state(o, t, local, stream);
+  if (rc) {
+    h->mask_ready = false;
+    return xfail(h, rc, o->err);
+  }
+  const cudaError_t e = cudaMemcpyAsync(h->at<uint32_t>(h->off_bits), global_bits,
+                                        (size_t)h->nwords * 4, cudaMemcpyDeviceToDevice, st);
+  if (e != cudaSuccess) return xcuda(h, e, "scape_xc_set_state: copy");
+  rc = rebuild_global(h, st);
+  if (rc) return rc;
+  h->t = t;
+  h->mask_ready = true;
   return SCAPE_OK;
 }
 

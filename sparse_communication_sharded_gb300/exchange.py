@@ -211,6 +211,22 @@ class ScapeDP:
         return _ws_view(self.workspace, self.buf.ptr["global_bits"], (self.P + 31) // 32,
                         torch.int32)
 
+    def get_state(self):
+        """(t, a copy of the global mask the next step uses): with w, m and the
+        residuals, what a checkpoint needs to resume."""
+        return self.t, self.global_bits().clone()
+
+    def set_state(self, t, global_bits):
+        """Resume after t completed steps from a checkpoint's global mask (an
+        int32 CUDA tensor of ceil(P/32) words, the same on every rank); w, m
+        and the residuals are restored by the caller.  The next refresh of the
+        owned shards is a cold one."""
+        if not global_bits.is_cuda or global_bits.numel() != (self.P + 31) // 32:
+            raise ValueError("global_bits must be a CUDA tensor of ceil(P/32) words")
+        bits = global_bits.contiguous()
+        C.scape_xc_set_state(self.h, t, bits.data_ptr(), self._stream())
+        self.steps = int(t)
+
     def launch_count(self):
         return C.scape_xc_launch_count(self.h)
 

@@ -123,3 +123,75 @@ def test_exchange_step_matches_single_process_oracle(cuda_device, tmp_path, name
             if key.startswith("e"):
                 w = int(key[1:])
                 assert np.array_equal(res[key].view(np.uint32), st.e[w].view(np.uint32)), key
+
+
+def _resume_rank(rank, world, port, name, out_path, split):
+    """`split` steps, a checkpoint (w, the owned m, the local residuals, t and
+    the global mask), a fresh handle resumed from it, then the remaining
+    steps."""
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import sparse_communication_sharded_gb300 as pkg  # noqa: F401
+        from sparse_communication_sharded_gb300 import multirank
+        from sparse_communication_sharded_gb300.exchange import ScapeDP
+
+        c = CASES[name]
+        dev = torch.device("cuda:0")
+        wl = _wl(c)
+        mine = multirank.rank_shards(wl.W, world, rank)
+        gdt = torch.bfloat16 if c["dtype"] == "bf16" else torch.float32
+        kw = dict(layer_numel=[n for _, n in wl.layers], grad_dtype=gdt, **HPV)
+        gen = synth.GradientStream(wl, seed=23, device="cpu")
+        params = synth.init_params(wl.P, seed=23).to(dev)
+        opt = ScapeDP(params, wl.W, c["s"], **kw)
+        for _ in range(split):
+            grads = gen.next()
+            opt.step([grads[w].to(dev) for w in mine])
+        t, bits = opt.get_state()
+        ck = {"w": params.clone(), "m": opt.m.clone(), "e": [x.clone() for x in opt.e]}
+        opt.close()
+        # a new handle and new buffers, restored from the checkpoint
+        params2 = ck["w"].clone()
+        opt2 = ScapeDP(params2, wl.W, c["s"], **kw)
+        opt2.m.copy_(ck["m"])
+        for x, y in zip(opt2.e, ck["e"]):
+            x.copy_(y)
+        opt2.set_state(t, bits)
+        assert opt2.t == t == split
+        for _ in range(c["steps"] - split):
+            grads = gen.next()
+            opt2.step([grads[w].to(dev) for w in mine])
+        torch.cuda.synchronize()
+        res = {"w": params2.cpu().numpy(), "m": opt2.m.cpu().numpy(), "own": np.array(opt2.own),
+               "bits": opt2.global_bits().cpu().numpy().view(np.uint32).copy()}
+        for j, w in enumerate(mine):
+            res[f"e{w}"] = opt2.e[j].cpu().numpy()
+        opt2.close()
+        np.savez(out_path.format(rank=rank), **res)
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_exchange_resume_matches_uninterrupted_oracle(cuda_device, tmp_path, name):
+    """Checkpoint/resume of the multi-rank step (scape_xc_set_state): two ranks
+    stop after 3 steps, new handles resume from the checkpoint, and the end
+    state equals the oracle's uninterrupted trajectory bit for bit."""
+    c = CASES[name]
+    world = 2
+    out = str(tmp_path / "rank{rank}.npz")
+    mp.spawn(_resume_rank, args=(world, _free_port(), name, out, 3), nprocs=world, join=True)
+    st, bits = _oracle(c)
+    for r in range(world):
+        res = np.load(out.format(rank=r))
+        assert np.array_equal(res["bits"], bits[-1]), f"rank {r}: mask differs"
+        assert np.array_equal(res["w"].view(np.uint32), st.w.view(np.uint32)), f"rank {r}: w"
+        lo, hi = res["own"]
+        assert np.array_equal(res["m"].view(np.uint32), st.m[lo:hi].view(np.uint32))
+        for key in res.files:
+            if key.startswith("e"):
+                w = int(key[1:])
+                assert np.array_equal(res[key].view(np.uint32), st.e[w].view(np.uint32)), key
