@@ -75,6 +75,7 @@ class Scape:
             self.e = [torch.zeros(P, dtype=torch.float32).pin_memory() for _ in range(W)]
         else:
             raise ValueError('residuals must be "device" or "host"')
+        self._lr = float(lr)
         self.ws_bytes = C.scape_workspace_bytes(self.h)
         self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
         C.scape_bind(self.h, params.data_ptr(), self.m.data_ptr(), [x.data_ptr() for x in self.e],
@@ -148,6 +149,7 @@ class Scape:
 
     def set_lr(self, lr):
         C.scape_set_lr(self.h, lr)
+        self._lr = float(lr)
 
     def set_graphs(self, on):
         """Replay the steady warm mask refresh as a CUDA graph (default on)."""
@@ -182,6 +184,26 @@ class Scape:
 
     def set_state(self, t, bits: torch.Tensor):
         C.scape_set_state(self.h, t, bits.data_ptr(), self._stream())
+
+    def state_dict(self):
+        """What a resume needs besides the parameters, as copies: the steps
+        taken, the mask the next step uses (take it after refresh_mask), the
+        first moment, the W residuals and the learning rate."""
+        t = self.t
+        return {"t": t, "bits": self.bits().clone() if t >= 1 else None, "m": self.m.clone(),
+                "e": [x.clone() for x in self.e], "lr": self._lr}
+
+    def load_state_dict(self, sd):
+        """Restore a state_dict() into this instance (same layout; the
+        parameters are the caller's).  The next mask refresh is a cold one."""
+        if len(sd["e"]) != self.W or sd["m"].numel() != self.P:
+            raise ValueError("state_dict of another layout")
+        self.m.copy_(sd["m"])
+        for x, y in zip(self.e, sd["e"]):
+            x.copy_(y)
+        self.set_lr(sd["lr"])
+        if sd["t"] >= 1:
+            self.set_state(sd["t"], sd["bits"])
 
     # ----------------------------------------------------------- profiling
     def profile(self, on=True):

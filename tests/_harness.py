@@ -23,9 +23,9 @@ def bits_to_bool(bits: np.ndarray, lo: int, hi: int) -> np.ndarray:
     return ((bits[i // 32] >> (i % 32).astype(np.uint32)) & 1).astype(bool)
 
 
-def make_opt(params, W, s, grad_dtype):
+def make_opt(params, W, s, grad_dtype, **kw):
     return Scape(params, W, s, lr=HP.lr, beta1=HP.beta1, beta2=HP.beta2, eps=HP.eps,
-                 weight_decay=HP.weight_decay, grad_dtype=grad_dtype)
+                 weight_decay=HP.weight_decay, grad_dtype=grad_dtype, **kw)
 
 
 def assert_close_f32(got: np.ndarray, want: np.ndarray, what: str):

@@ -257,6 +257,42 @@ def test_checkpoint_resume_bit_identical(cuda_device):
     assert np.array_equal(a[3], b[3])
 
 
+def test_state_dict_round_trip(cuda_device):
+    """Scape.state_dict / load_state_dict (t, mask, m, residuals, lr) into a
+    new instance continues the trajectory bit for bit, with an lr change on
+    the way; host-resident residuals included."""
+    P, W, s = 70001, 4, 0.95
+    wl = _wl(P, W, s, "bf16")
+
+    def run(split, residuals):
+        gen = synth.GradientStream(wl, seed=9, device=cuda_device)
+        params = synth.init_params(P, seed=9, device=cuda_device)
+        opt = make_opt(params, W, s, torch.bfloat16, residuals=residuals)
+        bufs = gen.alloc()
+        for t in range(8):
+            if t == 3:
+                opt.set_lr(5e-4)
+            if t == split:
+                sd, w_ck = opt.state_dict(), params.clone()
+                opt.close()
+                params = w_ck
+                opt = make_opt(params, W, s, torch.bfloat16, residuals=residuals)
+                opt.load_state_dict(sd)
+            gen.next_into(bufs)
+            opt.step(bufs)
+            opt.refresh_mask()
+        torch.cuda.synchronize()
+        out = (u32(params), u32(opt.m), [u32(x) for x in opt.e], u32(opt.bits()))
+        opt.close()
+        return out
+
+    for residuals in ("device", "host"):
+        a, b = run(None, residuals), run(5, residuals)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]), residuals
+        assert all(np.array_equal(x, y) for x, y in zip(a[2], b[2])), residuals
+        assert np.array_equal(a[3], b[3]), residuals
+
+
 def test_resume_into_a_live_handle(cuda_device):
     """set_state on a handle that already ran another trajectory: its next
     refresh starts from thresholds of unrelated data and must still give the
