@@ -6,7 +6,9 @@
  * extreme-sparsity AdamS optimizer for sharded data parallelism.  This library
  * runs its per-step update for W data-parallel workers held as W gradient
  * slices on one GPU, so the cross-worker sparse reduce is an on-device sum and
- * no collective runs.
+ * no collective runs.  The same step split over several GPUs: shard-range
+ * handles (scape_create_range; no data-path collective) and the exchange
+ * form (scape_xc_*; the caller issues the collectives between its phases).
  *
  * Citations below name the paper ("SCAPE", Chinese translation page, sections
  * I and II-A..II-C) and the technical summary ("Sintesi Tecnica: SCAPE",
@@ -20,7 +22,8 @@
  *   - Pointers are device pointers unless the name starts with host_.
  *   - The caller owns every device buffer (parameters, first moment, residuals,
  *     gradients, workspace).  The library keeps non-owning pointers and small
- *     host metadata only; it never allocates device memory.
+ *     host metadata only; it allocates no device buffers (it creates CUDA
+ *     streams, events and, for the replayed warm refresh, a CUDA graph).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *     All GPU work is enqueued asynchronously on it; a non-zero status reports
  *     argument, state or launch errors only.  Faults of enqueued work surface
